@@ -1,0 +1,460 @@
+#!/usr/bin/env python
+"""Benchmark of the GDN layer hot path on GB300.
+
+One step = one Qwen3.5-27B-shaped GDN layer prefill of one 4096-token sequence
+(token-major, Hk=16 q/k heads, Hv=48 v heads, dk=dv=128, chunk 64): the width-4 conv1d +
+SiLU over the 10240 packed q||k||v channels, then the chunked gated delta rule with
+in-kernel q/k L2 norm.  `value` is prefill tokens/s per layer over all ranks.  The decode
+half of the metric (256 sequences, one token each, fp32 state [256,48,128,128] updated in
+place, conv update over 10240 channels) is timed in the same run and reported under
+"decode" in state GB/s against HBM.
+
+Timing: W untimed warm-up steps, then K steps bracketed by barrier + synchronize;
+per-kernel CUDA events on the launching stream (torch's current stream); L2 flushed by a
+256 MiB write between prefill steps (the decode state, 805 MB, exceeds L2 by itself);
+max over ranks.  `e2e` repeats the prefill through the public API with pinned host
+inputs copied in and the outputs (o, final state) read back inside the timed region.
+
+--impl reference times the fp64 CPU oracle on the host cores on the same workload
+(the reference arm of this project; the pages publish no implementation to run).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "GDN prefill tokens/s per layer (% bf16 TC peak); decode step state GB/s vs HBM"
+SHAPE = dict(Hk=16, Hv=48, dk=128, dv=128)
+CHUNK = 64
+
+
+def prefill_flops_per_token(Hk, Hv, dk, dv, C=CHUNK):
+    """Algorithmic FLOPs per token of the chunked scan (WY/UT form, per chunk of C):
+    KK^T and QK^T per k-head (2 x 2*C*dk per token); per v-head the C-sized products
+    Tinv*K', Tinv*V', M*Vnew (3 x 2*C*d) and the d-sized products W*S, Q*S, K^T*Vnew
+    (3 x 2*d*d); the unit-triangular solve C^2/3 per token per v-head."""
+    d = dk
+    return Hk * 2 * 2 * C * d + Hv * 2 * (3 * C * d + 3 * d * dv) + Hv * C * C / 3.0
+
+
+def prefill_bytes(T, N, Hk, Hv, dk, dv, init_state=False):
+    act = T * (2 * Hk * dk + 2 * Hv * dv) * 2 + T * Hv * 4 * 2
+    st = N * Hv * dk * dv * 4 * (2 if init_state else 1)
+    return act + st
+
+
+def conv_bytes(T, C, N, with_state=False):
+    return T * C * 2 * 2 + C * 4 * 2 + (N * 3 * C * 2 * (2 if with_state else 1))
+
+
+def decode_bytes(N, Hk, Hv, dk, dv, C):
+    state = 2 * N * Hv * dk * dv * 4
+    act = N * (2 * Hk * dk + 2 * Hv * dv) * 2 + N * Hv * 4 * 2
+    conv = N * C * 2 * 2 + 2 * N * 3 * C * 2 + C * 4 * 2
+    return state + act + conv, state
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    out = dict(FALLBACK_PEAKS)
+    src = "fallback"
+    try:
+        with open(path) as f:
+            m = json.load(f)
+
+        def find(keys):
+            for k in keys:
+                if k in m and isinstance(m[k], (int, float)):
+                    return float(m[k])
+            return None
+        hb = find(["hbm_gbs", "hbm_GBps", "hbm_copy_gbs"])
+        tf = find(["bf16_tflops", "bf16_dense_tflops"])
+        ts = find(["bf16_tflops_sustained"])
+        if hb and tf:
+            out.update(hbm_gbs=hb, bf16_tflops=tf)
+            if ts:
+                out["bf16_tflops_sustained"] = ts
+            src = "measured"
+    except (OSError, ValueError):
+        pass
+    out["source"] = src
+    return out
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                 "-i", str(self.idx), "-lms", "200"], stdout=self.file,
+                stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                for nm, val in zip(names, r[5:9]):
+                    if val.strip().lower() == "active":
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------- our arm
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import gated_deltanet_linear_11_gb300 as gdn
+    from gated_deltanet_linear_11_gb300 import build as gbuild
+    from gated_deltanet_linear_11_gb300 import inputs
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    gbuild.build()
+    gdn.load()
+    peaks = read_peaks()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    launches = 0
+
+    # ---------------- prefill workload (27B layer, one 4096-token sequence)
+    T = args.T
+    s = SHAPE
+    C = inputs.conv_channels(**s)
+    wl = inputs.layer_27b(seed=2, T=T)
+    cv = wl["conv"]
+    x = cv["x"].to(dev)
+    w = cv["w"].to(dev)
+    g = wl["g"].to(dev)
+    beta = wl["beta"].to(dev)
+    cu_h = cv["cu_seqlens"]
+    cu = cu_h.to(dev)
+    y = torch.empty_like(x)
+    conv_out = torch.empty((1, 3, C), dtype=torch.bfloat16, device=dev)
+    o = torch.empty((T, s["Hv"], s["dv"]), dtype=torch.bfloat16, device=dev)
+    hT = torch.empty((1, s["Hv"], s["dk"], s["dv"]), dtype=torch.float32, device=dev)
+    ws_bytes = gdn.gdn_chunk_prefill_workspace_size(1, T, s["Hk"], s["Hv"], 128, 128, CHUNK)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.int32, device=dev)  # 256 MiB
+    q_v, k_v, v_v = gdn.split_qkv(y, s["Hk"], s["Hv"], s["dk"], s["dv"])
+
+    def prefill_step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        gdn.gdn_conv1d_fwd(x, w, None, cu, None, conv_out, y, cu_seqlens_host=cu_h)
+        if evs:
+            evs[1].record(stream)
+        gdn.gdn_chunk_prefill(q_v, k_v, v_v, g, beta, cu, chunk=CHUNK, l2norm=True,
+                              o=o, final_state=hT, cu_seqlens_host=cu_h, workspace=ws)
+        if evs:
+            evs[2].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        prefill_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = Clocks(local).start()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        prefill_step(evs[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    clk = clocks.stop()
+    conv_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    scan_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    step_ms = [a + b for a, b in zip(conv_ms, scan_ms)]
+    launches += args.steps * (1 + args.scan_launches)
+    ms_step = max_over_ranks(statistics.mean(step_ms), world)
+    scan_avg = statistics.mean(scan_ms)
+    conv_avg = statistics.mean(conv_ms)
+    value = world * T / (ms_step * 1e-3)
+
+    flops = prefill_flops_per_token(**s) * T
+    achieved_tf = flops / (scan_avg * 1e-3) / 1e12
+    conv_b = conv_bytes(T, C, 1)
+    scan_b = prefill_bytes(T, 1, **s)
+
+    # ---------------- decode workload (256 sequences, fp32 state pool 805 MB)
+    Nd = args.decode_n
+    dd = inputs.decode_27b(seed=4, N=Nd)
+    dx = dd["conv"]["x"].to(dev)
+    dcs = dd["conv"]["conv_state"].to(dev)
+    dw = torch.empty((C, 4), dtype=torch.bfloat16, device=dev).copy_(cv["w"])
+    dq, dk_, dvv = dd["q"].to(dev), dd["k"].to(dev), dd["v"].to(dev)
+    dg, db = dd["g"].to(dev), dd["beta"].to(dev)
+    pool = dd["state_pool"].to(dev)
+    idx = dd["state_idx"].to(dev)
+    dy = torch.empty_like(dx)
+    do = torch.empty((Nd, s["Hv"], s["dv"]), dtype=torch.bfloat16, device=dev)
+    dstatus = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def decode_step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        gdn.gdn_conv1d_update(dx, dw, None, dcs, idx, dy, dstatus)
+        if evs:
+            evs[1].record(stream)
+        gdn.gdn_recurrent_decode(dq, dk_, dvv, dg, db, pool, idx, 1.0, True, do, dstatus)
+        if evs:
+            evs[2].record(stream)
+
+    for _ in range(args.warmup):
+        decode_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    devs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        decode_step(devs[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    launches += 2 * args.steps
+    dconv_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in devs)
+    ddec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in devs)
+    dstep_ms = max_over_ranks(dconv_ms + ddec_ms, world)
+    dbytes, dstate = decode_bytes(Nd, s["Hk"], s["Hv"], s["dk"], s["dv"], C)
+    dconv_b = Nd * C * 2 * 2 + 2 * Nd * 3 * C * 2
+    dec_b = dbytes - dconv_b
+    assert int(dstatus.item()) == 0
+
+    # ---------------- e2e: pinned host inputs in, outputs out, through the public API
+    hx = cv["x"].pin_memory()
+    hg = wl["g"].pin_memory()
+    hb = wl["beta"].pin_memory()
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hh = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
+    e2e_steps = max(3, min(args.steps, 10))
+
+    def e2e_step():
+        x.copy_(hx, non_blocking=True)
+        g.copy_(hg, non_blocking=True)
+        beta.copy_(hb, non_blocking=True)
+        gdn.gdn_layer_prefill(x, w, None, g, beta, cu, s["Hk"], s["Hv"], s["dk"], s["dv"],
+                              conv_state_out=conv_out, final_state=hT, y=y, o=o,
+                              cu_seqlens_host=cu_h, workspace=ws)
+        ho.copy_(o, non_blocking=True)
+        hh.copy_(hT, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    launches += e2e_steps * (1 + args.scan_launches)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    h2d = hx.numel() * 2 + hg.numel() * 4 + hb.numel() * 4
+    d2h = ho.numel() * 2 + hh.numel() * 4
+
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 (fp32 state and accumulation)",
+        "data": "synthetic (seeded; Qwen3.5-27B head shapes, random conv weights)",
+        "config": {"workload": "qwen3.5-27b GDN layer prefill, 1 seq x %d tokens, Hk=16 "
+                               "Hv=48 dk=dv=128, conv 10240 ch, chunk 64, q/k L2 norm "
+                               "in kernel" % T,
+                   "global_batch": world, "seq_len": T, "parallelism": "replicas x%d" % world,
+                   "l2": "flushed between steps (256 MiB write)"},
+        "kernels_ms": {"conv1d_fwd": conv_avg, "chunk_prefill": scan_avg},
+        "roofline": {"kernel": "chunk_prefill", "bound": "tensor", "achieved": achieved_tf,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved_tf / peaks["bf16_tflops"],
+                     "peak_source": "%s (bf16 dense burst)" % peaks["source"],
+                     "traffic": None,
+                     "algorithmic_flops_per_launch": flops,
+                     "algorithmic_bytes_per_launch": scan_b,
+                     "hbm_gbs_equiv": scan_b / (scan_avg * 1e-3) / 1e9},
+        "conv_roofline": {"bound": "hbm", "achieved": conv_b / (conv_avg * 1e-3) / 1e9,
+                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": conv_b / (conv_avg * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+        "decode": {"workload": "256 seqs x 1 token, state [256,48,128,128] fp32 in place, "
+                               "conv update 10240 ch, permuted state_idx",
+                   "ms_per_step": dstep_ms,
+                   "state_gbs": dstate / (dstep_ms * 1e-3) / 1e9,
+                   "kernels_ms": {"conv1d_update": dconv_ms, "recurrent_decode": ddec_ms},
+                   "roofline": {"kernel": "recurrent_decode", "bound": "hbm",
+                                "achieved": dec_b / (ddec_ms * 1e-3) / 1e9,
+                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": dec_b / (ddec_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                "traffic": None}},
+        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "wall_s_timed_region": t_wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(T, samples=args.cpu_samples)
+    if rank == 0:
+        print(json.dumps(result))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# -------------------------------------------------------------- oracle on the host
+
+def oracle_layer_once(T, v_heads=None):
+    import oracle
+    from gated_deltanet_linear_11_gb300 import inputs
+    wl = inputs.layer_27b(seed=2, T=T)
+    cv = wl["conv"]
+    t0 = time.perf_counter()
+    oracle.layer_prefill(cv["x"], cv["w"], None, wl["g"], wl["beta"], cv["cu_seqlens"],
+                         v_heads=v_heads, **SHAPE)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(T, samples=3):
+    import oracle
+    oracle.build()
+    times = [oracle_layer_once(T) for _ in range(samples)]
+    t = statistics.median(times)
+    return {"value": T / t, "unit": "tokens/s", "cores": oracle.default_threads(),
+            "kind": "oracle",
+            "sample": "fp64 oracle layer prefill (conv + token recurrence), the full "
+                      "%d-token 27B-shaped workload, median of %d runs" % (T, samples)}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    T = args.T
+    for _ in range(args.warmup):
+        oracle_layer_once(T)
+    times = [oracle_layer_once(T) for _ in range(args.steps)]
+    t = statistics.mean(times)
+    value = T / t
+    cores = oracle.default_threads()
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": "qwen3.5-27b GDN layer prefill, 1 seq x %d tokens, Hk=16 "
+                                  "Hv=48 dk=dv=128, conv 10240 ch, chunk 64, q/k L2 norm "
+                                  "in kernel" % T, "global_batch": 1, "seq_len": T},
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                            "kind": "oracle",
+                            "sample": "each step: the full %d-token layer prefill on the "
+                                      "fp64 oracle" % T},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--T", type=int, default=4096)
+    ap.add_argument("--decode-n", type=int, default=256)
+    ap.add_argument("--cpu-samples", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    args.scan_launches = 1
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

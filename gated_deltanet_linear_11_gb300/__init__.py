@@ -1,1 +1,211 @@
-"""GB300-native Gated DeltaNet layer hot path (placeholder; binding added with the library)."""
+"""GB300-native (sm_103a) Gated DeltaNet layer hot path.
+
+Thin Python binding over the C ABI of ``libgdn.so`` (declared in ``include/gdn.h``).
+PyTorch supplies device memory and the current CUDA stream; every step of the layer runs
+in this package's CUDA kernels.  The functions keep the C entry points' names:
+
+* :func:`gdn_conv1d_fwd`       -- prefill conv1d + SiLU over packed sequences
+* :func:`gdn_conv1d_update`    -- decode conv step on a pool of conv states
+* :func:`gdn_chunk_prefill`    -- chunked gated delta rule over packed sequences
+* :func:`gdn_recurrent_decode` -- one-token gated delta rule step on a state pool
+
+plus :func:`gdn_layer_prefill` / :func:`gdn_layer_decode`, which chain the conv and the
+scan over the packed q||k||v channels (q, k, v are strided views of the conv output;
+nothing is copied).
+
+There is no CPU fallback: without the built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import GDN_PREFILL_SIMT, GDN_QK_L2NORM, GdnError  # noqa: F401
+
+__all__ = ["gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
+           "gdn_recurrent_decode", "gdn_chunk_prefill_workspace_size",
+           "gdn_layer_prefill", "gdn_layer_decode", "GdnError", "load"]
+
+_DT = {torch.bfloat16: _lib.GDN_BF16, torch.float32: _lib.GDN_F32}
+
+
+def load():
+    """Load the CUDA library (raises when it is not built)."""
+    return _lib.load()
+
+
+def _vp(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _desc(t):
+    if t.dtype not in _DT:
+        raise TypeError("activations must be bf16 or fp32, got %s" % t.dtype)
+    if t.dim() not in (3, 4):
+        raise ValueError("activations must be [T,H,D] or [1,T,H,D]")
+    d = _lib.GdnTensor()
+    d.ptr = t.data_ptr()
+    d.ndim = t.dim()
+    d.dtype = _DT[t.dtype]
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensor must live on a CUDA device")
+
+
+def _seqlens(cu_seqlens, cu_seqlens_host):
+    """Device and host int32 copies of the offsets (a host copy avoids a sync)."""
+    if cu_seqlens_host is None:
+        cu_seqlens_host = cu_seqlens.detach().to("cpu", torch.int32).contiguous()
+    else:
+        cu_seqlens_host = cu_seqlens_host.to(torch.int32).contiguous()
+    if not cu_seqlens.is_cuda:
+        cu_seqlens = cu_seqlens.to(torch.int32).cuda()
+    cu_seqlens = cu_seqlens.to(torch.int32).contiguous()
+    return cu_seqlens, cu_seqlens_host
+
+
+def gdn_conv1d_fwd(x, w, bias, cu_seqlens, conv_state_in=None, conv_state_out=None,
+                   y=None, cu_seqlens_host=None):
+    """y = silu(conv1d(cat(conv_state, x_seq))) per sequence; returns (y, conv_state_out).
+
+    x [T, C] bf16; w [C, 4] (or [C, 1, 4]) bf16; bias [C] or None; cu_seqlens [N+1] int32;
+    conv_state_in [N, 3, C] or None (zeros); conv_state_out may be conv_state_in.
+    """
+    lib = _lib.load()
+    _need_cuda(x, w, bias, conv_state_in, conv_state_out, y)
+    T, C = x.shape
+    w = w.reshape(C, 4).contiguous()
+    cu, cu_h = _seqlens(cu_seqlens, cu_seqlens_host)
+    N = cu_h.numel() - 1
+    if y is None:
+        y = torch.empty_like(x)
+    if conv_state_out is None:
+        conv_state_out = torch.empty((N, 3, C), dtype=x.dtype, device=x.device)
+    rc = lib.gdn_conv1d_fwd(_vp(x), T, C, _vp(w), _vp(bias), _vp(cu),
+                            ctypes.c_void_p(cu_h.data_ptr()), N, _vp(conv_state_in),
+                            _vp(conv_state_out), _vp(y), _stream())
+    _lib.check(rc, "gdn_conv1d_fwd")
+    return y, conv_state_out
+
+
+def gdn_conv1d_update(x, w, bias, conv_state, state_idx=None, y=None, status=None):
+    """One-token conv step; conv_state [P, 3, C] is shifted in place.  Returns y [N, C]."""
+    lib = _lib.load()
+    _need_cuda(x, w, bias, conv_state, state_idx, y, status)
+    N, C = x.shape
+    w = w.reshape(C, 4).contiguous()
+    if y is None:
+        y = torch.empty_like(x)
+    rc = lib.gdn_conv1d_update(_vp(x), N, C, _vp(w), _vp(bias), _vp(conv_state),
+                               conv_state.shape[0], _vp(state_idx), _vp(y), _vp(status),
+                               _stream())
+    _lib.check(rc, "gdn_conv1d_update")
+    return y
+
+
+def gdn_chunk_prefill_workspace_size(N, T, Hk, Hv, dk, dv, chunk=64, simt=False):
+    lib = _lib.load()
+    return int(lib.gdn_chunk_prefill_workspace_size(N, T, Hk, Hv, dk, dv, chunk,
+                                                    GDN_PREFILL_SIMT if simt else 0))
+
+
+def gdn_chunk_prefill(q, k, v, g, beta, cu_seqlens, chunk=64, scale=1.0, l2norm=False,
+                      initial_state=None, output_final_state=True, o=None,
+                      final_state=None, simt=False, cu_seqlens_host=None, workspace=None,
+                      status=None):
+    """Chunked gated delta rule over packed sequences.  Returns (o, final_state).
+
+    q, k [T, Hk, dk]; v [T, Hv, dv] (token-major views; head-first is rejected);
+    g, beta [T, Hv] fp32; cu_seqlens [N+1]; initial_state [N, Hv, dk, dv] fp32 or None.
+    """
+    lib = _lib.load()
+    _need_cuda(q, k, v, g, beta, initial_state, o, final_state, workspace, status)
+    cu, cu_h = _seqlens(cu_seqlens, cu_seqlens_host)
+    N = cu_h.numel() - 1
+    T, Hk, dk = q.shape[-3:]
+    Hv, dv = v.shape[-2:]
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=q.device)
+    flags = (GDN_QK_L2NORM if l2norm else 0) | (GDN_PREFILL_SIMT if simt else 0)
+    ws_bytes = int(lib.gdn_chunk_prefill_workspace_size(N, T, Hk, Hv, dk, dv, chunk, flags))
+    if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    g = g.contiguous()
+    beta = beta.contiguous()
+    dq, dk_, dv_, do = _desc(q), _desc(k), _desc(v), _desc(o)
+    rc = lib.gdn_chunk_prefill(
+        ctypes.byref(dq), ctypes.byref(dk_), ctypes.byref(dv_), _vp(g), _vp(beta), _vp(cu),
+        ctypes.c_void_p(cu_h.data_ptr()), N, chunk, float(scale), flags,
+        _vp(initial_state), ctypes.byref(do), _vp(final_state), _vp(workspace),
+        ws_bytes, _vp(status), _stream())
+    _lib.check(rc, "gdn_chunk_prefill")
+    return o, final_state
+
+
+def gdn_recurrent_decode(q, k, v, g, beta, state, state_idx=None, scale=1.0, l2norm=False,
+                         o=None, status=None):
+    """One token per sequence; state [P, Hv, dk, dv] fp32 updated in place.  Returns o."""
+    lib = _lib.load()
+    _need_cuda(q, k, v, g, beta, state, state_idx, o, status)
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    dq, dk_, dv_, do = _desc(q), _desc(k), _desc(v), _desc(o)
+    rc = lib.gdn_recurrent_decode(
+        ctypes.byref(dq), ctypes.byref(dk_), ctypes.byref(dv_), _vp(g.contiguous()),
+        _vp(beta.contiguous()), _vp(state), state.shape[0], _vp(state_idx), float(scale),
+        GDN_QK_L2NORM if l2norm else 0, ctypes.byref(do), _vp(status), _stream())
+    _lib.check(rc, "gdn_recurrent_decode")
+    return o
+
+
+def split_qkv(y, Hk, Hv, dk, dv):
+    """Strided [T, H, D] views of the packed q||k||v conv output (no copy)."""
+    T = y.shape[0]
+    q = y[:, : Hk * dk].unflatten(1, (Hk, dk))
+    k = y[:, Hk * dk: 2 * Hk * dk].unflatten(1, (Hk, dk))
+    v = y[:, 2 * Hk * dk: 2 * Hk * dk + Hv * dv].unflatten(1, (Hv, dv))
+    assert q.shape[0] == T
+    return q, k, v
+
+
+def gdn_layer_prefill(x_qkv, conv_w, conv_bias, g, beta, cu_seqlens, Hk, Hv, dk, dv,
+                      conv_state_in=None, conv_state_out=None, initial_state=None,
+                      final_state=None, scale=1.0, chunk=64, l2norm=True, y=None, o=None,
+                      cu_seqlens_host=None, workspace=None):
+    """conv1d + SiLU over packed q||k||v, then the chunked scan with in-kernel q/k L2 norm.
+
+    Returns (o [T, Hv, dv], final_state [N, Hv, dk, dv], conv_state_out [N, 3, C]).
+    """
+    cu, cu_h = _seqlens(cu_seqlens, cu_seqlens_host)
+    y, conv_state_out = gdn_conv1d_fwd(x_qkv, conv_w, conv_bias, cu, conv_state_in,
+                                       conv_state_out, y, cu_seqlens_host=cu_h)
+    q, k, v = split_qkv(y, Hk, Hv, dk, dv)
+    o, final_state = gdn_chunk_prefill(q, k, v, g, beta, cu, chunk=chunk, scale=scale,
+                                       l2norm=l2norm, initial_state=initial_state, o=o,
+                                       final_state=final_state, cu_seqlens_host=cu_h,
+                                       workspace=workspace)
+    return o, final_state, conv_state_out
+
+
+def gdn_layer_decode(x_qkv, conv_w, conv_bias, g, beta, conv_state, state, Hk, Hv, dk, dv,
+                     state_idx=None, scale=1.0, l2norm=True, y=None, o=None, status=None):
+    """One-token layer step: conv update, then the recurrent step (states in place)."""
+    y = gdn_conv1d_update(x_qkv, conv_w, conv_bias, conv_state, state_idx, y, status)
+    q, k, v = split_qkv(y, Hk, Hv, dk, dv)
+    return gdn_recurrent_decode(q, k, v, g, beta, state, state_idx, scale, l2norm, o,
+                                status)

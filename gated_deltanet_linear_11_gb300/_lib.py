@@ -1,0 +1,76 @@
+"""ctypes binding of libgdn.so.  Argument marshalling only: every step runs in the CUDA
+kernels behind the C ABI declared in include/gdn.h.  There is no CPU fallback: if the
+library is missing or fails to load, every call raises."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libgdn.so")
+
+GDN_BF16, GDN_F32, GDN_I32 = 0, 1, 2
+GDN_QK_L2NORM = 0x1
+GDN_PREFILL_SIMT = 0x100
+
+STATUS = {
+    0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_LAYOUT",
+    4: "GDN_ERR_DTYPE", 5: "GDN_ERR_SEQLENS", 6: "GDN_ERR_UNSUPPORTED", 7: "GDN_ERR_CUDA",
+    8: "GDN_ERR_TIMEOUT", 9: "GDN_ERR_WORKSPACE", 10: "GDN_ERR_INDEX",
+}
+
+EXPORTS = ("gdn_status_string", "gdn_version", "gdn_conv1d_fwd", "gdn_conv1d_update",
+           "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill",
+           "gdn_recurrent_decode")
+
+
+class GdnTensor(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("ndim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("shape", ctypes.c_int64 * 4),
+                ("stride", ctypes.c_int64 * 4)]
+
+
+class GdnError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__("%s returned %s" % (where, STATUS.get(code, code)))
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libgdn.so and declare the signatures.  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError("libgdn.so not built (%s); run gated_deltanet_linear_11_gb300"
+                           ".build.build() -- there is no fallback path" % path)
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, u32, f32 = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                              ctypes.c_uint32, ctypes.c_float)
+    tp = ctypes.POINTER(GdnTensor)
+    sig = {
+        "gdn_status_string": ([i32], ctypes.c_char_p),
+        "gdn_version": ([], i32),
+        "gdn_conv1d_fwd": ([vp, i64, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp], i32),
+        "gdn_conv1d_update": ([vp, i32, i32, vp, vp, vp, i32, vp, vp, vp, vp], i32),
+        "gdn_chunk_prefill_workspace_size": ([i32, i64, i32, i32, i32, i32, i32, u32],
+                                             ctypes.c_size_t),
+        "gdn_chunk_prefill": ([tp, tp, tp, vp, vp, vp, vp, i32, i32, f32, u32, vp, tp, vp,
+                               vp, ctypes.c_size_t, vp, vp], i32),
+        "gdn_recurrent_decode": ([tp, tp, tp, vp, vp, vp, i32, vp, f32, u32, tp, vp, vp],
+                                 i32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def check(code, where):
+    if code != 0:
+        raise GdnError(code, where)

@@ -1,0 +1,210 @@
+// api.cu -- the extern "C" boundary of libgdn.so: argument validation and dispatch.
+//
+// Every entry point validates its arguments on the host and returns a gdn_status_t
+// before launching anything; nothing here allocates device memory.
+#include <string.h>
+
+#include "common.cuh"
+
+namespace {
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int elem_size(int32_t dt) { return dt == GDN_BF16 ? 2 : 4; }
+
+// Token-major activation view: [T,H,D] or [1,T,H,D]; unit element stride, head stride
+// D, token stride >= H*D and a multiple of 16 bytes, 16-byte aligned base.  A view whose
+// head stride exceeds its token stride is head-first and is rejected (no T < H guess).
+struct View {
+    void *ptr;
+    int64_t T, H, D, tok;
+    int32_t dtype;
+};
+
+gdn_status_t view_of(const gdn_tensor_t *t, View &out) {
+    if (!t || !t->ptr) return GDN_ERR_NULL;
+    int off;
+    if (t->ndim == 3) {
+        off = 0;
+    } else if (t->ndim == 4) {
+        if (t->shape[0] != 1) return GDN_ERR_LAYOUT;  // packed varlen uses B = 1
+        off = 1;
+    } else {
+        return GDN_ERR_SHAPE;
+    }
+    if (t->dtype != GDN_BF16 && t->dtype != GDN_F32) return GDN_ERR_DTYPE;
+    const int64_t T = t->shape[off], H = t->shape[off + 1], D = t->shape[off + 2];
+    const int64_t st = t->stride[off], sh = t->stride[off + 1], sd = t->stride[off + 2];
+    if (T < 0 || H <= 0 || D <= 0) return GDN_ERR_SHAPE;
+    if (T > 1 && H > 1 && sh > st) return GDN_ERR_LAYOUT;  // head-first
+    if (sd != 1 || sh != D) return GDN_ERR_LAYOUT;
+    if (T > 1 && st < H * D) return GDN_ERR_LAYOUT;
+    if ((st * elem_size(t->dtype)) % 16 != 0 || !aligned16(t->ptr)) return GDN_ERR_LAYOUT;
+    out.ptr = t->ptr;
+    out.T = T;
+    out.H = H;
+    out.D = D;
+    out.tok = T > 1 ? st : H * D;
+    out.dtype = t->dtype;
+    return GDN_OK;
+}
+
+gdn_status_t check_seqlens(const int32_t *cu, int32_t N, int64_t T, int32_t *max_len) {
+    if (!cu) return GDN_ERR_NULL;
+    if (cu[0] != 0 || (int64_t)cu[N] != T) return GDN_ERR_SEQLENS;
+    int32_t m = 0;
+    for (int32_t n = 0; n < N; ++n) {
+        if (cu[n + 1] < cu[n]) return GDN_ERR_SEQLENS;
+        m = cu[n + 1] - cu[n] > m ? cu[n + 1] - cu[n] : m;
+    }
+    *max_len = m;
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gdn_status_string(gdn_status_t s) {
+    switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_NULL: return "GDN_ERR_NULL: a required pointer is NULL";
+    case GDN_ERR_SHAPE: return "GDN_ERR_SHAPE: inconsistent sizes";
+    case GDN_ERR_LAYOUT: return "GDN_ERR_LAYOUT: head-first or unsupported strides/alignment";
+    case GDN_ERR_DTYPE: return "GDN_ERR_DTYPE: unsupported or mismatched element type";
+    case GDN_ERR_SEQLENS: return "GDN_ERR_SEQLENS: cu_seqlens must rise from 0 to T";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: no kernel for this shape";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA runtime call failed";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded device wait gave up";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace missing or too small";
+    case GDN_ERR_INDEX: return "GDN_ERR_INDEX: state index outside the pool";
+    }
+    return "GDN_ERR_UNKNOWN";
+}
+
+int32_t gdn_version(void) { return 100; }
+
+gdn_status_t gdn_conv1d_fwd(const void *x, int64_t T, int32_t C, const void *w,
+                            const void *bias, const int32_t *cu_seqlens_dev,
+                            const int32_t *cu_seqlens_host, int32_t N,
+                            const void *conv_state_in, void *conv_state_out, void *y,
+                            void *stream) {
+    if ((!x && T > 0) || !w || !cu_seqlens_dev || !cu_seqlens_host || (!y && T > 0))
+        return GDN_ERR_NULL;
+    if (N < 0 || T < 0 || C <= 0 || N > 65535) return GDN_ERR_SHAPE;
+    if (C % 8 != 0) return GDN_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(bias) || !aligned16(y) ||
+        !aligned16(conv_state_in) || !aligned16(conv_state_out))
+        return GDN_ERR_LAYOUT;
+    int32_t max_len = 0;
+    gdn_status_t s = check_seqlens(cu_seqlens_host, N, T, &max_len);
+    if (s != GDN_OK) return s;
+    if ((max_len + 15) / 16 > 65535) return GDN_ERR_SHAPE;
+    return gdn_host::launch_conv1d_fwd(x, C, w, bias, cu_seqlens_dev, N, max_len,
+                                       conv_state_in, conv_state_out, y,
+                                       (cudaStream_t)stream);
+}
+
+gdn_status_t gdn_conv1d_update(const void *x, int32_t N, int32_t C, const void *w,
+                               const void *bias, void *conv_state, int32_t P,
+                               const int32_t *state_idx, void *y, int32_t *status_dev,
+                               void *stream) {
+    if (N < 0 || C <= 0 || P < 0 || N > 65535) return GDN_ERR_SHAPE;
+    if (N == 0) return GDN_OK;
+    if (!x || !w || !conv_state || !y) return GDN_ERR_NULL;
+    if (C % 8 != 0) return GDN_ERR_UNSUPPORTED;
+    if (!state_idx && P < N) return GDN_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(bias) || !aligned16(y) ||
+        !aligned16(conv_state))
+        return GDN_ERR_LAYOUT;
+    return gdn_host::launch_conv1d_update(x, N, C, w, bias, conv_state, P, state_idx, y,
+                                          status_dev, (cudaStream_t)stream);
+}
+
+size_t gdn_chunk_prefill_workspace_size(int32_t N, int64_t T, int32_t Hk, int32_t Hv,
+                                        int32_t dk, int32_t dv, int32_t chunk,
+                                        uint32_t flags) {
+    if ((flags & GDN_PREFILL_SIMT) || !gdn_host::chunk_tc_supported(dk, dv, chunk, 0))
+        return 0;
+    return gdn_host::chunk_tc_workspace(N, T, Hk, Hv);
+}
+
+gdn_status_t gdn_chunk_prefill(const gdn_tensor_t *q, const gdn_tensor_t *k,
+                               const gdn_tensor_t *v, const float *g, const float *beta,
+                               const int32_t *cu_seqlens_dev,
+                               const int32_t *cu_seqlens_host, int32_t N, int32_t chunk,
+                               float scale, uint32_t flags, const float *initial_state,
+                               const gdn_tensor_t *o, float *final_state, void *workspace,
+                               size_t workspace_bytes, int32_t *status_dev, void *stream) {
+    View Q, K, V, O;
+    gdn_status_t s;
+    if ((s = view_of(q, Q)) != GDN_OK) return s;
+    if ((s = view_of(k, K)) != GDN_OK) return s;
+    if ((s = view_of(v, V)) != GDN_OK) return s;
+    if ((s = view_of(o, O)) != GDN_OK) return s;
+    if (!g || !beta || !cu_seqlens_dev || !cu_seqlens_host) return GDN_ERR_NULL;
+    if (N < 0 || N > 65535) return GDN_ERR_SHAPE;
+    if (K.T != Q.T || V.T != Q.T || O.T != Q.T || K.H != Q.H || K.D != Q.D ||
+        O.H != V.H || O.D != V.D)
+        return GDN_ERR_SHAPE;
+    if (V.H % Q.H != 0) return GDN_ERR_SHAPE;
+    if (Q.dtype != K.dtype || Q.dtype != V.dtype) return GDN_ERR_DTYPE;
+    if (!aligned16(initial_state) || !aligned16(final_state)) return GDN_ERR_LAYOUT;
+    int32_t max_len = 0;
+    if ((s = check_seqlens(cu_seqlens_host, N, Q.T, &max_len)) != GDN_OK) return s;
+
+    gdn_host::ScanArgs a;
+    memset(&a, 0, sizeof(a));
+    a.q = Q.ptr; a.k = K.ptr; a.v = V.ptr; a.o = O.ptr;
+    a.q_tok = Q.tok; a.k_tok = K.tok; a.v_tok = V.tok; a.o_tok = O.tok;
+    a.g = g; a.beta = beta; a.cu = cu_seqlens_dev;
+    a.h0 = initial_state; a.hT = final_state;
+    a.N = N; a.Hk = (int32_t)Q.H; a.Hv = (int32_t)V.H; a.dk = (int32_t)Q.D;
+    a.dv = (int32_t)V.D; a.chunk = chunk; a.T = Q.T; a.max_len = max_len;
+    a.scale = scale; a.flags = flags;
+    a.in_f32 = Q.dtype == GDN_F32; a.out_f32 = O.dtype == GDN_F32;
+    a.status = status_dev; a.ws = workspace; a.ws_bytes = workspace_bytes;
+    cudaStream_t st = (cudaStream_t)stream;
+
+    if (!(flags & GDN_PREFILL_SIMT) && gdn_host::chunk_tc_supported(a.dk, a.dv, chunk, a.in_f32)) {
+        const size_t need = gdn_host::chunk_tc_workspace(N, Q.T, a.Hk, a.Hv);
+        if (need > 0 && (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u)))
+            return GDN_ERR_WORKSPACE;
+        return gdn_host::launch_chunk_tc(a, cu_seqlens_host, st);
+    }
+    return gdn_host::launch_chunk_simt(a, st);
+}
+
+gdn_status_t gdn_recurrent_decode(const gdn_tensor_t *q, const gdn_tensor_t *k,
+                                  const gdn_tensor_t *v, const float *g,
+                                  const float *beta, float *state, int32_t P,
+                                  const int32_t *state_idx, float scale, uint32_t flags,
+                                  const gdn_tensor_t *o, int32_t *status_dev,
+                                  void *stream) {
+    View Q, K, V, O;
+    gdn_status_t s;
+    if ((s = view_of(q, Q)) != GDN_OK) return s;
+    if ((s = view_of(k, K)) != GDN_OK) return s;
+    if ((s = view_of(v, V)) != GDN_OK) return s;
+    if ((s = view_of(o, O)) != GDN_OK) return s;
+    if (!g || !beta || !state) return GDN_ERR_NULL;
+    if (K.T != Q.T || V.T != Q.T || O.T != Q.T || K.H != Q.H || K.D != Q.D ||
+        O.H != V.H || O.D != V.D)
+        return GDN_ERR_SHAPE;
+    if (V.H % Q.H != 0 || P < 0 || Q.T > 65535) return GDN_ERR_SHAPE;
+    if (!state_idx && P < Q.T) return GDN_ERR_SHAPE;
+    if (Q.dtype != K.dtype || Q.dtype != V.dtype) return GDN_ERR_DTYPE;
+    if (!aligned16(state)) return GDN_ERR_LAYOUT;
+    gdn_host::DecodeArgs a;
+    memset(&a, 0, sizeof(a));
+    a.q = Q.ptr; a.k = K.ptr; a.v = V.ptr; a.o = O.ptr;
+    a.q_tok = Q.tok; a.k_tok = K.tok; a.v_tok = V.tok; a.o_tok = O.tok;
+    a.g = g; a.beta = beta; a.state = state; a.idx = state_idx;
+    a.N = (int32_t)Q.T; a.P = P; a.Hk = (int32_t)Q.H; a.Hv = (int32_t)V.H;
+    a.dk = (int32_t)Q.D; a.dv = (int32_t)V.D; a.scale = scale; a.flags = flags;
+    a.in_f32 = Q.dtype == GDN_F32; a.out_f32 = O.dtype == GDN_F32;
+    a.status = status_dev;
+    return gdn_host::launch_decode(a, (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,97 @@
+// common.cuh -- small device helpers shared by the GDN kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+namespace gdn {
+
+typedef __nv_bfloat16 bf16;
+
+// 8 bf16 packed in 16 bytes <-> 8 floats.
+__device__ __forceinline__ void unpack8(const uint4 &u, float f[8]) {
+    const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 t = __bfloat1622float2(p[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ uint4 pack8(const float f[8]) {
+    uint4 u;
+    __nv_bfloat162 *p = reinterpret_cast<__nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    return u;
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<bf16>(bf16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f32<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// Record a device-side error without faulting: first writer wins.
+__device__ __forceinline__ void report(int32_t *status, int32_t code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+}  // namespace gdn
+
+// Host-side launch helpers (defined in api.cu).
+namespace gdn_host {
+gdn_status_t launch_conv1d_fwd(const void *x, int32_t C, const void *w, const void *bias,
+                               const int32_t *cu, int32_t N, int32_t max_len,
+                               const void *s_in, void *s_out, void *y, cudaStream_t st);
+gdn_status_t launch_conv1d_update(const void *x, int32_t N, int32_t C, const void *w,
+                                  const void *bias, void *state, int32_t P,
+                                  const int32_t *idx, void *y, int32_t *status,
+                                  cudaStream_t st);
+
+struct ScanArgs {
+    const void *q, *k, *v;
+    void *o;
+    int64_t q_tok, k_tok, v_tok, o_tok;  // token strides in elements
+    const float *g, *beta;
+    const int32_t *cu;       // device [N+1]
+    const float *h0;         // [N,Hv,dk,dv] or null
+    float *hT;               // [N,Hv,dk,dv] or null
+    int32_t N, Hk, Hv, dk, dv, chunk;
+    int64_t T;
+    int32_t max_len;         // longest sequence (host-computed)
+    float scale;
+    uint32_t flags;
+    int in_f32, out_f32;     // dtypes
+    int32_t *status;
+    void *ws;
+    size_t ws_bytes;
+};
+gdn_status_t launch_chunk_simt(const ScanArgs &a, cudaStream_t st);
+gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStream_t st);
+size_t chunk_tc_workspace(int32_t N, int64_t T, int32_t Hk, int32_t Hv);
+bool chunk_tc_supported(int32_t dk, int32_t dv, int32_t chunk, int in_f32);
+
+struct DecodeArgs {
+    const void *q, *k, *v;
+    void *o;
+    int64_t q_tok, k_tok, v_tok, o_tok;
+    const float *g, *beta;
+    float *state;
+    const int32_t *idx;
+    int32_t N, P, Hk, Hv, dk, dv;
+    float scale;
+    uint32_t flags;
+    int in_f32, out_f32;
+    int32_t *status;
+};
+gdn_status_t launch_decode(const DecodeArgs &a, cudaStream_t st);
+}  // namespace gdn_host

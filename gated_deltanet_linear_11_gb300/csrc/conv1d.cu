@@ -1,0 +1,183 @@
+// conv1d.cu -- width-4 causal depthwise conv1d + SiLU, prefill and one-token update.
+//
+// Source: "[Feature] Add batch invariance support to GDN_ATTN backend - #45819", Birol's
+// comment, part 3(a): conv over cat(conv_state, x), padding 0, groups = channels, SiLU of
+// the last seq_len outputs, new conv state = the last three conv inputs.
+//
+// Both kernels are HBM-bound streams: every thread owns 8 adjacent channels (one 16-byte
+// vector), so a warp moves 512 contiguous bytes per token row.  The four taps are summed
+// in one fixed order (bias, then w0..w3 oldest to newest) in fp32, so the prefill and the
+// decode update give the same bits for the same token, and no value depends on how the
+// packed batch is tiled.
+#include "common.cuh"
+
+namespace gdn {
+
+constexpr int kConvThreads = 128;   // threads per block, 8 channels each
+constexpr int kConvTile = 16;       // tokens per thread (anchored at the sequence start)
+
+struct Taps {
+    float w[8][4];
+    float b[8];
+};
+
+__device__ __forceinline__ void load_taps(Taps &tp, const bf16 *w, const bf16 *bias, int c0) {
+    const uint4 *wp = reinterpret_cast<const uint4 *>(w + (size_t)c0 * 4);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float f[8];
+        unpack8(__ldg(wp + i), f);  // channels c0+2i, c0+2i+1, 4 taps each
+        tp.w[2 * i][0] = f[0]; tp.w[2 * i][1] = f[1]; tp.w[2 * i][2] = f[2]; tp.w[2 * i][3] = f[3];
+        tp.w[2 * i + 1][0] = f[4]; tp.w[2 * i + 1][1] = f[5]; tp.w[2 * i + 1][2] = f[6]; tp.w[2 * i + 1][3] = f[7];
+    }
+    if (bias) {
+        unpack8(__ldg(reinterpret_cast<const uint4 *>(bias + c0)), tp.b);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tp.b[i] = 0.f;
+    }
+}
+
+// y = silu(b + w0*x0 + w1*x1 + w2*x2 + w3*x3), x0 oldest.  Fixed evaluation order.
+__device__ __forceinline__ uint4 conv_out(const Taps &tp, const float x0[8], const float x1[8],
+                                          const float x2[8], const float x3[8]) {
+    float r[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float z = tp.b[i];
+        z = fmaf(tp.w[i][0], x0[i], z);
+        z = fmaf(tp.w[i][1], x1[i], z);
+        z = fmaf(tp.w[i][2], x2[i], z);
+        z = fmaf(tp.w[i][3], x3[i], z);
+        r[i] = silu(z);
+    }
+    return pack8(r);
+}
+
+// grid: (ceil(C / (8*kConvThreads)), ceil(max_len / kConvTile) (>=1), N)
+__global__ void __launch_bounds__(kConvThreads)
+conv1d_fwd_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
+                  const bf16 *__restrict__ bias, const int32_t *__restrict__ cu,
+                  const bf16 *s_in, bf16 *s_out, bf16 *__restrict__ y, int C) {
+    const int n = blockIdx.z;
+    const int tile = blockIdx.y;
+    const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * 8;
+    if (c0 >= C) return;
+    const int start = cu[n];
+    const int L = cu[n + 1] - start;
+    const int t0 = tile * kConvTile;
+    if (t0 >= L && tile > 0) return;
+
+    Taps tp;
+    load_taps(tp, w, bias, c0);
+
+    // Window of the three conv inputs before token t0 (state rows when t0 - 3 + j < 0).
+    float win[3][8];
+    float old[3][8];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        const int p = t0 - 3 + j;
+        if (p >= 0) {
+            unpack8(*reinterpret_cast<const uint4 *>(x + (size_t)(start + p) * C + c0), win[j]);
+        } else if (s_in) {
+            unpack8(*reinterpret_cast<const uint4 *>(s_in + ((size_t)n * 3 + (3 + p)) * C + c0), win[j]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) win[j][i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) old[j][i] = win[j][i];
+    }
+
+    const int t1 = min(t0 + kConvTile, L);
+    for (int t = t0; t < t1; ++t) {
+        float cur[8];
+        unpack8(*reinterpret_cast<const uint4 *>(x + (size_t)(start + t) * C + c0), cur);
+        const uint4 out = conv_out(tp, win[0], win[1], win[2], cur);
+        *reinterpret_cast<uint4 *>(y + (size_t)(start + t) * C + c0) = out;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            win[0][i] = win[1][i];
+            win[1][i] = win[2][i];
+            win[2][i] = cur[i];
+        }
+    }
+
+    // The first tile of a sequence is the only reader of the old conv state, so it also
+    // writes the new one (safe when s_out == s_in).  xs = [old(3) ; x_seq]; the new state
+    // is xs[L], xs[L+1], xs[L+2].
+    if (tile == 0 && s_out) {
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            const int m = L + j;
+            uint4 val;
+            if (m < 3) {
+                val = pack8(old[m]);
+            } else {
+                val = *reinterpret_cast<const uint4 *>(x + (size_t)(start + m - 3) * C + c0);
+            }
+            *reinterpret_cast<uint4 *>(s_out + ((size_t)n * 3 + j) * C + c0) = val;
+        }
+    }
+}
+
+// grid: (ceil(C / (8*kConvThreads)), N)
+__global__ void __launch_bounds__(kConvThreads)
+conv1d_update_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
+                     const bf16 *__restrict__ bias, bf16 *state, int P,
+                     const int32_t *__restrict__ idx, bf16 *__restrict__ y, int C,
+                     int32_t *status) {
+    const int n = blockIdx.y;
+    const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * 8;
+    if (c0 >= C) return;
+    const int slot = idx ? idx[n] : n;
+    if (slot < 0 || slot >= P) {
+        if (c0 == 0) report(status, GDN_ERR_INDEX);
+        return;
+    }
+    Taps tp;
+    load_taps(tp, w, bias, c0);
+    bf16 *s = state + (size_t)slot * 3 * C + c0;
+    float s0[8], s1[8], s2[8], cur[8];
+    unpack8(*reinterpret_cast<const uint4 *>(s), s0);
+    const uint4 u1 = *reinterpret_cast<const uint4 *>(s + C);
+    const uint4 u2 = *reinterpret_cast<const uint4 *>(s + 2 * C);
+    const uint4 ux = *reinterpret_cast<const uint4 *>(x + (size_t)n * C + c0);
+    unpack8(u1, s1);
+    unpack8(u2, s2);
+    unpack8(ux, cur);
+    *reinterpret_cast<uint4 *>(y + (size_t)n * C + c0) = conv_out(tp, s0, s1, s2, cur);
+    *reinterpret_cast<uint4 *>(s) = u1;
+    *reinterpret_cast<uint4 *>(s + C) = u2;
+    *reinterpret_cast<uint4 *>(s + 2 * C) = ux;
+}
+
+}  // namespace gdn
+
+namespace gdn_host {
+
+gdn_status_t launch_conv1d_fwd(const void *x, int32_t C, const void *w, const void *bias,
+                               const int32_t *cu, int32_t N, int32_t max_len,
+                               const void *s_in, void *s_out, void *y, cudaStream_t st) {
+    if (N == 0) return GDN_OK;
+    const int tiles = max_len > 0 ? (max_len + gdn::kConvTile - 1) / gdn::kConvTile : 1;
+    dim3 grid((C / 8 + gdn::kConvThreads - 1) / gdn::kConvThreads, tiles, N);
+    gdn::conv1d_fwd_kernel<<<grid, gdn::kConvThreads, 0, st>>>(
+        (const gdn::bf16 *)x, (const gdn::bf16 *)w, (const gdn::bf16 *)bias, cu,
+        (const gdn::bf16 *)s_in, (gdn::bf16 *)s_out, (gdn::bf16 *)y, C);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status_t launch_conv1d_update(const void *x, int32_t N, int32_t C, const void *w,
+                                  const void *bias, void *state, int32_t P,
+                                  const int32_t *idx, void *y, int32_t *status,
+                                  cudaStream_t st) {
+    if (N == 0) return GDN_OK;
+    dim3 grid((C / 8 + gdn::kConvThreads - 1) / gdn::kConvThreads, N);
+    gdn::conv1d_update_kernel<<<grid, gdn::kConvThreads, 0, st>>>(
+        (const gdn::bf16 *)x, (const gdn::bf16 *)w, (const gdn::bf16 *)bias,
+        (gdn::bf16 *)state, P, idx, (gdn::bf16 *)y, C, status);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace gdn_host

@@ -1,0 +1,178 @@
+/*
+ * gdn.h -- C ABI of libgdn.so, the GB300 (sm_103a) Gated DeltaNet layer hot path.
+ *
+ * The layer (Qwen3.5-style hybrid models) is a width-4 causal depthwise conv1d with SiLU
+ * over the packed q||k||v channels, followed by the gated delta rule
+ *
+ *     S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,   o_t = scale * S_t q_t
+ *
+ * ("Qwen3.5-27B GPTQ Garbage Inference -- Root Cause Analysis", "Why abliteration failed
+ * on Qwen3.5", item 3), run as a chunked prefill over packed variable-length sequences and
+ * as a one-token recurrent decode step on fp32 state ("[Feature] Add batch invariance
+ * support to GDN_ATTN backend - #45819", Birol's comment, parts 1 and 3).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  * Activations are token-major: [T, H, D] (or [1, T, H, D]); head_first layouts are
+ *    rejected by an explicit stride check, never by a "T < H" heuristic ("Fix [Bug]:
+ *    Qwen3.5 ... FLA linear attention tensor format mismatch causes gibberish output",
+ *    Root Cause).  T = 1 and T < H are legal.
+ *  * The recurrent state is fp32 with layout [.., Hv, dk, dv]; element [i][j] is S[j][i]
+ *    (S is dv x dk), so o[j] = scale * sum_i state[i][j] q[i].
+ *  * The conv state is the three conv inputs that precede the next token, [.., 3, C],
+ *    oldest first, in the activation dtype (bf16).
+ *  * v-head h reads q/k head h / (Hv / Hk).  g and beta are per v-head, fp32 [T, Hv].
+ *  * Every device pointer is owned by the caller.  The library allocates no device or
+ *    pinned memory and keeps no global state beyond per-device cached properties and
+ *    driver entry points.  Inputs are read-only; only the documented outputs are
+ *    written.  All calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and may be issued from several host threads.
+ *  * Validation failures return before anything is launched.  Launch failures return
+ *    GDN_ERR_CUDA.  Errors found on the device (an out-of-range state index) are
+ *    written to the optional device int `status_dev` (0 untouched = OK), which the
+ *    caller reads after synchronising; the offending item is skipped, nothing faults.
+ *  * Results are batch-invariant: each sequence's outputs and states are bit-identical
+ *    whatever other sequences share the launch (the reduction order of every value
+ *    depends only on that sequence's own data and its position relative to its start).
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_NULL = 1,        /* a required pointer is NULL */
+    GDN_ERR_SHAPE = 2,       /* inconsistent sizes */
+    GDN_ERR_LAYOUT = 3,      /* head-first or otherwise unsupported strides/alignment */
+    GDN_ERR_DTYPE = 4,       /* unsupported or mismatched element type */
+    GDN_ERR_SEQLENS = 5,     /* cu_seqlens not 0 = c0 <= c1 <= ... <= cN = T */
+    GDN_ERR_UNSUPPORTED = 6, /* shape combination without a kernel */
+    GDN_ERR_CUDA = 7,        /* a CUDA runtime call failed */
+    GDN_ERR_TIMEOUT = 8,     /* a bounded device-side wait gave up (device status) */
+    GDN_ERR_WORKSPACE = 9,   /* workspace missing, too small or misaligned */
+    GDN_ERR_INDEX = 10       /* a state index outside [0, P) (device status) */
+} gdn_status_t;
+
+typedef enum { GDN_BF16 = 0, GDN_F32 = 1, GDN_I32 = 2 } gdn_dtype_t;
+
+/* Strided view of an activation tensor.  Strides are in elements.  q/k/v/o must have a
+ * unit element stride, a head stride equal to D, a token stride >= H*D that is a multiple
+ * of 16 bytes, and a 16-byte aligned base pointer. */
+typedef struct {
+    void *ptr;
+    int32_t ndim;       /* 3: [T,H,D]   4: [1,T,H,D] */
+    int32_t dtype;      /* gdn_dtype_t */
+    int64_t shape[4];
+    int64_t stride[4];
+} gdn_tensor_t;
+
+/* Flags */
+#define GDN_QK_L2NORM 0x1u /* normalise q and k per head: x / sqrt(sum x^2 + 1e-6) */
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *gdn_status_string(gdn_status_t s);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int32_t gdn_version(void);
+
+/*
+ * gdn_conv1d_fwd -- prefill conv over packed sequences.
+ * Source: "[Feature] Add batch invariance support to GDN_ATTN backend - #45819", Birol's
+ * comment, part 3(a): conv over cat(conv_state, x) with padding 0 and groups = channels,
+ * SiLU of the last seq_len outputs, new conv state = last three conv inputs.
+ *
+ *   y[t,c] = silu(bias[c] + sum_{j=0..3} w[c][j] * xs[t+j][c]),  xs = [state(3) ; x_seq]
+ *
+ * x [T, C] bf16 contiguous (device); w [C, 4] bf16; bias [C] bf16 or NULL;
+ * cu_seqlens_dev / cu_seqlens_host: the same int32 [N+1] offsets on device and host;
+ * conv_state_in [N, 3, C] bf16 or NULL (zeros: fresh prefill);
+ * conv_state_out [N, 3, C] bf16 or NULL (may equal conv_state_in: updated in place);
+ * y [T, C] bf16 contiguous.  C must be a multiple of 8; pointers 16-byte aligned.
+ * Sequences with length 0 pass their conv state through unchanged.
+ */
+gdn_status_t gdn_conv1d_fwd(const void *x, int64_t T, int32_t C, const void *w,
+                            const void *bias, const int32_t *cu_seqlens_dev,
+                            const int32_t *cu_seqlens_host, int32_t N,
+                            const void *conv_state_in, void *conv_state_out, void *y,
+                            void *stream);
+
+/*
+ * gdn_conv1d_update -- decode conv: one new token per sequence, conv state shifted in
+ * place.  Same arithmetic (and the same fp32 operation order) as gdn_conv1d_fwd for that
+ * token.  Source: the decode conv update of the same PR comment (causal_conv1d_update).
+ *
+ * x [N, C] bf16; w [C, 4]; bias [C] or NULL; conv_state [P, 3, C] bf16, in place;
+ * state_idx [N] int32 (device) or NULL for identity (then P >= N); y [N, C] bf16.
+ * Indices outside [0, P) set *status_dev = GDN_ERR_INDEX and skip that sequence.
+ */
+gdn_status_t gdn_conv1d_update(const void *x, int32_t N, int32_t C, const void *w,
+                               const void *bias, void *conv_state, int32_t P,
+                               const int32_t *state_idx, void *y, int32_t *status_dev,
+                               void *stream);
+
+/*
+ * gdn_chunk_prefill -- chunked gated delta rule over packed variable-length sequences.
+ * Source: "[Feature] Add batch invariance support to GDN_ATTN backend - #45819", Birol's
+ * comment, part 3(a) (chunk_gated_delta_rule with initial_state, output_final_state and
+ * use_qk_l2norm_in_kernel; chunk boundaries on multiples of the 64-token block) and the
+ * PR's commit message "Fixes: 2." (per-sequence chunking independent of batch geometry).
+ *
+ * q, k [T, Hk, dk]; v [T, Hv, dv]; o [T, Hv, dv] (views as described for gdn_tensor_t);
+ * g, beta [T, Hv] fp32 contiguous; cu_seqlens_dev / cu_seqlens_host int32 [N+1];
+ * initial_state [N, Hv, dk, dv] fp32 or NULL (zeros); final_state [N, Hv, dk, dv] fp32 or
+ * NULL (not written).  initial_state == final_state is allowed (updated in place).
+ * chunk: the chunk length; chunks are anchored at every sequence start, so a sequence's
+ * result never depends on its neighbours, and a continuation split at a multiple of
+ * `chunk` reproduces the unsplit run bit for bit.
+ * Kernels: q/k/v bf16 with dk = dv = 128 and chunk = 64 run on the tensor cores
+ * (tcgen05, TMEM, TMA); q/k/v bf16 or fp32 with dk = dv in {16, 32, 64, 128} and chunk in
+ * {16, 32, 64} run on a CUDA-core fp32 kernel when flags has GDN_PREFILL_SIMT or the
+ * shape has no tensor-core kernel.  Anything else returns GDN_ERR_UNSUPPORTED.
+ * workspace: device scratch of gdn_chunk_prefill_workspace_size() bytes, 256-byte
+ * aligned (may be NULL when that size is 0).
+ */
+#define GDN_PREFILL_SIMT 0x100u /* force the CUDA-core kernel */
+
+size_t gdn_chunk_prefill_workspace_size(int32_t N, int64_t T, int32_t Hk, int32_t Hv,
+                                        int32_t dk, int32_t dv, int32_t chunk,
+                                        uint32_t flags);
+
+gdn_status_t gdn_chunk_prefill(const gdn_tensor_t *q, const gdn_tensor_t *k,
+                               const gdn_tensor_t *v, const float *g, const float *beta,
+                               const int32_t *cu_seqlens_dev,
+                               const int32_t *cu_seqlens_host, int32_t N, int32_t chunk,
+                               float scale, uint32_t flags, const float *initial_state,
+                               const gdn_tensor_t *o, float *final_state, void *workspace,
+                               size_t workspace_bytes, int32_t *status_dev, void *stream);
+
+/*
+ * gdn_recurrent_decode -- one token per sequence on a pool of fp32 states, in place.
+ * Source: the decode path of "[Feature] Add batch invariance support to GDN_ATTN
+ * backend - #45819" (fused_sigmoid_gating_delta_rule_update with ssm_state_indices into
+ * the state pool; fp32 recurrent state from Birol's comment, part 1).
+ *
+ *   h <- exp(g) h;  u = beta (v - h^T k);  h <- h + k u^T;  o = scale * h^T q
+ *
+ * q, k [N, Hk, dk]; v [N, Hv, dv]; o [N, Hv, dv] (gdn_tensor_t views, T = N);
+ * g, beta [N, Hv] fp32; state [P, Hv, dk, dv] fp32, read once and written once;
+ * state_idx [N] int32 (device) or NULL for identity (then P >= N).  dk = dv = 128.
+ * Indices outside [0, P) set *status_dev = GDN_ERR_INDEX and skip that sequence.
+ */
+gdn_status_t gdn_recurrent_decode(const gdn_tensor_t *q, const gdn_tensor_t *k,
+                                  const gdn_tensor_t *v, const float *g,
+                                  const float *beta, float *state, int32_t P,
+                                  const int32_t *state_idx, float scale, uint32_t flags,
+                                  const gdn_tensor_t *o, int32_t *status_dev,
+                                  void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

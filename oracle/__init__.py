@@ -197,3 +197,51 @@ def l2_normalise(x, eps=L2NORM_EPS):
     """x / sqrt(sum x^2 + eps) over the last axis, fp64."""
     x = _f64(x)
     return x / np.sqrt((x * x).sum(-1, keepdims=True) + eps)
+
+
+# ------------------------------------------------------------------- layer helpers
+
+def round_to_bf16(a):
+    """Round fp64 values to bf16 (via fp32, round-to-nearest-even) and return fp64.
+
+    The conv output that feeds the scan is an activation in the model's compute dtype,
+    bf16 ("[Feature] Add batch invariance support to GDN_ATTN backend - #45819", Birol's
+    comment, part 1: conv state in compute dtype)."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a, np.float64)).float().to(
+        torch.bfloat16).double().numpy()
+
+
+def split_qkv(y, Hk, Hv, dk, dv):
+    T = y.shape[0]
+    q = y[:, :Hk * dk].reshape(T, Hk, dk)
+    k = y[:, Hk * dk:2 * Hk * dk].reshape(T, Hk, dk)
+    v = y[:, 2 * Hk * dk:2 * Hk * dk + Hv * dv].reshape(T, Hv, dv)
+    return q, k, v
+
+
+def layer_prefill(x, w, bias, g, beta, cu_seqlens, Hk, Hv, dk, dv, conv_state=None,
+                  initial_state=None, scale=1.0, l2norm=True, v_heads=None, nthreads=None):
+    """conv1d+SiLU over packed q||k||v (bf16 activations), then the gated delta rule.
+
+    v_heads: optional list of v-heads to evaluate (the others are skipped); the result
+    arrays then hold those heads in that order.  Returns (o, final_state, conv_state_out).
+    """
+    y, s_out = conv1d_varlen(x, w, bias, cu_seqlens, conv_state)
+    q, k, v = split_qkv(round_to_bf16(y), Hk, Hv, dk, dv)
+    g = _f64(g)
+    beta = _f64(beta)
+    h0 = _f64(initial_state)
+    if v_heads is None:
+        o, hT = gated_delta_rule(q, k, v, g, beta, cu_seqlens, scale, l2norm, h0, nthreads)
+        return o, hT, s_out
+    G = Hv // Hk
+    outs, states = [], []
+    for hv in v_heads:
+        hk = hv // G
+        o, hT = gated_delta_rule(q[:, hk:hk + 1], k[:, hk:hk + 1], v[:, hv:hv + 1],
+                                 g[:, hv:hv + 1], beta[:, hv:hv + 1], cu_seqlens, scale,
+                                 l2norm, None if h0 is None else h0[:, hv:hv + 1], nthreads)
+        outs.append(o)
+        states.append(hT)
+    return np.concatenate(outs, 1), np.concatenate(states, 1), s_out

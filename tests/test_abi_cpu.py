@@ -1,0 +1,146 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every entry point
+include/gdn.h declares, and rejects bad arguments before launching anything.
+
+The rejection tests hand the library fake device addresses; they only run where no CUDA
+device exists (validation must return first, so nothing is ever dereferenced there).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from gated_deltanet_linear_11_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
+                 "gdn_recurrent_decode", "gdn_chunk_prefill_workspace_size",
+                 "gdn_status_string", "gdn_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(_lib.EXPORTS) <= set(declared_functions())
+
+
+def test_status_strings_and_version(lib):
+    assert lib.gdn_version() >= 100
+    for code, name in _lib.STATUS.items():
+        assert lib.gdn_status_string(code).decode().startswith(name)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    saved = _lib._lib
+    _lib._lib = None
+    try:
+        with pytest.raises(RuntimeError):
+            _lib.load(str(tmp_path / "nope.so"))
+    finally:
+        _lib._lib = saved
+
+
+# ----------------------------------------------------------------- rejections (no GPU)
+
+no_gpu = pytest.mark.skipif(torch.cuda.is_available(),
+                            reason="fake device addresses are only used where no GPU exists")
+FAKE = 1 << 40  # 16-byte aligned, never dereferenced
+
+
+def desc(T, H, D, stride=None, dtype=_lib.GDN_BF16, ptr=FAKE, ndim=3):
+    d = _lib.GdnTensor()
+    d.ptr = ptr
+    d.ndim = ndim
+    d.dtype = dtype
+    shape = (T, H, D) if ndim == 3 else (1, T, H, D)
+    st = stride or (H * D, D, 1)
+    if ndim == 4:
+        st = (T * H * D,) + tuple(st)
+    for i, (a, b) in enumerate(zip(shape, st)):
+        d.shape[i] = a
+        d.stride[i] = b
+    return d
+
+
+def prefill(lib, q, k, v, o, cu, N, chunk=64, flags=0):
+    cu_arr = (ctypes.c_int32 * len(cu))(*cu)
+    return lib.gdn_chunk_prefill(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v),
+                                 FAKE, FAKE, FAKE, ctypes.cast(cu_arr, ctypes.c_void_p),
+                                 N, chunk, 1.0, flags, None, ctypes.byref(o), None, None,
+                                 0, None, None)
+
+
+@no_gpu
+def test_head_first_rejected_without_T_less_than_H_heuristic(lib):
+    T, Hk, Hv, D = 12, 16, 32, 128
+    q = desc(T, Hk, D, stride=(D, T * D, 1))          # head-first memory
+    k, v, o = desc(T, Hk, D), desc(T, Hv, D), desc(T, Hv, D)
+    assert prefill(lib, q, k, v, o, [0, T], 1) == 3   # GDN_ERR_LAYOUT
+
+
+@no_gpu
+def test_batched_4d_with_b_gt_1_rejected(lib):
+    q = desc(8, 2, 128, ndim=4)
+    q.shape[0] = 2
+    k, v, o = desc(8, 2, 128), desc(8, 2, 128), desc(8, 2, 128)
+    assert prefill(lib, q, k, v, o, [0, 8], 1) == 3
+
+
+@no_gpu
+@pytest.mark.parametrize("cu", [[1, 8], [0, 9], [0, 5, 3, 8]])
+def test_bad_cu_seqlens_rejected(lib, cu):
+    q, k, v, o = desc(8, 2, 128), desc(8, 2, 128), desc(8, 2, 128), desc(8, 2, 128)
+    assert prefill(lib, q, k, v, o, cu, len(cu) - 1) == 5
+
+
+@no_gpu
+def test_shape_and_dtype_mismatches_rejected(lib):
+    q, k, o = desc(8, 2, 128), desc(8, 2, 128), desc(8, 3, 128)
+    v = desc(8, 3, 128)
+    assert prefill(lib, q, k, v, o, [0, 8], 1) == 2            # Hv % Hk != 0
+    v = desc(8, 2, 128, dtype=_lib.GDN_F32)
+    assert prefill(lib, q, k, v, desc(8, 2, 128), [0, 8], 1) == 4
+    q2 = desc(8, 2, 128, ptr=FAKE + 2)                       # misaligned
+    assert prefill(lib, q2, k, desc(8, 2, 128), desc(8, 2, 128), [0, 8], 1) == 3
+
+
+@no_gpu
+def test_unsupported_shapes_rejected(lib):
+    q, k, v, o = desc(8, 2, 96), desc(8, 2, 96), desc(8, 2, 96), desc(8, 2, 96)
+    assert prefill(lib, q, k, v, o, [0, 8], 1) == 6
+    q, k, v, o = desc(8, 2, 64), desc(8, 2, 64), desc(8, 2, 64), desc(8, 2, 64)
+    dq = ctypes.byref
+    rc = lib.gdn_recurrent_decode(dq(q), dq(k), dq(v), FAKE, FAKE, FAKE, 8, None, 1.0, 0,
+                                  dq(o), None, None)
+    assert rc == 6
+
+
+@no_gpu
+def test_conv_rejections(lib):
+    cu = (ctypes.c_int32 * 2)(0, 8)
+    cup = ctypes.cast(cu, ctypes.c_void_p)
+    assert lib.gdn_conv1d_fwd(FAKE, 8, 12, FAKE, None, FAKE, cup, 1, None, None, FAKE,
+                              None) == 6                        # C % 8 != 0
+    assert lib.gdn_conv1d_fwd(FAKE, 8, 16, None, None, FAKE, cup, 1, None, None, FAKE,
+                              None) == 1                        # no weights
+    assert lib.gdn_conv1d_update(FAKE, 4, 16, FAKE, None, FAKE, 2, None, FAKE, None,
+                                 None) == 2                     # P < N without indices

@@ -1,0 +1,253 @@
+"""GPU parity: every entry point of libgdn.so against the fp64 oracle, through the C ABI.
+
+Sizes are small enough for the oracle to finish in seconds but span several chunks,
+several conv tiles and ragged tails.  Tolerances live in tests/gpu_util.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_linear_11_gb300 import inputs
+from gpu_util import (OUT_ATOL_F32, STATE_RTOL_F32, assert_bits_equal, assert_out_close,
+                      assert_state_close, np64)
+
+pytestmark = pytest.mark.gpu
+
+gdn = pytest.importorskip("gated_deltanet_linear_11_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gdn.load()
+
+
+def cuda(d):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+# ----------------------------------------------------------------------------- conv
+
+@pytest.mark.parametrize("with_state,with_bias", [(False, False), (True, True)])
+def test_conv1d_fwd_parity(with_state, with_bias):
+    lens = [1, 2, 3, 15, 16, 17, 100]
+    C = 1024 + 8 * 3
+    d = inputs.conv_inputs(21, lens, C, with_state=with_state, with_bias=with_bias)
+    x, w, b, st, cu = (d["x"].cuda(), d["w"].cuda(),
+                       None if d["bias"] is None else d["bias"].cuda(),
+                       None if d["conv_state"] is None else d["conv_state"].cuda(),
+                       d["cu_seqlens"])
+    y, s_out = gdn.gdn_conv1d_fwd(x, w, b, cu.cuda(), st, None, cu_seqlens_host=cu)
+    yr, sr = oracle.conv1d_varlen(d["x"], d["w"], d["bias"], cu, d["conv_state"])
+    assert_out_close(y, yr, what="conv y")
+    # tails are copies of inputs: bit-exact
+    np.testing.assert_array_equal(np64(s_out), sr)
+
+
+def test_conv1d_fwd_in_place_state_and_empty_sequence():
+    lens = [0, 5, 0, 40]
+    C = 256
+    d = inputs.conv_inputs(22, lens, C, with_state=True)
+    st = d["conv_state"].cuda()
+    cu = d["cu_seqlens"]
+    y, s_out = gdn.gdn_conv1d_fwd(d["x"].cuda(), d["w"].cuda(), None, cu.cuda(), st, st,
+                                  cu_seqlens_host=cu)
+    assert s_out.data_ptr() == st.data_ptr()
+    yr, sr = oracle.conv1d_varlen(d["x"], d["w"], None, cu, d["conv_state"])
+    assert_out_close(y, yr, what="conv y")
+    np.testing.assert_array_equal(np64(st), sr)
+
+
+def test_conv1d_update_matches_oracle_and_prefill_bits():
+    N, P, C = 12, 20, 1024
+    d = inputs.conv_inputs(23, [1] * N, C, with_state=True, with_bias=True)
+    pool = torch.randn(P, 3, C, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    idx = torch.randperm(P, generator=torch.Generator().manual_seed(6))[:N].to(torch.int32)
+    pool_gpu = pool.cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = gdn.gdn_conv1d_update(d["x"].cuda(), d["w"].cuda(), d["bias"].cuda(), pool_gpu,
+                              idx.cuda(), status=status)
+    yr, pr = oracle.conv1d_update(d["x"], d["w"], d["bias"], pool, idx)
+    assert int(status.item()) == 0
+    assert_out_close(y, yr, what="conv update y")
+    np.testing.assert_array_equal(np64(pool_gpu), pr)
+    # The decode step is the prefill conv for one token: same bits.
+    cu = torch.arange(N + 1, dtype=torch.int32)
+    y2, _ = gdn.gdn_conv1d_fwd(d["x"].cuda(), d["w"].cuda(), d["bias"].cuda(), cu.cuda(),
+                               pool[idx.long()].contiguous().cuda(), None, cu_seqlens_host=cu)
+    assert_bits_equal(y, y2, "conv update vs prefill conv")
+
+
+def test_conv1d_update_bad_index_reports_status():
+    N, P, C = 4, 4, 64
+    x = torch.randn(N, C, device="cuda").to(torch.bfloat16)
+    w = torch.rand(C, 4, device="cuda").to(torch.bfloat16)
+    pool = torch.zeros(P, 3, C, device="cuda", dtype=torch.bfloat16)
+    idx = torch.tensor([0, 1, 7, 2], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gdn.gdn_conv1d_update(x, w, None, pool, idx, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 10  # GDN_ERR_INDEX; the other sequences still ran
+    assert pool[[0, 1, 2], 2].abs().sum().item() > 0
+
+
+# --------------------------------------------------------------------------- decode
+
+@pytest.mark.parametrize("l2norm", [False, True])
+def test_recurrent_decode_parity(l2norm):
+    N, P, Hk, Hv, d = 8, 11, 2, 6, 128
+    x = inputs.scan_inputs(31, [1] * N, Hk, Hv, d, d, normalise_qk=not l2norm)
+    pool = (torch.randn(P, Hv, d, d, generator=torch.Generator().manual_seed(3)) * 0.02)
+    idx = torch.tensor([3, 0, 10, 5, 7, 1, 9, 2], dtype=torch.int32)
+    pool_gpu = pool.cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = gdn.gdn_recurrent_decode(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(),
+                                 x["g"].cuda(), x["beta"].cuda(), pool_gpu, idx.cuda(),
+                                 scale=0.75, l2norm=l2norm, status=status)
+    o_ref, pool_ref = oracle.recurrent_decode(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                                              pool, idx, scale=0.75, l2norm=l2norm)
+    assert int(status.item()) == 0
+    assert_out_close(o, o_ref)
+    assert_state_close(pool_gpu, pool_ref)
+
+
+def test_recurrent_decode_fp32_tight():
+    N, Hk, Hv, d = 3, 1, 2, 128
+    x = inputs.scan_inputs(32, [1] * N, Hk, Hv, d, d, dtype=torch.float32)
+    pool = torch.randn(N, Hv, d, d, generator=torch.Generator().manual_seed(4)) * 0.02
+    pool_gpu = pool.cuda()
+    o = gdn.gdn_recurrent_decode(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(),
+                                 x["g"].cuda(), x["beta"].cuda(), pool_gpu)
+    o_ref, pool_ref = oracle.recurrent_decode(x["q"], x["k"], x["v"], x["g"], x["beta"], pool)
+    assert_out_close(o, o_ref, atol=OUT_ATOL_F32)
+    assert_state_close(pool_gpu, pool_ref, rtol=STATE_RTOL_F32)
+
+
+# --------------------------------------------------------------------- chunk prefill
+
+def run_prefill(x, chunk=64, l2norm=False, simt=False, scale=1.0):
+    xg = cuda(x)
+    o, hT = gdn.gdn_chunk_prefill(xg["q"], xg["k"], xg["v"], xg["g"], xg["beta"],
+                                  xg["cu_seqlens"], chunk=chunk, scale=scale, l2norm=l2norm,
+                                  initial_state=xg["initial_state"], simt=simt,
+                                  cu_seqlens_host=x["cu_seqlens"])
+    return o, hT
+
+
+def ref_prefill(x, l2norm=False, scale=1.0):
+    return oracle.gated_delta_rule(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                                   x["cu_seqlens"], scale=scale, l2norm=l2norm,
+                                   initial_state=x["initial_state"])
+
+
+def test_tiny_fp32_config():
+    """B=1, T=64, 2 heads, dk=dv=16, chunk 16, fp32."""
+    x = inputs.tiny()
+    o, hT = run_prefill(x, chunk=16)
+    o_ref, h_ref = ref_prefill(x)
+    assert_out_close(o, o_ref, atol=OUT_ATOL_F32)
+    assert_state_close(hT, h_ref, rtol=STATE_RTOL_F32)
+
+
+@pytest.mark.parametrize("d,chunk", [(16, 16), (32, 32), (64, 64), (128, 16)])
+def test_simt_fp32_shapes(d, chunk):
+    x = inputs.scan_inputs(41, [1, chunk - 1, chunk, chunk + 1, 3 * chunk + 5], 2, 4, d, d,
+                           dtype=torch.float32, g_shift=0.0, init_state_std=0.05)
+    o, hT = run_prefill(x, chunk=chunk, simt=True, scale=0.5)
+    o_ref, h_ref = ref_prefill(x, scale=0.5)
+    assert_out_close(o, o_ref, atol=OUT_ATOL_F32)
+    assert_state_close(hT, h_ref, rtol=STATE_RTOL_F32)
+
+
+@pytest.mark.parametrize("simt", [True, False])
+@pytest.mark.parametrize("l2norm", [False, True])
+def test_prefill_bf16_d128_parity(simt, l2norm):
+    lens = [1, 63, 64, 65, 200, 7]
+    x = inputs.scan_inputs(42, lens, 2, 6, 128, 128, normalise_qk=not l2norm,
+                           init_state_std=0.02)
+    o, hT = run_prefill(x, chunk=64, l2norm=l2norm, simt=simt)
+    o_ref, h_ref = ref_prefill(x, l2norm=l2norm)
+    assert_out_close(o, o_ref)
+    assert_state_close(hT, h_ref)
+
+
+@pytest.mark.parametrize("simt", [True, False])
+def test_prefill_weak_decay_long(simt):
+    """g = -softplus(N(0,1) - 3): long memory, errors carried across many chunks."""
+    x = inputs.scan_inputs(43, [777], 1, 3, 128, 128, g_shift=-3.0, init_state_std=0.02)
+    o, hT = run_prefill(x, simt=simt)
+    o_ref, h_ref = ref_prefill(x)
+    assert_out_close(o, o_ref)
+    assert_state_close(hT, h_ref)
+
+
+@pytest.mark.parametrize("simt", [True, False])
+def test_prefill_batch_invariance_bits(simt):
+    lens = [130, 1, 64, 300, 17]
+    x = inputs.scan_inputs(44, lens, 2, 4, 128, 128, init_state_std=0.02)
+    o, hT = run_prefill(x, simt=simt)
+    cu = x["cu_seqlens"]
+    for n, L in enumerate(lens):
+        s0, s1 = int(cu[n]), int(cu[n + 1])
+        solo = {k: x[k][s0:s1] for k in ("q", "k", "v", "g", "beta")}
+        solo["cu_seqlens"] = torch.tensor([0, L], dtype=torch.int32)
+        solo["initial_state"] = x["initial_state"][n:n + 1]
+        o1, h1 = run_prefill(solo, simt=simt)
+        assert_bits_equal(o[s0:s1], o1, "o of sequence %d" % n)
+        assert_bits_equal(hT[n:n + 1], h1, "state of sequence %d" % n)
+
+
+@pytest.mark.parametrize("simt", [True, False])
+def test_prefill_continuation_split_on_chunk_multiple_is_exact(simt):
+    T, tau = 333, 128
+    x = inputs.scan_inputs(45, [T], 2, 4, 128, 128, init_state_std=0.02)
+    o, hT = run_prefill(x, simt=simt)
+    a = {k: x[k][:tau] for k in ("q", "k", "v", "g", "beta")}
+    a["cu_seqlens"] = torch.tensor([0, tau], dtype=torch.int32)
+    a["initial_state"] = x["initial_state"]
+    o1, h1 = run_prefill(a, simt=simt)
+    b = {k: x[k][tau:] for k in ("q", "k", "v", "g", "beta")}
+    b["cu_seqlens"] = torch.tensor([0, T - tau], dtype=torch.int32)
+    b["initial_state"] = h1.cpu()
+    o2, h2 = run_prefill(b, simt=simt)
+    assert_bits_equal(torch.cat([o1, o2]), o, "continued o")
+    assert_bits_equal(h2, hT, "continued state")
+
+
+def test_prefill_rejects_head_first():
+    x = cuda(inputs.scan_inputs(46, [12], 16, 32, 128, 128))
+    hf = x["q"].transpose(0, 1).contiguous().transpose(0, 1)   # [T,H,D] view of [H,T,D]
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.gdn_chunk_prefill(hf, x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"])
+    assert e.value.code == 3
+    # a genuine 12-token prompt with 16/32 heads (T < H) is accepted
+    o, _ = gdn.gdn_chunk_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], x["cu_seqlens"])
+    assert torch.isfinite(o.float()).all()
+
+
+def test_layer_prefill_27b_heads_sampled():
+    """Conv over the packed 10240 q||k||v channels, then the scan with in-kernel L2 norm,
+    at the 27B head shapes on a shorter packed batch; every v-head checked."""
+    s = inputs.QWEN35_27B
+    lens = [300, 65]
+    C = inputs.conv_channels(**s)
+    cv = inputs.conv_inputs(47, lens, C, with_state=True)
+    rng = np.random.default_rng(48)
+    T = sum(lens)
+    g, beta = inputs.gates(rng, T, s["Hv"], 2.0)
+    h0 = torch.randn(len(lens), s["Hv"], 128, 128, generator=torch.Generator().manual_seed(1)) * 0.02
+    cu = cv["cu_seqlens"]
+    o, hT, st = gdn.gdn_layer_prefill(cv["x"].cuda(), cv["w"].cuda(), None, g.cuda(),
+                                      beta.cuda(), cu.cuda(), s["Hk"], s["Hv"], 128, 128,
+                                      conv_state_in=cv["conv_state"].cuda(),
+                                      initial_state=h0.cuda(), cu_seqlens_host=cu)
+    heads = list(range(0, 48, 5)) + [47]
+    o_ref, h_ref, st_ref = oracle.layer_prefill(cv["x"], cv["w"], None, g, beta, cu,
+                                                s["Hk"], s["Hv"], 128, 128,
+                                                conv_state=cv["conv_state"],
+                                                initial_state=h0, v_heads=heads)
+    assert_out_close(o[:, heads], o_ref)
+    assert_state_close(hT[:, heads], h_ref)
+    np.testing.assert_array_equal(np64(st), st_ref)
