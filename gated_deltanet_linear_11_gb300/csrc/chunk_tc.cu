@@ -1,15 +1,716 @@
-// chunk_tc.cu -- tensor-core (tcgen05 / TMEM / TMA) chunked gated delta rule.
-// Placeholder: no shape is routed here yet.
+// chunk_tc.cu -- tensor-core chunked gated delta rule for dk = dv = 128, chunk 64, bf16.
+//
+// Recurrence: "Qwen3.5-27B GPTQ Garbage Inference -- Root Cause Analysis", "Why
+// abliteration failed on Qwen3.5", item 3.  Chunk boundaries anchored at every sequence
+// start ("[Feature] Add batch invariance support to GDN_ATTN backend - #45819", Birol's
+// comment, part 3(a), and the PR's "Fixes: 2."), so nothing depends on the packed batch.
+//
+// Two kernels, both tcgen05 (MMA into TMEM, operands in 128B-swizzled shared memory fed
+// by TMA):
+//
+//  chunk_prep (one CTA per (chunk, k-head), fully parallel):
+//      P = [K;Q] K^T                                   (tcgen05, M=128 N=64 K=128)
+//    per v-head of the group, with gamma the in-chunk inclusive log-decay sums and nk, nq
+//    the L2-norm factors (1 when the flag is off):
+//      A[r][s]  = beta_r e^{gamma_r-gamma_s} nk_r nk_s (k_r.k_s)          s < r
+//      M[r][s]  = e^{gamma_r-gamma_s} nq_r nk_s (q_r.k_s)                  s <= r
+//      Tinv     = (I + A)^{-1}   (fp32, blocked forward substitution on CUDA cores)
+//      Lo       = Tinv - I,  Mt = M Tinv = M + M Lo   (tcgen05 for M Lo)
+//    and stores the 128x64 bf16 tile X = [Lo ; Mt] (already swizzled) to the workspace.
+//
+//  chunk_state (one CTA per (sequence, v-head, 64-column dv tile), walks the chunks):
+//      D1 = [K;Q] h                      (h: fp32 state in TMEM, bf16 copy as operand)
+//      R  = diag(beta) (V - diag(e^gamma nk) K h)              (fp32, CUDA cores)
+//      D2 = X R  = [Lo R ; Mt R]
+//      Vn = R + Lo R                     (identity part of Tinv applied exactly in fp32)
+//      O  = scale (diag(e^gamma nq) Q h + Mt R)
+//      h <- e^{gamma_L} h + K^T diag(e^{gamma_L-gamma} nk) Vn
+//    The last product takes diag(.)Vn as a bf16 hi + lo pair (two MMAs) so the state
+//    keeps fp32-level accuracy; q/k L2 norms and decays are per-token fp32 scalars applied
+//    outside the MMAs, so the raw bf16 inputs are the only operands that are not split.
+//
+// Every wait on an mbarrier is bounded in time; on expiry the CTA records GDN_ERR_TIMEOUT
+// in the status word, stops issuing work, frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace gdn {
+
+constexpr int kTcThreads = 128;
+constexpr int kC = 64;          // chunk
+constexpr int kD = 128;         // dk = dv
+constexpr int kDVT = 64;        // dv columns per state CTA
+constexpr uint32_t kXTile = 16384;   // bf16 [128 rows][64] swizzled
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s bound on any single wait
+
+struct TcMaps {
+    CUtensorMap q, k, v;
+};
+
+struct TcParams {
+    const float *g, *beta;
+    const int32_t *cu;
+    const float *h0;
+    float *hT;
+    bf16 *o;
+    int64_t o_tok;
+    uint8_t *ws;
+    int N, Hk, Hv;
+    float scale;
+    int l2norm;
+    int32_t *status;
+};
+
+__device__ __forceinline__ uint64_t now_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on an mbarrier phase by every thread, then a CTA-wide agreement.
+__device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
+    bool ok = tc::mbar_try_wait(bar, parity);
+    if (!ok) {
+        const uint64_t t0 = now_ns();
+        while (!(ok = tc::mbar_try_wait(bar, parity)))
+            if (now_ns() - t0 > kWaitNs) break;
+    }
+    return __syncthreads_and(ok ? 1 : 0) != 0;
+}
+
+// First chunk slot of sequence n: floor(cu[n] / 64) + n.  Distinct chunks of a packed
+// batch get distinct slots below ceil(T / 64) + N.
+__device__ __forceinline__ int slot0(const int32_t *cu, int n) { return cu[n] / kC + n; }
+
+__device__ __forceinline__ void pack_row64(uint8_t *tile, int row, const float (&v)[64]) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = v[8 * c + e];
+        *reinterpret_cast<uint4 *>(tile + tc::swz(row, c)) = pack8(f);
+    }
+}
+
+__device__ __forceinline__ void tmem_row64(uint32_t taddr, float (&v)[64]) {
+    float a[32], b[32];
+    tc::tmem_ld32(taddr, a);
+    tc::tmem_ld32(taddr + 32, b);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        v[i] = a[i];
+        v[32 + i] = b[i];
+    }
+}
+
+// Sum of squares of one 128-element bf16 row held in a K-major tile of two 64-wide
+// blocks (block stride `blk` bytes), fixed order.
+__device__ __forceinline__ float row_sumsq(const uint8_t *tile, int row, uint32_t blk) {
+    float acc = 0.f;
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            float f[8];
+            unpack8(*reinterpret_cast<const uint4 *>(tile + kb * blk + tc::swz(row, c)), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc = fmaf(f[e], f[e], acc);
+        }
+    }
+    return acc;
+}
+
+// Inclusive cumulative sum of g over the chunk by warps 0 and 1 (token r = thread r),
+// fixed order; also beta.  Writes gam[64], bet[64].  Must be called by all threads.
+__device__ __forceinline__ void chunk_gates(const TcParams &p, int t0, int L, int hv,
+                                            float *gam, float *bet, float *carry) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    float x = 0.f;
+    if (tid < kC) {
+        if (tid < L) {
+            x = p.g[(size_t)(t0 + tid) * p.Hv + hv];
+            bet[tid] = p.beta[(size_t)(t0 + tid) * p.Hv + hv];
+        } else {
+            bet[tid] = 0.f;
+        }
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (tid == 31) *carry = x;
+    }
+    __syncthreads();
+    if (tid < kC) gam[tid] = tid >= 32 ? x + *carry : x;
+    __syncthreads();
+}
+
+// ------------------------------------------------------------------ Tinv (fp32)
+// T = (I + A)^{-1} for a 64x64 strictly lower A (row stride 65), by 16x16 blocks:
+// diagonal blocks by forward substitution (one thread per column), then block rows
+// i = 1..3 from  T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.  All 128 threads call this.
+__device__ void tinv64(float (*A)[65], float (*T)[65], float (*Y)[65]) {
+    const int tid = threadIdx.x;
+    if (tid < 64) {
+        const int b = tid >> 4, j = tid & 15, o = 16 * b;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
+#pragma unroll
+        for (int r = 1; r < 16; ++r) {
+            float acc = x[r];
+#pragma unroll
+            for (int s = 0; s < r; ++s) acc = fmaf(-A[o + r][o + s], x[s], acc);
+            x[r] = acc;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) T[o + r][o + j] = x[r];
+    } else {
+        // zero the blocks above the diagonal
+        for (int e = tid - 64; e < 64 * 64; e += 64) {
+            const int r = e >> 6, c = e & 63;
+            if ((c >> 4) > (r >> 4)) T[r][c] = 0.f;
+        }
+    }
+    __syncthreads();
+    for (int i = 1; i < 4; ++i) {
+        // Y_j = sum_{k=j}^{i-1} A_ik T_kj   for j < i   (16x16 each)
+        for (int e = tid; e < i * 256; e += kTcThreads) {
+            const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+            float acc = 0.f;
+            for (int k = j; k < i; ++k) {
+#pragma unroll
+                for (int m = 0; m < 16; ++m)
+                    acc = fmaf(A[16 * i + rr][16 * k + m], T[16 * k + m][16 * j + cc], acc);
+            }
+            Y[16 * j + rr][cc] = acc;
+        }
+        __syncthreads();
+        for (int e = tid; e < i * 256; e += kTcThreads) {
+            const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+            float acc = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) acc = fmaf(T[16 * i + rr][16 * i + m], Y[16 * j + m][cc], acc);
+            T[16 * i + rr][16 * j + cc] = -acc;
+        }
+        __syncthreads();
+    }
+}
+
+// ================================================================ chunk_prep kernel
+
+struct PrepSmem {
+    uint8_t kq[32768];       // [K;Q] K-major, 2 K blocks of [128 rows][128 B]
+    uint8_t x[kXTile];       // [Lo ; M] then [Lo ; Mt]
+    float A[64][65];
+    float T[64][65];
+    float Y[64][65];
+    float gam[64], bet[64], nk[64], nq[64];
+    float carry;
+    uint64_t bar_tma, bar_mma;
+    uint32_t tmem;
+};
+
+__global__ void __launch_bounds__(kTcThreads)
+chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    PrepSmem &S = *reinterpret_cast<PrepSmem *>(
+        (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int slot = blockIdx.x, hk = blockIdx.y;
+    const int G = p.Hv / p.Hk;
+
+    // slot -> (sequence n, chunk c): the last n with slot0(n) <= slot.
+    int lo = 0, hi = p.N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (slot0(p.cu, mid) <= slot) lo = mid; else hi = mid - 1;
+    }
+    const int n = lo;
+    const int c = slot - slot0(p.cu, n);
+    const int start = p.cu[n], len = p.cu[n + 1] - start;
+    if (p.N == 0 || c < 0 || c * kC >= len) return;
+    const int t0 = start + c * kC;
+    const int L = min(kC, len - t0 + start);
+
+    if (warp == 0) {
+        tc::tmem_alloc(&S.tmem, 128);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        tc::mbar_init(&S.bar_tma, 1);
+        tc::mbar_init(&S.bar_mma, 1);
+        tc::mbar_fence_init();
+        tc::prefetch_tmap(&maps.k);
+        tc::prefetch_tmap(&maps.q);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = S.tmem;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t colP = 0, colM = 64;
+    bool ok = true;
+    uint32_t mma_phase = 0;
+
+    if (tid == 0) {
+        tc::mbar_expect_tx(&S.bar_tma, 32768);
+        tc::tma_load_3d(S.kq + 0, &maps.k, &S.bar_tma, 0, hk, t0);
+        tc::tma_load_3d(S.kq + 16384, &maps.k, &S.bar_tma, 64, hk, t0);
+        tc::tma_load_3d(S.kq + 8192, &maps.q, &S.bar_tma, 0, hk, t0);
+        tc::tma_load_3d(S.kq + 16384 + 8192, &maps.q, &S.bar_tma, 64, hk, t0);
+    }
+    ok = wait_all(&S.bar_tma, 0);
+    if (ok && tid == 0) {
+        tc::fence_after_sync();
+        constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 0);
+        const uint32_t base = tc::smem_u32(S.kq);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            tc::mma_bf16(tmem + colP, tc::sdesc(base + off, 16, 1024),
+                         tc::sdesc(base + off, 16, 1024), id, ks > 0);
+        }
+        tc::mma_commit(&S.bar_mma);
+    }
+    // L2-norm factors of this chunk's k rows (threads 0..63) and q rows (64..127)
+    if (ok) {
+        const float ss = row_sumsq(S.kq, tid, 16384);
+        const float f = p.l2norm ? rsqrtf(ss + 1e-6f) : 1.f;
+        const int r = tid & 63;
+        if (tid < 64) S.nk[r] = r < L ? f : 0.f;
+        else S.nq[r] = r < L ? f : 0.f;
+    }
+    if (ok) ok = wait_all(&S.bar_mma, mma_phase);
+    mma_phase ^= 1;
+    float P[64];
+    if (ok) {
+        tc::fence_after_sync();
+        tmem_row64(tmem + lane_off + colP, P);  // row tid: k_r.k_s (tid<64) or q_r.k_s
+    }
+
+    for (int gi = 0; gi < G && ok; ++gi) {
+        const int hv = hk * G + gi;
+        chunk_gates(p, t0, L, hv, S.gam, S.bet, &S.carry);
+        const int r = tid & 63;
+        float Mrow[64];
+        if (tid < 64) {
+            const float gr = S.gam[r], br = S.bet[r], nr = S.nk[r];
+#pragma unroll
+            for (int s = 0; s < 64; ++s)
+                S.A[r][s] = (s < r && r < L) ? br * expf(gr - S.gam[s]) * nr * S.nk[s] * P[s] : 0.f;
+        } else {
+            const float gr = S.gam[r], nr = S.nq[r];
+#pragma unroll
+            for (int s = 0; s < 64; ++s)
+                Mrow[s] = (s <= r && r < L) ? expf(gr - S.gam[s]) * nr * S.nk[s] * P[s] : 0.f;
+            pack_row64(S.x, tid, Mrow);
+        }
+        __syncthreads();
+        tinv64(S.A, S.T, S.Y);
+        uint8_t *wtile = p.ws + ((size_t)slot * p.Hv + hv) * kXTile;
+        if (tid < 64) {
+            float lrow[64];
+#pragma unroll
+            for (int t = 0; t < 64; ++t) lrow[t] = (t == r) ? 0.f : S.T[r][t];
+            pack_row64(S.x, tid, lrow);
+            // Lo rows go to the workspace as they are
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc)
+                *reinterpret_cast<uint4 *>(wtile + tc::swz(tid, cc)) =
+                    *reinterpret_cast<const uint4 *>(S.x + tc::swz(tid, cc));
+        }
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+            // D[128x64] = X[128 x 64] * Lo[64 x 64]  (B = rows 0..63 of X, MN-major)
+            constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
+            const uint32_t xb = tc::smem_u32(S.x);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16(tmem + colM, tc::sdesc(xb + ks * 32, 16, 1024),
+                             tc::sdesc(xb + ks * 2048, 8192, 1024), id, ks > 0);
+            tc::mma_commit(&S.bar_mma);
+        }
+        ok = wait_all(&S.bar_mma, mma_phase);
+        mma_phase ^= 1;
+        if (ok) {
+            tc::fence_after_sync();
+            if (tid >= 64) {
+                float mt[64];
+                tmem_row64(tmem + lane_off + colM, mt);
+#pragma unroll
+                for (int s = 0; s < 64; ++s) mt[s] += Mrow[s];   // Mt = M + M Lo
+                float f[8];
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = mt[8 * cc + e];
+                    *reinterpret_cast<uint4 *>(wtile + tc::swz(tid, cc)) = pack8(f);
+                }
+            }
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+    }
+    if (!ok && tid == 0) report(p.status, GDN_ERR_TIMEOUT);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 128);
+}
+
+// =============================================================== chunk_state kernel
+
+struct StateSmem {
+    uint8_t kq[2][32768];    // [K;Q] per stage
+    uint8_t x[2][kXTile];    // [Lo ; Mt] per stage
+    uint8_t v[2][8192];      // V tile [64 tokens][64 dv] per stage
+    uint8_t hb[16384];       // bf16 h  [128 dk rows][64 dv]  (MN-major B)
+    uint8_t rb[8192];        // bf16 R  [64 tokens][64 dv]    (MN-major B)
+    uint8_t dvh[8192];       // bf16 hi of diag(dcy) Vn
+    uint8_t dvl[8192];       // bf16 lo
+    float gam[64], bet[64], nk[64], nq[64];
+    float carry;
+    uint64_t bar_tma[2], bar_d1, bar_d2, bar_d3;
+    uint32_t tmem;
+};
+
+__device__ __forceinline__ void issue_chunk_loads(StateSmem &S, const TcMaps &maps,
+                                                  const TcParams &p, int stage, int t0,
+                                                  int hk, int hv, int j0, int slot) {
+    uint64_t *bar = &S.bar_tma[stage];
+    tc::mbar_expect_tx(bar, 32768 + 8192 + kXTile);
+    uint8_t *kq = S.kq[stage];
+    tc::tma_load_3d(kq + 0, &maps.k, bar, 0, hk, t0);
+    tc::tma_load_3d(kq + 16384, &maps.k, bar, 64, hk, t0);
+    tc::tma_load_3d(kq + 8192, &maps.q, bar, 0, hk, t0);
+    tc::tma_load_3d(kq + 16384 + 8192, &maps.q, bar, 64, hk, t0);
+    tc::tma_load_3d(S.v[stage], &maps.v, bar, j0, hv, t0);
+    const uint8_t *src = p.ws + ((size_t)slot * p.Hv + hv) * kXTile;
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(tc::smem_u32(S.x[stage])), "l"(src), "r"(kXTile),
+                    "r"(tc::smem_u32(bar)) : "memory");
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    StateSmem &S = *reinterpret_cast<StateSmem *>(
+        (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023));
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int jt = blockIdx.x, hv = blockIdx.y, n = blockIdx.z;
+    const int hk = hv / (p.Hv / p.Hk);
+    const int j0 = jt * kDVT;
+    const int start = p.cu[n], len = p.cu[n + 1] - start;
+    const int nch = (len + kC - 1) / kC;
+    const int s0 = slot0(p.cu, n);
+    const size_t hoff = ((size_t)n * p.Hv + hv) * kD * kD;
+
+    if (warp == 0) {
+        tc::tmem_alloc(&S.tmem, 256);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        tc::mbar_init(&S.bar_tma[0], 1);
+        tc::mbar_init(&S.bar_tma[1], 1);
+        tc::mbar_init(&S.bar_d1, 1);
+        tc::mbar_init(&S.bar_d2, 1);
+        tc::mbar_init(&S.bar_d3, 1);
+        tc::mbar_fence_init();
+        tc::prefetch_tmap(&maps.k);
+        tc::prefetch_tmap(&maps.q);
+        tc::prefetch_tmap(&maps.v);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = S.tmem;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t colH = 0, colD1 = 64, colD2 = 128;
+
+    // Initial state: thread i holds dk row i of the [128][64] fp32 tile.
+    {
+        float h[64];
+        if (p.h0) {
+            const float4 *src = reinterpret_cast<const float4 *>(p.h0 + hoff + (size_t)tid * kD + j0);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float4 f = src[i];
+                h[4 * i] = f.x; h[4 * i + 1] = f.y; h[4 * i + 2] = f.z; h[4 * i + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) h[i] = 0.f;
+        }
+        float a[32], b[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) { a[i] = h[i]; b[i] = h[32 + i]; }
+        tc::tmem_st32(tmem + lane_off + colH, a);
+        tc::tmem_st32(tmem + lane_off + colH + 32, b);
+        tc::tmem_wait_st();
+    }
+    if (tid == 0 && nch > 0) issue_chunk_loads(S, maps, p, 0, start, hk, hv, j0, s0);
+    tc::fence_before_sync();
+    __syncthreads();
+
+    bool ok = true;
+    const int r = tid & 63;
+    for (int c = 0; c < nch && ok; ++c) {
+        const int st = c & 1;
+        const uint32_t ph = c & 1;
+        const int t0 = start + c * kC;
+        const int L = min(kC, len - c * kC);
+        if (c > 0) {
+            ok = wait_all(&S.bar_d3, ph ^ 1);  // previous chunk's state update done
+            if (!ok) break;
+        }
+        if (tid == 0 && c + 1 < nch)
+            issue_chunk_loads(S, maps, p, st ^ 1, t0 + kC, hk, hv, j0, s0 + c + 1);
+        ok = wait_all(&S.bar_tma[st], (c >> 1) & 1);
+        if (!ok) break;
+        tc::fence_after_sync();
+
+        // per-token scalars
+        {
+            const float ss = row_sumsq(S.kq[st], tid, 16384);
+            const float f = p.l2norm ? rsqrtf(ss + 1e-6f) : 1.f;
+            if (tid < 64) S.nk[r] = r < L ? f : 0.f;
+            else S.nq[r] = r < L ? f : 0.f;
+        }
+        chunk_gates(p, t0, L, hv, S.gam, S.bet, &S.carry);
+        const float gL = S.gam[L - 1];
+
+        // h: bf16 copy for the MMA, then scale the fp32 master by e^{gamma_L}
+        {
+            float h[64];
+            tmem_row64(tmem + lane_off + colH, h);
+            pack_row64(S.hb, tid, h);
+            const float aL = expf(gL);
+            float a[32], b[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) { a[i] = aL * h[i]; b[i] = aL * h[32 + i]; }
+            tc::tmem_st32(tmem + lane_off + colH, a);
+            tc::tmem_st32(tmem + lane_off + colH + 32, b);
+            tc::tmem_wait_st();
+        }
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+            constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
+            const uint32_t kqb = tc::smem_u32(S.kq[st]), hbb = tc::smem_u32(S.hb);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16(tmem + colD1,
+                             tc::sdesc(kqb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                             tc::sdesc(hbb + ks * 2048, 8192, 1024), id, ks > 0);
+            tc::mma_commit(&S.bar_d1);
+        }
+        ok = wait_all(&S.bar_d1, ph);
+        if (!ok) break;
+        tc::fence_after_sync();
+
+        // keep = R (rows 0..63) or e^gamma nq Q h (rows 64..127), fp32
+        float keep[64];
+        {
+            float d1[64];
+            tmem_row64(tmem + lane_off + colD1, d1);
+            if (tid < 64) {
+                const float br = S.bet[r];
+                const float cr = expf(S.gam[r]) * S.nk[r];
+                const bool live = r < L;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    float vv[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(S.v[st] + tc::swz(r, cc)), vv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        keep[8 * cc + e] = live ? br * (vv[e] - cr * d1[8 * cc + e]) : 0.f;
+                }
+                pack_row64(S.rb, r, keep);
+            } else {
+                const float cq = expf(S.gam[r]) * S.nq[r];
+#pragma unroll
+                for (int j = 0; j < 64; ++j) keep[j] = cq * d1[j];
+            }
+        }
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+            constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
+            const uint32_t xb = tc::smem_u32(S.x[st]), rbb = tc::smem_u32(S.rb);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16(tmem + colD2, tc::sdesc(xb + ks * 32, 16, 1024),
+                             tc::sdesc(rbb + ks * 2048, 8192, 1024), id, ks > 0);
+            tc::mma_commit(&S.bar_d2);
+        }
+        ok = wait_all(&S.bar_d2, ph);
+        if (!ok) break;
+        tc::fence_after_sync();
+        {
+            float d2[64];
+            tmem_row64(tmem + lane_off + colD2, d2);
+            if (tid < 64) {
+                const float dc = r < L ? expf(gL - S.gam[r]) * S.nk[r] : 0.f;
+                float hi[64], lo[64];
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    const float x = dc * (keep[j] + d2[j]);
+                    const float xh = __bfloat162float(__float2bfloat16_rn(x));
+                    hi[j] = xh;
+                    lo[j] = x - xh;
+                }
+                pack_row64(S.dvh, r, hi);
+                pack_row64(S.dvl, r, lo);
+            } else if (r < L) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.o + (size_t)(t0 + r) * p.o_tok +
+                                                       (size_t)hv * kD + j0);
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = p.scale * (keep[8 * cc + e] + d2[8 * cc + e]);
+                    dst[cc] = pack8(f);
+                }
+            }
+        }
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+            constexpr uint32_t id = tc::idesc_bf16(128, 64, 1, 1);
+            const uint32_t kqb = tc::smem_u32(S.kq[st]);
+            const uint32_t hb = tc::smem_u32(S.dvh), lb = tc::smem_u32(S.dvl);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16(tmem + colH, tc::sdesc(kqb + ks * 2048, 16384, 1024),
+                             tc::sdesc(hb + ks * 2048, 8192, 1024), id, 1);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16(tmem + colH, tc::sdesc(kqb + ks * 2048, 16384, 1024),
+                             tc::sdesc(lb + ks * 2048, 8192, 1024), id, 1);
+            tc::mma_commit(&S.bar_d3);
+        }
+    }
+    if (ok && nch > 0) ok = wait_all(&S.bar_d3, (nch - 1) & 1);
+    if (ok && p.hT) {
+        tc::fence_after_sync();
+        float h[64];
+        tmem_row64(tmem + lane_off + colH, h);
+        float4 *dst = reinterpret_cast<float4 *>(p.hT + hoff + (size_t)tid * kD + j0);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            dst[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+    }
+    if (!ok && tid == 0) report(p.status, GDN_ERR_TIMEOUT);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+}  // namespace gdn
+
+// ======================================================================== host side
 
 namespace gdn_host {
 
-bool chunk_tc_supported(int32_t, int32_t, int32_t, int) { return false; }
+namespace {
 
-size_t chunk_tc_workspace(int32_t, int64_t, int32_t, int32_t) { return 0; }
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
 
-gdn_status_t launch_chunk_tc(const ScanArgs &, const int32_t *, cudaStream_t) {
-    return GDN_ERR_UNSUPPORTED;
+// [T, H, 128] bf16 token-major view -> 3-D map (d, head, token), box (64, 1, 64), 128B swizzle.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int H, int64_t tok_stride) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)gdn::kD, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)gdn::kD * 2, (cuuint64_t)tok_stride * 2};
+    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool chunk_tc_supported(int32_t dk, int32_t dv, int32_t chunk, int in_f32) {
+    return dk == gdn::kD && dv == gdn::kD && chunk == gdn::kC && !in_f32;
+}
+
+size_t chunk_tc_workspace(int32_t N, int64_t T, int32_t Hk, int32_t Hv) {
+    (void)Hk;
+    const size_t slots = (size_t)((T + gdn::kC - 1) / gdn::kC) + (size_t)N + 1;
+    return slots * (size_t)Hv * gdn::kXTile;
+}
+
+gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStream_t st) {
+    (void)cu_host;
+    if (a.N == 0) return GDN_OK;
+    if (a.out_f32) return GDN_ERR_DTYPE;
+    gdn::TcMaps maps;
+    if (!make_map(&maps.q, a.q, a.T, a.Hk, a.q_tok) || !make_map(&maps.k, a.k, a.T, a.Hk, a.k_tok) ||
+        !make_map(&maps.v, a.v, a.T, a.Hv, a.v_tok))
+        return GDN_ERR_CUDA;
+    gdn::TcParams p;
+    p.g = a.g;
+    p.beta = a.beta;
+    p.cu = a.cu;
+    p.h0 = a.h0;
+    p.hT = a.hT;
+    p.o = (gdn::bf16 *)a.o;
+    p.o_tok = a.o_tok;
+    p.ws = (uint8_t *)a.ws;
+    p.N = a.N;
+    p.Hk = a.Hk;
+    p.Hv = a.Hv;
+    p.scale = a.scale;
+    p.l2norm = (a.flags & GDN_QK_L2NORM) ? 1 : 0;
+    p.status = a.status;
+
+    const size_t prep_smem = sizeof(gdn::PrepSmem) + 1024;
+    const size_t state_smem = sizeof(gdn::StateSmem) + 1024;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(gdn::chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)prep_smem) != cudaSuccess ||
+            cudaFuncSetAttribute(gdn::chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)state_smem) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        attr_set = true;
+    }
+    const int slots = (int)((a.T + gdn::kC - 1) / gdn::kC) + a.N;
+    if (slots > 0) {
+        dim3 g1(slots, a.Hk);
+        gdn::chunk_prep_kernel<<<g1, gdn::kTcThreads, prep_smem, st>>>(maps, p);
+    }
+    dim3 g2(gdn::kD / gdn::kDVT, a.Hv, a.N);
+    gdn::chunk_state_kernel<<<g2, gdn::kTcThreads, state_smem, st>>>(maps, p);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 }  // namespace gdn_host

@@ -14,7 +14,8 @@
 namespace gdn {
 
 constexpr int kConvThreads = 128;   // threads per block, 8 channels each
-constexpr int kConvTile = 16;       // tokens per thread (anchored at the sequence start)
+constexpr int kConvTile = 32;       // tokens per thread (anchored at the sequence start)
+constexpr int kConvGroup = 4;       // tokens loaded together; the next group is in flight
 
 struct Taps {
     float w[8][4];
@@ -55,7 +56,7 @@ __device__ __forceinline__ uint4 conv_out(const Taps &tp, const float x0[8], con
 }
 
 // grid: (ceil(C / (8*kConvThreads)), ceil(max_len / kConvTile) (>=1), N)
-__global__ void __launch_bounds__(kConvThreads)
+__global__ void __launch_bounds__(kConvThreads, 4)
 conv1d_fwd_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
                   const bf16 *__restrict__ bias, const int32_t *__restrict__ cu,
                   const bf16 *s_in, bf16 *s_out, bf16 *__restrict__ y, int C) {
@@ -73,7 +74,6 @@ conv1d_fwd_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
 
     // Window of the three conv inputs before token t0 (state rows when t0 - 3 + j < 0).
     float win[3][8];
-    float old[3][8];
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
         const int p = t0 - 3 + j;
@@ -85,36 +85,53 @@ conv1d_fwd_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
 #pragma unroll
             for (int i = 0; i < 8; ++i) win[j][i] = 0.f;
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) old[j][i] = win[j][i];
     }
 
-    const int t1 = min(t0 + kConvTile, L);
-    for (int t = t0; t < t1; ++t) {
-        float cur[8];
-        unpack8(*reinterpret_cast<const uint4 *>(x + (size_t)(start + t) * C + c0), cur);
-        const uint4 out = conv_out(tp, win[0], win[1], win[2], cur);
-        *reinterpret_cast<uint4 *>(y + (size_t)(start + t) * C + c0) = out;
+    // Tokens are processed in groups of kConvGroup; the loads of group g+1 are issued
+    // before group g is computed, so a thread always has a group of rows in flight.
+    const int cnt = min(kConvTile, L - t0);
+    uint4 cur_g[kConvGroup], nxt_g[kConvGroup];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            win[0][i] = win[1][i];
-            win[1][i] = win[2][i];
-            win[2][i] = cur[i];
+    for (int i = 0; i < kConvGroup; ++i)
+        if (i < cnt) cur_g[i] = *reinterpret_cast<const uint4 *>(x + (size_t)(start + t0 + i) * C + c0);
+#pragma unroll 1
+    for (int base = 0; base < cnt; base += kConvGroup) {
+        const int nb = base + kConvGroup;
+#pragma unroll
+        for (int i = 0; i < kConvGroup; ++i)
+            if (nb + i < cnt)
+                nxt_g[i] = *reinterpret_cast<const uint4 *>(x + (size_t)(start + t0 + nb + i) * C + c0);
+#pragma unroll
+        for (int i = 0; i < kConvGroup; ++i) {
+            if (base + i < cnt) {
+                float cur[8];
+                unpack8(cur_g[i], cur);
+                const uint4 out = conv_out(tp, win[0], win[1], win[2], cur);
+                *reinterpret_cast<uint4 *>(y + (size_t)(start + t0 + base + i) * C + c0) = out;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    win[0][e] = win[1][e];
+                    win[1][e] = win[2][e];
+                    win[2][e] = cur[e];
+                }
+            }
         }
+#pragma unroll
+        for (int i = 0; i < kConvGroup; ++i) cur_g[i] = nxt_g[i];
     }
 
     // The first tile of a sequence is the only reader of the old conv state, so it also
-    // writes the new one (safe when s_out == s_in).  xs = [old(3) ; x_seq]; the new state
-    // is xs[L], xs[L+1], xs[L+2].
+    // writes the new one.  xs = [old(3) ; x_seq]; the new state is xs[L], xs[L+1],
+    // xs[L+2].  Row j is written after old row L+j >= j was read, so s_out == s_in is safe.
     if (tile == 0 && s_out) {
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
             const int m = L + j;
-            uint4 val;
-            if (m < 3) {
-                val = pack8(old[m]);
-            } else {
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (m >= 3) {
                 val = *reinterpret_cast<const uint4 *>(x + (size_t)(start + m - 3) * C + c0);
+            } else if (s_in) {
+                val = *reinterpret_cast<const uint4 *>(s_in + ((size_t)n * 3 + m) * C + c0);
             }
             *reinterpret_cast<uint4 *>(s_out + ((size_t)n * 3 + j) * C + c0) = val;
         }
