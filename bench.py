@@ -210,123 +210,145 @@ def run_ours(args, world, rank, local):
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.int32, device=dev)  # 256 MiB
     q_v, k_v, v_v = gdn.split_qkv(y, s["Hk"], s["Hv"], s["dk"], s["dv"])
 
-    def prefill_step(evs=None):
-        if evs:
-            evs[0].record(stream)
-        gdn.gdn_conv1d_fwd(x, w, None, cu, None, conv_out, y, cu_seqlens_host=cu_h)
-        if evs:
-            evs[1].record(stream)
-        gdn.gdn_chunk_prefill(q_v, k_v, v_v, g, beta, cu, chunk=CHUNK, l2norm=True,
-                              o=o, final_state=hT, cu_seqlens_host=cu_h, workspace=ws)
-        if evs:
-            evs[2].record(stream)
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        prefill_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    clocks = Clocks(local).start()
-    t_wall = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()
-        prefill_step(evs[i])
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall
-    barrier(world)
-    clk = clocks.stop()
-    conv_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    scan_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    step_ms = [a + b for a, b in zip(conv_ms, scan_ms)]
-    launches += args.steps * (1 + args.scan_launches)
-    ms_step = max_over_ranks(statistics.mean(step_ms), world)
-    scan_avg = statistics.mean(scan_ms)
-    conv_avg = statistics.mean(conv_ms)
-    value = world * T / (ms_step * 1e-3)
-
+    scan_launches = 2 if ws_bytes else 1   # tensor-core path: prep + state kernels
+    legs = set(args.legs.split(","))
+    clk, t_wall, ms_step, value = None, None, None, None
+    scan_avg = conv_avg = achieved_tf = None
     flops = prefill_flops_per_token(**s) * T
-    achieved_tf = flops / (scan_avg * 1e-3) / 1e12
     conv_b = conv_bytes(T, C, 1)
     scan_b = prefill_bytes(T, 1, **s)
 
-    # ---------------- decode workload (256 sequences, fp32 state pool 805 MB)
-    Nd = args.decode_n
-    dd = inputs.decode_27b(seed=4, N=Nd)
-    dx = dd["conv"]["x"].to(dev)
-    dcs = dd["conv"]["conv_state"].to(dev)
-    dw = torch.empty((C, 4), dtype=torch.bfloat16, device=dev).copy_(cv["w"])
-    dq, dk_, dvv = dd["q"].to(dev), dd["k"].to(dev), dd["v"].to(dev)
-    dg, db = dd["g"].to(dev), dd["beta"].to(dev)
-    pool = dd["state_pool"].to(dev)
-    idx = dd["state_idx"].to(dev)
-    dy = torch.empty_like(dx)
-    do = torch.empty((Nd, s["Hv"], s["dv"]), dtype=torch.bfloat16, device=dev)
-    dstatus = torch.zeros(1, dtype=torch.int32, device=dev)
+    if "prefill" in legs:
+        def prefill_step(evs=None):
+            if evs:
+                evs[0].record(stream)
+            gdn.gdn_conv1d_fwd(x, w, None, cu, None, conv_out, y, cu_seqlens_host=cu_h)
+            if evs:
+                evs[1].record(stream)
+            gdn.gdn_chunk_prefill(q_v, k_v, v_v, g, beta, cu, chunk=CHUNK, l2norm=True,
+                                  o=o, final_state=hT, cu_seqlens_host=cu_h, workspace=ws)
+            if evs:
+                evs[2].record(stream)
 
-    def decode_step(evs=None):
-        if evs:
-            evs[0].record(stream)
-        gdn.gdn_conv1d_update(dx, dw, None, dcs, idx, dy, dstatus)
-        if evs:
-            evs[1].record(stream)
-        gdn.gdn_recurrent_decode(dq, dk_, dvv, dg, db, pool, idx, 1.0, True, do, dstatus)
-        if evs:
-            evs[2].record(stream)
+        for _ in range(args.warmup):
+            flush.zero_()
+            prefill_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        clocks = Clocks(local).start()
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            prefill_step(evs[i])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+        barrier(world)
+        clk = clocks.stop()
+        conv_ms = [e[0].elapsed_time(e[1]) for e in evs]
+        scan_ms = [e[1].elapsed_time(e[2]) for e in evs]
+        step_ms = [a + b for a, b in zip(conv_ms, scan_ms)]
+        launches += args.steps * (1 + scan_launches)
+        ms_step = max_over_ranks(statistics.mean(step_ms), world)
+        scan_avg = statistics.mean(scan_ms)
+        conv_avg = statistics.mean(conv_ms)
+        value = world * T / (ms_step * 1e-3)
 
-    for _ in range(args.warmup):
-        decode_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    devs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    for i in range(args.steps):
-        decode_step(devs[i])
-    torch.cuda.synchronize()
-    barrier(world)
-    launches += 2 * args.steps
-    dconv_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in devs)
-    ddec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in devs)
-    dstep_ms = max_over_ranks(dconv_ms + ddec_ms, world)
-    dbytes, dstate = decode_bytes(Nd, s["Hk"], s["Hv"], s["dk"], s["dv"], C)
-    dconv_b = Nd * C * 2 * 2 + 2 * Nd * 3 * C * 2
-    dec_b = dbytes - dconv_b
-    assert int(dstatus.item()) == 0
+        achieved_tf = flops / (scan_avg * 1e-3) / 1e12
 
-    # ---------------- e2e: pinned host inputs in, outputs out, through the public API
-    hx = cv["x"].pin_memory()
-    hg = wl["g"].pin_memory()
-    hb = wl["beta"].pin_memory()
-    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    hh = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
-    e2e_steps = max(3, min(args.steps, 10))
+    decode = None
+    if "decode" in legs:
+        # ---------------- decode workload (256 sequences, fp32 state pool 805 MB)
+        Nd = args.decode_n
+        dd = inputs.decode_27b(seed=4, N=Nd)
+        dx = dd["conv"]["x"].to(dev)
+        dcs = dd["conv"]["conv_state"].to(dev)
+        dw = torch.empty((C, 4), dtype=torch.bfloat16, device=dev).copy_(cv["w"])
+        dq, dk_, dvv = dd["q"].to(dev), dd["k"].to(dev), dd["v"].to(dev)
+        dg, db = dd["g"].to(dev), dd["beta"].to(dev)
+        pool = dd["state_pool"].to(dev)
+        idx = dd["state_idx"].to(dev)
+        dy = torch.empty_like(dx)
+        do = torch.empty((Nd, s["Hv"], s["dv"]), dtype=torch.bfloat16, device=dev)
+        dstatus = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    def e2e_step():
-        x.copy_(hx, non_blocking=True)
-        g.copy_(hg, non_blocking=True)
-        beta.copy_(hb, non_blocking=True)
-        gdn.gdn_layer_prefill(x, w, None, g, beta, cu, s["Hk"], s["Hv"], s["dk"], s["dv"],
-                              conv_state_out=conv_out, final_state=hT, y=y, o=o,
-                              cu_seqlens_host=cu_h, workspace=ws)
-        ho.copy_(o, non_blocking=True)
-        hh.copy_(hT, non_blocking=True)
+        def decode_step(evs=None):
+            if evs:
+                evs[0].record(stream)
+            gdn.gdn_conv1d_update(dx, dw, None, dcs, idx, dy, dstatus)
+            if evs:
+                evs[1].record(stream)
+            gdn.gdn_recurrent_decode(dq, dk_, dvv, dg, db, pool, idx, 1.0, True, do, dstatus)
+            if evs:
+                evs[2].record(stream)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    launches += e2e_steps * (1 + args.scan_launches)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
-    h2d = hx.numel() * 2 + hg.numel() * 4 + hb.numel() * 4
-    d2h = ho.numel() * 2 + hh.numel() * 4
+        for _ in range(args.warmup):
+            decode_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        devs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            decode_step(devs[i])
+        torch.cuda.synchronize()
+        barrier(world)
+        launches += 2 * args.steps
+        dconv_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in devs)
+        ddec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in devs)
+        dstep_ms = max_over_ranks(dconv_ms + ddec_ms, world)
+        dbytes, dstate = decode_bytes(Nd, s["Hk"], s["Hv"], s["dk"], s["dv"], C)
+        dconv_b = Nd * C * 2 * 2 + 2 * Nd * 3 * C * 2
+        dec_b = dbytes - dconv_b
+        assert int(dstatus.item()) == 0
+        decode = {"workload": "%d seqs x 1 token, state [%d,48,128,128] fp32 in place, "
+                              "conv update 10240 ch, permuted state_idx" % (Nd, Nd),
+                  "ms_per_step": dstep_ms,
+                  "state_gbs": dstate / (dstep_ms * 1e-3) / 1e9,
+                  "kernels_ms": {"conv1d_update": dconv_ms, "recurrent_decode": ddec_ms},
+                  "roofline": {"kernel": "recurrent_decode", "bound": "hbm",
+                               "achieved": dec_b / (ddec_ms * 1e-3) / 1e9,
+                               "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": dec_b / (ddec_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                               "traffic": None}}
+
+    e2e = None
+    if "e2e" in legs:
+        # ---------------- e2e: pinned host inputs in, outputs out, through the public API
+        hx = cv["x"].pin_memory()
+        hg = wl["g"].pin_memory()
+        hb = wl["beta"].pin_memory()
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hh = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
+        e2e_steps = max(3, min(args.steps, 10))
+
+        def e2e_step():
+            x.copy_(hx, non_blocking=True)
+            g.copy_(hg, non_blocking=True)
+            beta.copy_(hb, non_blocking=True)
+            gdn.gdn_layer_prefill(x, w, None, g, beta, cu, s["Hk"], s["Hv"], s["dk"], s["dv"],
+                                  conv_state_out=conv_out, final_state=hT, y=y, o=o,
+                                  cu_seqlens_host=cu_h, workspace=ws)
+            ho.copy_(o, non_blocking=True)
+            hh.copy_(hT, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        launches += e2e_steps * (1 + scan_launches)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+        h2d = hx.numel() * 2 + hg.numel() * 4 + hb.numel() * 4
+        d2h = ho.numel() * 2 + hh.numel() * 4
+        e2e = {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     result = {
         "metric": METRIC,
@@ -346,35 +368,29 @@ def run_ours(args, world, rank, local):
                                "in kernel" % T,
                    "global_batch": world, "seq_len": T, "parallelism": "replicas x%d" % world,
                    "l2": "flushed between steps (256 MiB write)"},
-        "kernels_ms": {"conv1d_fwd": conv_avg, "chunk_prefill": scan_avg},
-        "roofline": {"kernel": "chunk_prefill", "bound": "tensor", "achieved": achieved_tf,
-                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved_tf / peaks["bf16_tflops"],
-                     "peak_source": "%s (bf16 dense burst)" % peaks["source"],
-                     "traffic": None,
-                     "algorithmic_flops_per_launch": flops,
-                     "algorithmic_bytes_per_launch": scan_b,
-                     "hbm_gbs_equiv": scan_b / (scan_avg * 1e-3) / 1e9},
-        "conv_roofline": {"bound": "hbm", "achieved": conv_b / (conv_avg * 1e-3) / 1e9,
-                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                          "frac": conv_b / (conv_avg * 1e-3) / 1e9 / peaks["hbm_gbs"]},
-        "decode": {"workload": "256 seqs x 1 token, state [256,48,128,128] fp32 in place, "
-                               "conv update 10240 ch, permuted state_idx",
-                   "ms_per_step": dstep_ms,
-                   "state_gbs": dstate / (dstep_ms * 1e-3) / 1e9,
-                   "kernels_ms": {"conv1d_update": dconv_ms, "recurrent_decode": ddec_ms},
-                   "roofline": {"kernel": "recurrent_decode", "bound": "hbm",
-                                "achieved": dec_b / (ddec_ms * 1e-3) / 1e9,
-                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                "frac": dec_b / (ddec_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                                "traffic": None}},
-        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
-        "gpu_launches": launches,
-        "clocks": clk,
-        "wall_s_timed_region": t_wall,
     }
+    if "prefill" in legs:
+        result["kernels_ms"] = {"conv1d_fwd": conv_avg, "chunk_prefill": scan_avg}
+        result["roofline"] = {
+            "kernel": "chunk_prefill", "bound": "tensor", "achieved": achieved_tf,
+            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": achieved_tf / peaks["bf16_tflops"],
+            "peak_source": "%s (bf16 dense burst)" % peaks["source"],
+            "traffic": None,
+            "algorithmic_flops_per_launch": flops,
+            "algorithmic_bytes_per_launch": scan_b,
+            "hbm_gbs_equiv": scan_b / (scan_avg * 1e-3) / 1e9}
+        result["conv_roofline"] = {
+            "bound": "hbm", "achieved": conv_b / (conv_avg * 1e-3) / 1e9,
+            "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": conv_b / (conv_avg * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+        result["clocks"] = clk
+        result["wall_s_timed_region"] = t_wall
+    if decode is not None:
+        result["decode"] = decode
+    if e2e is not None:
+        result["e2e"] = e2e
+    result["gpu_launches"] = launches
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(T, samples=args.cpu_samples)
     if rank == 0:
@@ -446,9 +462,10 @@ def main():
     ap.add_argument("--decode-n", type=int, default=256)
     ap.add_argument("--cpu-samples", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--legs", default="prefill,decode,e2e",
+                    help="comma list of legs to run (profiling runs pick one)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    args.scan_launches = 1
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
