@@ -124,19 +124,27 @@ __device__ __forceinline__ float row_sumsq(const uint8_t *tile, int row, uint32_
     return acc;
 }
 
+// g and beta of token r = thread r (threads 0..63) of one chunk for v-head hv; zeros past
+// the chunk's end.  Issued ahead of use so the global latency hides behind other work.
+__device__ __forceinline__ void load_gates(const TcParams &p, int t0, int L, int hv, float &gx,
+                                           float &bx) {
+    const int tid = threadIdx.x;
+    gx = 0.f;
+    bx = 0.f;
+    if (tid < L) {
+        gx = p.g[(size_t)(t0 + tid) * p.Hv + hv];
+        bx = p.beta[(size_t)(t0 + tid) * p.Hv + hv];
+    }
+}
+
 // Inclusive cumulative sum of g over the chunk by warps 0 and 1 (token r = thread r),
-// fixed order; also beta.  Writes gam[64], bet[64].  Must be called by all threads.
-__device__ __forceinline__ void chunk_gates(const TcParams &p, int t0, int L, int hv,
-                                            float *gam, float *bet, float *carry) {
+// fixed order; writes gam[64] and bet[64].  Must be called by all threads.
+__device__ __forceinline__ void chunk_gates(float gx, float bx, float *gam, float *bet,
+                                            float *carry) {
     const int tid = threadIdx.x, lane = tid & 31;
-    float x = 0.f;
+    float x = gx;
     if (tid < kC) {
-        if (tid < L) {
-            x = p.g[(size_t)(t0 + tid) * p.Hv + hv];
-            bet[tid] = p.beta[(size_t)(t0 + tid) * p.Hv + hv];
-        } else {
-            bet[tid] = 0.f;
-        }
+        bet[tid] = bx;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const float y = __shfl_up_sync(0xffffffffu, x, off);
@@ -293,9 +301,12 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
         tmem_row64(tmem + lane_off + colP, P);  // row tid: k_r.k_s (tid<64) or q_r.k_s
     }
 
+    float gx, bx;
+    load_gates(p, t0, L, hk * G, gx, bx);
     for (int gi = 0; gi < G && ok; ++gi) {
         const int hv = hk * G + gi;
-        chunk_gates(p, t0, L, hv, S.gam, S.bet, &S.carry);
+        chunk_gates(gx, bx, S.gam, S.bet, &S.carry);
+        if (gi + 1 < G) load_gates(p, t0, L, hv + 1, gx, bx);
         const int r = tid & 63;
         float Mrow[64];
         if (tid < 64) {
@@ -461,6 +472,8 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
 
     bool ok = true;
     const int r = tid & 63;
+    float gx = 0.f, bx = 0.f;
+    if (nch > 0) load_gates(p, start, min(kC, len), hv, gx, bx);
     for (int c = 0; c < nch && ok; ++c) {
         const int st = c & 1;
         const uint32_t ph = c & 1;
@@ -483,7 +496,8 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
             if (tid < 64) S.nk[r] = r < L ? f : 0.f;
             else S.nq[r] = r < L ? f : 0.f;
         }
-        chunk_gates(p, t0, L, hv, S.gam, S.bet, &S.carry);
+        chunk_gates(gx, bx, S.gam, S.bet, &S.carry);
+        if (c + 1 < nch) load_gates(p, t0 + kC, min(kC, len - (c + 1) * kC), hv, gx, bx);
         const float gL = S.gam[L - 1];
 
         // h: bf16 copy for the MMA, then scale the fp32 master by e^{gamma_L}
