@@ -25,6 +25,7 @@ from . import _lib
 from ._lib import GDN_PREFILL_SIMT, GDN_QK_L2NORM, GdnError  # noqa: F401
 
 __all__ = ["gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
+           "gdn_chunk_prefill_noalloc",
            "gdn_recurrent_decode", "gdn_chunk_prefill_workspace_size",
            "gdn_layer_prefill", "gdn_layer_decode", "GdnError", "load"]
 
@@ -154,6 +155,35 @@ def gdn_chunk_prefill(q, k, v, g, beta, cu_seqlens, chunk=64, scale=1.0, l2norm=
         _vp(initial_state), ctypes.byref(do), _vp(final_state), _vp(workspace),
         ws_bytes, _vp(status), _stream())
     _lib.check(rc, "gdn_chunk_prefill")
+    return o, final_state
+
+
+def gdn_chunk_prefill_noalloc(q, k, v, g, beta, cu_seqlens, chunk=64, scale=1.0,
+                              l2norm=False, initial_state=None, output_final_state=True,
+                              o=None, final_state=None, simt=False, cu_seqlens_host=None,
+                              status=None):
+    """gdn_chunk_prefill for callers that cannot allocate device scratch: the library
+    uses its own fixed 64 MiB device array instead of a workspace (see include/gdn.h).
+    Output tensors are still the caller's; pass ``o``/``final_state`` to avoid any
+    allocation on the Python side as well.  Returns (o, final_state)."""
+    lib = _lib.load()
+    _need_cuda(q, k, v, g, beta, initial_state, o, final_state, status)
+    cu, cu_h = _seqlens(cu_seqlens, cu_seqlens_host)
+    N = cu_h.numel() - 1
+    T, Hk, dk = q.shape[-3:]
+    Hv, dv = v.shape[-2:]
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=q.device)
+    flags = (GDN_QK_L2NORM if l2norm else 0) | (GDN_PREFILL_SIMT if simt else 0)
+    dq, dk_, dv_, do = _desc(q), _desc(k), _desc(v), _desc(o)
+    rc = lib.gdn_chunk_prefill_noalloc(
+        ctypes.byref(dq), ctypes.byref(dk_), ctypes.byref(dv_), _vp(g.contiguous()),
+        _vp(beta.contiguous()), _vp(cu), ctypes.c_void_p(cu_h.data_ptr()), N, chunk,
+        float(scale), flags, _vp(initial_state), ctypes.byref(do), _vp(final_state),
+        _vp(status), _stream())
+    _lib.check(rc, "gdn_chunk_prefill_noalloc")
     return o, final_state
 
 

@@ -21,7 +21,9 @@ STATUS = {
 
 EXPORTS = ("gdn_status_string", "gdn_version", "gdn_conv1d_fwd", "gdn_conv1d_update",
            "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill",
-           "gdn_recurrent_decode")
+           "gdn_chunk_prefill_noalloc", "gdn_recurrent_decode")
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class GdnTensor(ctypes.Structure):
@@ -60,6 +62,8 @@ def load(path: str = LIB_PATH):
                                              ctypes.c_size_t),
         "gdn_chunk_prefill": ([tp, tp, tp, vp, vp, vp, vp, i32, i32, f32, u32, vp, tp, vp,
                                vp, ctypes.c_size_t, vp, vp], i32),
+        "gdn_chunk_prefill_noalloc": ([tp, tp, tp, vp, vp, vp, vp, i32, i32, f32, u32, vp,
+                                       tp, vp, vp, vp], i32),
         "gdn_recurrent_decode": ([tp, tp, tp, vp, vp, vp, i32, vp, f32, u32, tp, vp, vp],
                                  i32),
     }

@@ -152,6 +152,36 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t *q, const gdn_tensor_t *k,
                                size_t workspace_bytes, int32_t *status_dev, void *stream);
 
 /*
+ * gdn_chunk_prefill_noalloc -- gdn_chunk_prefill without a caller-provided workspace.
+ * The pages have no counterpart to this entry point; it exists for callers that cannot
+ * call cudaMalloc (an engine whose allocator owns all device memory, a latency-critical
+ * loop that must not allocate, a host program with no device allocator of its own).
+ *
+ * Arguments, results, kernels and errors are those of gdn_chunk_prefill, except that the
+ * scratch comes from a fixed array of GDN_NOALLOC_SCRATCH_BYTES inside the library's
+ * device image, which every GPU that loads the library holds until the process exits.
+ * A call whose gdn_chunk_prefill_workspace_size() exceeds that size returns
+ * GDN_ERR_WORKSPACE before launching anything.  The call allocates nothing (no cudaMalloc
+ * or cudaFree, no allocating library routine).
+ * The first call on a device (with that device current) looks up the array's device
+ * address once and caches it; make that first call before any stream capture.
+ * Every call shares the one array: calls that overlap on the GPU (on different streams,
+ * or from several threads without ordering) race on it and must be serialised by the
+ * caller.  Each call writes every scratch byte it later reads, so stale contents from an
+ * earlier call do not matter.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+gdn_status_t gdn_chunk_prefill_noalloc(const gdn_tensor_t *q, const gdn_tensor_t *k,
+                                       const gdn_tensor_t *v, const float *g,
+                                       const float *beta, const int32_t *cu_seqlens_dev,
+                                       const int32_t *cu_seqlens_host, int32_t N,
+                                       int32_t chunk, float scale, uint32_t flags,
+                                       const float *initial_state, const gdn_tensor_t *o,
+                                       float *final_state, int32_t *status_dev,
+                                       void *stream);
+
+/*
  * gdn_recurrent_decode -- one token per sequence on a pool of fp32 states, in place.
  * Source: the decode path of "[Feature] Add batch invariance support to GDN_ATTN
  * backend - #45819" (fused_sigmoid_gating_delta_rule_update with ssm_state_indices into
