@@ -8,15 +8,16 @@
 // Two kernels, both tcgen05 (MMA into TMEM, operands in 128B-swizzled shared memory fed
 // by TMA):
 //
-//  chunk_prep (one CTA per (chunk, k-head), fully parallel):
+//  chunk_prep (one CTA per (chunk, v-head), fully parallel):
 //      P = [K;Q] K^T                                   (tcgen05, M=128 N=64 K=128)
-//    per v-head of the group, with gamma the in-chunk inclusive log-decay sums and nk, nq
-//    the L2-norm factors (1 when the flag is off):
+//    with gamma the in-chunk inclusive log-decay sums and nk, nq the L2-norm factors
+//    (1 when the flag is off):
 //      A[r][s]  = beta_r e^{gamma_r-gamma_s} nk_r nk_s (k_r.k_s)          s < r
 //      M[r][s]  = e^{gamma_r-gamma_s} nq_r nk_s (q_r.k_s)                  s <= r
 //      Tinv     = (I + A)^{-1}   (fp32, blocked forward substitution on CUDA cores)
 //      Lo       = Tinv - I,  Mt = M Tinv = M + M Lo   (tcgen05 for M Lo)
-//    and stores the 128x64 bf16 tile X = [Lo ; Mt] (already swizzled) to the workspace.
+//    and stores one workspace tile: the 128x64 bf16 X = [Lo ; Mt] (already swizzled)
+//    followed by the chunk's fp32 gamma, beta, nk and nq.
 //
 //  chunk_state (one CTA per (sequence, v-head, 64-column dv tile), walks the chunks):
 //      D1 = [K;Q] h                      (h: fp32 state in TMEM, bf16 copy as operand)
@@ -28,6 +29,7 @@
 //    The last product takes diag(.)Vn as a bf16 hi + lo pair (two MMAs) so the state
 //    keeps fp32-level accuracy; q/k L2 norms and decays are per-token fp32 scalars applied
 //    outside the MMAs, so the raw bf16 inputs are the only operands that are not split.
+//    Eight warps: warps w and w+4 share TMEM lanes 32(w%4).. and take 32 columns each.
 //
 // Every wait on an mbarrier is bounded in time; on expiry the CTA records GDN_ERR_TIMEOUT
 // in the status word, stops issuing work, frees its TMEM and returns.
@@ -39,12 +41,15 @@
 
 namespace gdn {
 
-constexpr int kTcThreads = 128;
+constexpr int kPrepThreads = 128;
+constexpr int kStateThreads = 256;
 constexpr int kC = 64;          // chunk
 constexpr int kD = 128;         // dk = dv
 constexpr int kDVT = 64;        // dv columns per state CTA
-constexpr uint32_t kXTile = 16384;   // bf16 [128 rows][64] swizzled
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s bound on any single wait
+constexpr uint32_t kXTile = 16384;            // bf16 [128 rows][64] swizzled
+constexpr uint32_t kScal = 4 * kC * 4;        // gamma, beta, nk, nq (fp32 x 64 each)
+constexpr uint32_t kWsTile = kXTile + kScal;  // one workspace tile per (slot, v-head)
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s bound on any single wait
 
 struct TcMaps {
     CUtensorMap q, k, v;
@@ -85,13 +90,15 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
 // batch get distinct slots below ceil(T / 64) + N.
 __device__ __forceinline__ int slot0(const int32_t *cu, int n) { return cu[n] / kC + n; }
 
-__device__ __forceinline__ void pack_row64(uint8_t *tile, int row, const float (&v)[64]) {
+// Pack N consecutive floats to bf16 into 16-byte chunks c0.. of a swizzled tile row.
+template <int N>
+__device__ __forceinline__ void pack_row(uint8_t *tile, int row, int c0, const float (&v)[N]) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < N / 8; ++c) {
         float f[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) f[e] = v[8 * c + e];
-        *reinterpret_cast<uint4 *>(tile + tc::swz(row, c)) = pack8(f);
+        *reinterpret_cast<uint4 *>(tile + tc::swz(row, c0 + c)) = pack8(f);
     }
 }
 
@@ -105,6 +112,11 @@ __device__ __forceinline__ void tmem_row64(uint32_t taddr, float (&v)[64]) {
         v[i] = a[i];
         v[32 + i] = b[i];
     }
+}
+
+__device__ __forceinline__ void tmem_row32(uint32_t taddr, float (&v)[32]) {
+    tc::tmem_ld32(taddr, v);
+    tc::tmem_wait_ld();
 }
 
 // Sum of squares of one 128-element bf16 row held in a K-major tile of two 64-wide
@@ -122,39 +134,6 @@ __device__ __forceinline__ float row_sumsq(const uint8_t *tile, int row, uint32_
         }
     }
     return acc;
-}
-
-// g and beta of token r = thread r (threads 0..63) of one chunk for v-head hv; zeros past
-// the chunk's end.  Issued ahead of use so the global latency hides behind other work.
-__device__ __forceinline__ void load_gates(const TcParams &p, int t0, int L, int hv, float &gx,
-                                           float &bx) {
-    const int tid = threadIdx.x;
-    gx = 0.f;
-    bx = 0.f;
-    if (tid < L) {
-        gx = p.g[(size_t)(t0 + tid) * p.Hv + hv];
-        bx = p.beta[(size_t)(t0 + tid) * p.Hv + hv];
-    }
-}
-
-// Inclusive cumulative sum of g over the chunk by warps 0 and 1 (token r = thread r),
-// fixed order; writes gam[64] and bet[64].  Must be called by all threads.
-__device__ __forceinline__ void chunk_gates(float gx, float bx, float *gam, float *bet,
-                                            float *carry) {
-    const int tid = threadIdx.x, lane = tid & 31;
-    float x = gx;
-    if (tid < kC) {
-        bet[tid] = bx;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, x, off);
-            if (lane >= off) x += y;
-        }
-        if (tid == 31) *carry = x;
-    }
-    __syncthreads();
-    if (tid < kC) gam[tid] = tid >= 32 ? x + *carry : x;
-    __syncthreads();
 }
 
 // ------------------------------------------------------------------ Tinv (fp32)
@@ -185,25 +164,35 @@ __device__ void tinv64(float (*A)[65], float (*T)[65], float (*Y)[65]) {
         }
     }
     __syncthreads();
+    // Each thread computes two adjacent columns of one output row per pass.
     for (int i = 1; i < 4; ++i) {
         // Y_j = sum_{k=j}^{i-1} A_ik T_kj   for j < i   (16x16 each)
-        for (int e = tid; e < i * 256; e += kTcThreads) {
-            const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-            float acc = 0.f;
+        for (int e = tid; e < i * 128; e += kPrepThreads) {
+            const int j = e >> 7, rr = (e >> 3) & 15, cc = (e & 7) * 2;
+            float a0 = 0.f, a1 = 0.f;
             for (int k = j; k < i; ++k) {
 #pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    acc = fmaf(A[16 * i + rr][16 * k + m], T[16 * k + m][16 * j + cc], acc);
+                for (int m = 0; m < 16; ++m) {
+                    const float av = A[16 * i + rr][16 * k + m];
+                    a0 = fmaf(av, T[16 * k + m][16 * j + cc], a0);
+                    a1 = fmaf(av, T[16 * k + m][16 * j + cc + 1], a1);
+                }
             }
-            Y[16 * j + rr][cc] = acc;
+            Y[16 * j + rr][cc] = a0;
+            Y[16 * j + rr][cc + 1] = a1;
         }
         __syncthreads();
-        for (int e = tid; e < i * 256; e += kTcThreads) {
-            const int j = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-            float acc = 0.f;
+        for (int e = tid; e < i * 128; e += kPrepThreads) {
+            const int j = e >> 7, rr = (e >> 3) & 15, cc = (e & 7) * 2;
+            float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-            for (int m = 0; m < 16; ++m) acc = fmaf(T[16 * i + rr][16 * i + m], Y[16 * j + m][cc], acc);
-            T[16 * i + rr][16 * j + cc] = -acc;
+            for (int m = 0; m < 16; ++m) {
+                const float tv = T[16 * i + rr][16 * i + m];
+                a0 = fmaf(tv, Y[16 * j + m][cc], a0);
+                a1 = fmaf(tv, Y[16 * j + m][cc + 1], a1);
+            }
+            T[16 * i + rr][16 * j + cc] = -a0;
+            T[16 * i + rr][16 * j + cc + 1] = -a1;
         }
         __syncthreads();
     }
@@ -213,7 +202,7 @@ __device__ void tinv64(float (*A)[65], float (*T)[65], float (*Y)[65]) {
 
 struct PrepSmem {
     uint8_t kq[32768];       // [K;Q] K-major, 2 K blocks of [128 rows][128 B]
-    uint8_t x[kXTile];       // [Lo ; M] then [Lo ; Mt]
+    uint8_t x[kXTile];       // [Lo ; M]
     float A[64][65];
     float T[64][65];
     float Y[64][65];
@@ -223,14 +212,14 @@ struct PrepSmem {
     uint32_t tmem;
 };
 
-__global__ void __launch_bounds__(kTcThreads)
+__global__ void __launch_bounds__(kPrepThreads)
 chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     PrepSmem &S = *reinterpret_cast<PrepSmem *>(
         (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023));
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int slot = blockIdx.x, hk = blockIdx.y;
-    const int G = p.Hv / p.Hk;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int slot = blockIdx.x, hv = blockIdx.y;
+    const int hk = hv / (p.Hv / p.Hk);
 
     // slot -> (sequence n, chunk c): the last n with slot0(n) <= slot.
     int lo = 0, hi = p.N - 1;
@@ -241,9 +230,16 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     const int n = lo;
     const int c = slot - slot0(p.cu, n);
     const int start = p.cu[n], len = p.cu[n + 1] - start;
-    if (p.N == 0 || c < 0 || c * kC >= len) return;
+    if (c < 0 || c * kC >= len) return;
     const int t0 = start + c * kC;
-    const int L = min(kC, len - t0 + start);
+    const int L = min(kC, len - c * kC);
+
+    // this chunk's gates (latency hidden behind the TMA and the first MMA)
+    float gx = 0.f, bx = 0.f;
+    if (tid < L) {
+        gx = p.g[(size_t)(t0 + tid) * p.Hv + hv];
+        bx = p.beta[(size_t)(t0 + tid) * p.Hv + hv];
+    }
 
     if (warp == 0) {
         tc::tmem_alloc(&S.tmem, 128);
@@ -263,7 +259,6 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const uint32_t colP = 0, colM = 64;
     bool ok = true;
-    uint32_t mma_phase = 0;
 
     if (tid == 0) {
         tc::mbar_expect_tx(&S.bar_tma, 32768);
@@ -272,6 +267,14 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
         tc::tma_load_3d(S.kq + 8192, &maps.q, &S.bar_tma, 0, hk, t0);
         tc::tma_load_3d(S.kq + 16384 + 8192, &maps.q, &S.bar_tma, 64, hk, t0);
     }
+    // inclusive scan of g by warps 0 and 1 (fixed order), while the loads fly
+    float gs = gx;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, gs, off);
+        if (lane >= off) gs += y;
+    }
+    if (tid == 31) S.carry = gs;
     ok = wait_all(&S.bar_tma, 0);
     if (ok && tid == 0) {
         tc::fence_after_sync();
@@ -285,90 +288,94 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
         }
         tc::mma_commit(&S.bar_mma);
     }
-    // L2-norm factors of this chunk's k rows (threads 0..63) and q rows (64..127)
+    const int r = tid & 63;
     if (ok) {
+        // L2-norm factors of this chunk's k rows (threads 0..63) and q rows (64..127)
         const float ss = row_sumsq(S.kq, tid, 16384);
         const float f = p.l2norm ? rsqrtf(ss + 1e-6f) : 1.f;
-        const int r = tid & 63;
-        if (tid < 64) S.nk[r] = r < L ? f : 0.f;
-        else S.nq[r] = r < L ? f : 0.f;
+        if (tid < 64) {
+            S.nk[r] = r < L ? f : 0.f;
+            S.gam[r] = tid >= 32 ? gs + S.carry : gs;
+            S.bet[r] = bx;
+        } else {
+            S.nq[r] = r < L ? f : 0.f;
+        }
     }
-    if (ok) ok = wait_all(&S.bar_mma, mma_phase);
-    mma_phase ^= 1;
+    if (ok) ok = wait_all(&S.bar_mma, 0);
     float P[64];
     if (ok) {
         tc::fence_after_sync();
         tmem_row64(tmem + lane_off + colP, P);  // row tid: k_r.k_s (tid<64) or q_r.k_s
     }
-
-    float gx, bx;
-    load_gates(p, t0, L, hk * G, gx, bx);
-    for (int gi = 0; gi < G && ok; ++gi) {
-        const int hv = hk * G + gi;
-        chunk_gates(gx, bx, S.gam, S.bet, &S.carry);
-        if (gi + 1 < G) load_gates(p, t0, L, hv + 1, gx, bx);
-        const int r = tid & 63;
-        float Mrow[64];
+    uint8_t *wtile = p.ws + ((size_t)slot * p.Hv + hv) * kWsTile;
+    float Mrow[64];
+    if (ok) {
+        const float gr = S.gam[r];
         if (tid < 64) {
-            const float gr = S.gam[r], br = S.bet[r], nr = S.nk[r];
+            const float br = S.bet[r] * S.nk[r];
 #pragma unroll
             for (int s = 0; s < 64; ++s)
-                S.A[r][s] = (s < r && r < L) ? br * expf(gr - S.gam[s]) * nr * S.nk[s] * P[s] : 0.f;
+                S.A[r][s] = (s < r && r < L) ? br * __expf(gr - S.gam[s]) * S.nk[s] * P[s] : 0.f;
         } else {
-            const float gr = S.gam[r], nr = S.nq[r];
+            const float nr = S.nq[r];
 #pragma unroll
             for (int s = 0; s < 64; ++s)
-                Mrow[s] = (s <= r && r < L) ? expf(gr - S.gam[s]) * nr * S.nk[s] * P[s] : 0.f;
-            pack_row64(S.x, tid, Mrow);
+                Mrow[s] = (s <= r && r < L) ? nr * __expf(gr - S.gam[s]) * S.nk[s] * P[s] : 0.f;
+            pack_row<64>(S.x, tid, 0, Mrow);
         }
-        __syncthreads();
-        tinv64(S.A, S.T, S.Y);
-        uint8_t *wtile = p.ws + ((size_t)slot * p.Hv + hv) * kXTile;
+        // per-token scalars for the state kernel
+        float *ws_s = reinterpret_cast<float *>(wtile + kXTile);
         if (tid < 64) {
-            float lrow[64];
-#pragma unroll
-            for (int t = 0; t < 64; ++t) lrow[t] = (t == r) ? 0.f : S.T[r][t];
-            pack_row64(S.x, tid, lrow);
-            // Lo rows go to the workspace as they are
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc)
-                *reinterpret_cast<uint4 *>(wtile + tc::swz(tid, cc)) =
-                    *reinterpret_cast<const uint4 *>(S.x + tc::swz(tid, cc));
+            ws_s[r] = S.gam[r];
+            ws_s[64 + r] = S.bet[r];
+            ws_s[128 + r] = S.nk[r];
+        } else {
+            ws_s[192 + r] = S.nq[r];
         }
-        tc::fence_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            tc::fence_after_sync();
-            // D[128x64] = X[128 x 64] * Lo[64 x 64]  (B = rows 0..63 of X, MN-major)
-            constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
-            const uint32_t xb = tc::smem_u32(S.x);
+    }
+    __syncthreads();
+    if (ok) tinv64(S.A, S.T, S.Y);
+    if (ok && tid < 64) {
+        float lrow[64];
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tmem + colM, tc::sdesc(xb + ks * 32, 16, 1024),
-                             tc::sdesc(xb + ks * 2048, 8192, 1024), id, ks > 0);
-            tc::mma_commit(&S.bar_mma);
-        }
-        ok = wait_all(&S.bar_mma, mma_phase);
-        mma_phase ^= 1;
-        if (ok) {
-            tc::fence_after_sync();
-            if (tid >= 64) {
-                float mt[64];
-                tmem_row64(tmem + lane_off + colM, mt);
+        for (int t = 0; t < 64; ++t) lrow[t] = (t == r) ? 0.f : S.T[r][t];
+        pack_row<64>(S.x, tid, 0, lrow);
+        // Lo rows go to the workspace as they are
 #pragma unroll
-                for (int s = 0; s < 64; ++s) mt[s] += Mrow[s];   // Mt = M + M Lo
-                float f[8];
+        for (int cc = 0; cc < 8; ++cc)
+            *reinterpret_cast<uint4 *>(wtile + tc::swz(tid, cc)) =
+                *reinterpret_cast<const uint4 *>(S.x + tc::swz(tid, cc));
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (ok && tid == 0) {
+        tc::fence_after_sync();
+        // D[128x64] = X[128 x 64] * Lo[64 x 64]  (B = rows 0..63 of X, MN-major)
+        constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
+        const uint32_t xb = tc::smem_u32(S.x);
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
+        for (int ks = 0; ks < 4; ++ks)
+            tc::mma_bf16(tmem + colM, tc::sdesc(xb + ks * 32, 16, 1024),
+                         tc::sdesc(xb + ks * 2048, 8192, 1024), id, ks > 0);
+        tc::mma_commit(&S.bar_mma);
+    }
+    if (ok) ok = wait_all(&S.bar_mma, 1);
+    if (ok) {
+        tc::fence_after_sync();
+        if (tid >= 64) {
+            float mt[64];
+            tmem_row64(tmem + lane_off + colM, mt);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = mt[8 * cc + e];
-                    *reinterpret_cast<uint4 *>(wtile + tc::swz(tid, cc)) = pack8(f);
-                }
+            for (int s = 0; s < 64; ++s) mt[s] += Mrow[s];   // Mt = M + M Lo
+            float f[8];
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = mt[8 * cc + e];
+                *reinterpret_cast<uint4 *>(wtile + tc::swz(tid, cc)) = pack8(f);
             }
         }
-        tc::fence_before_sync();
-        __syncthreads();
     }
     if (!ok && tid == 0) report(p.status, GDN_ERR_TIMEOUT);
     tc::fence_before_sync();
@@ -378,16 +385,16 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
 
 // =============================================================== chunk_state kernel
 
+constexpr uint32_t kXStage = 18432;  // workspace tile rounded up to 1024 bytes
+
 struct StateSmem {
     uint8_t kq[2][32768];    // [K;Q] per stage
-    uint8_t x[2][kXTile];    // [Lo ; Mt] per stage
+    uint8_t x[2][kXStage];   // [Lo ; Mt] + scalars per stage
     uint8_t v[2][8192];      // V tile [64 tokens][64 dv] per stage
     uint8_t hb[16384];       // bf16 h  [128 dk rows][64 dv]  (MN-major B)
     uint8_t rb[8192];        // bf16 R  [64 tokens][64 dv]    (MN-major B)
     uint8_t dvh[8192];       // bf16 hi of diag(dcy) Vn
     uint8_t dvl[8192];       // bf16 lo
-    float gam[64], bet[64], nk[64], nq[64];
-    float carry;
     uint64_t bar_tma[2], bar_d1, bar_d2, bar_d3;
     uint32_t tmem;
 };
@@ -396,25 +403,28 @@ __device__ __forceinline__ void issue_chunk_loads(StateSmem &S, const TcMaps &ma
                                                   const TcParams &p, int stage, int t0,
                                                   int hk, int hv, int j0, int slot) {
     uint64_t *bar = &S.bar_tma[stage];
-    tc::mbar_expect_tx(bar, 32768 + 8192 + kXTile);
+    tc::mbar_expect_tx(bar, 32768 + 8192 + kWsTile);
     uint8_t *kq = S.kq[stage];
     tc::tma_load_3d(kq + 0, &maps.k, bar, 0, hk, t0);
     tc::tma_load_3d(kq + 16384, &maps.k, bar, 64, hk, t0);
     tc::tma_load_3d(kq + 8192, &maps.q, bar, 0, hk, t0);
     tc::tma_load_3d(kq + 16384 + 8192, &maps.q, bar, 64, hk, t0);
     tc::tma_load_3d(S.v[stage], &maps.v, bar, j0, hv, t0);
-    const uint8_t *src = p.ws + ((size_t)slot * p.Hv + hv) * kXTile;
+    const uint8_t *src = p.ws + ((size_t)slot * p.Hv + hv) * kWsTile;
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 :: "r"(tc::smem_u32(S.x[stage])), "l"(src), "r"(kXTile),
+                 :: "r"(tc::smem_u32(S.x[stage])), "l"(src), "r"(kWsTile),
                     "r"(tc::smem_u32(bar)) : "memory");
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kStateThreads, 1)
 chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     StateSmem &S = *reinterpret_cast<StateSmem *>(
         (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023));
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3;           // TMEM lane quarter
+    const int half = warp >> 2;          // which 32 of the 64 dv columns
+    const int row = quad * 32 + lane;    // TMEM lane = tile row
     const int jt = blockIdx.x, hv = blockIdx.y, n = blockIdx.z;
     const int hk = hv / (p.Hv / p.Hk);
     const int j0 = jt * kDVT;
@@ -442,28 +452,25 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = S.tmem;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t ch = half * 32;       // this thread's column offset
     const uint32_t colH = 0, colD1 = 64, colD2 = 128;
 
-    // Initial state: thread i holds dk row i of the [128][64] fp32 tile.
+    // Initial state: thread (row, half) holds dk row `row`, columns ch..ch+31.
     {
-        float h[64];
+        float h[32];
         if (p.h0) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.h0 + hoff + (size_t)tid * kD + j0);
+            const float4 *src = reinterpret_cast<const float4 *>(p.h0 + hoff + (size_t)row * kD + j0 + ch);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < 8; ++i) {
                 const float4 f = src[i];
                 h[4 * i] = f.x; h[4 * i + 1] = f.y; h[4 * i + 2] = f.z; h[4 * i + 3] = f.w;
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < 64; ++i) h[i] = 0.f;
+            for (int i = 0; i < 32; ++i) h[i] = 0.f;
         }
-        float a[32], b[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) { a[i] = h[i]; b[i] = h[32 + i]; }
-        tc::tmem_st32(tmem + lane_off + colH, a);
-        tc::tmem_st32(tmem + lane_off + colH + 32, b);
+        tc::tmem_st32(tmem + lane_off + colH + ch, h);
         tc::tmem_wait_st();
     }
     if (tid == 0 && nch > 0) issue_chunk_loads(S, maps, p, 0, start, hk, hv, j0, s0);
@@ -471,9 +478,7 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
     __syncthreads();
 
     bool ok = true;
-    const int r = tid & 63;
-    float gx = 0.f, bx = 0.f;
-    if (nch > 0) load_gates(p, start, min(kC, len), hv, gx, bx);
+    const int r = row & 63;
     for (int c = 0; c < nch && ok; ++c) {
         const int st = c & 1;
         const uint32_t ph = c & 1;
@@ -488,29 +493,19 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         ok = wait_all(&S.bar_tma[st], (c >> 1) & 1);
         if (!ok) break;
         tc::fence_after_sync();
-
-        // per-token scalars
-        {
-            const float ss = row_sumsq(S.kq[st], tid, 16384);
-            const float f = p.l2norm ? rsqrtf(ss + 1e-6f) : 1.f;
-            if (tid < 64) S.nk[r] = r < L ? f : 0.f;
-            else S.nq[r] = r < L ? f : 0.f;
-        }
-        chunk_gates(gx, bx, S.gam, S.bet, &S.carry);
-        if (c + 1 < nch) load_gates(p, t0 + kC, min(kC, len - (c + 1) * kC), hv, gx, bx);
-        const float gL = S.gam[L - 1];
+        const float *sc = reinterpret_cast<const float *>(S.x[st] + kXTile);
+        const float *gam = sc, *bet = sc + 64, *nk = sc + 128, *nq = sc + 192;
+        const float gL = gam[L - 1];
 
         // h: bf16 copy for the MMA, then scale the fp32 master by e^{gamma_L}
         {
-            float h[64];
-            tmem_row64(tmem + lane_off + colH, h);
-            pack_row64(S.hb, tid, h);
-            const float aL = expf(gL);
-            float a[32], b[32];
+            float h[32];
+            tmem_row32(tmem + lane_off + colH + ch, h);
+            pack_row<32>(S.hb, row, half * 4, h);
+            const float aL = __expf(gL);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) { a[i] = aL * h[i]; b[i] = aL * h[32 + i]; }
-            tc::tmem_st32(tmem + lane_off + colH, a);
-            tc::tmem_st32(tmem + lane_off + colH + 32, b);
+            for (int i = 0; i < 32; ++i) h[i] *= aL;
+            tc::tmem_st32(tmem + lane_off + colH + ch, h);
             tc::tmem_wait_st();
         }
         tc::fence_async_smem();
@@ -531,28 +526,28 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         if (!ok) break;
         tc::fence_after_sync();
 
-        // keep = R (rows 0..63) or e^gamma nq Q h (rows 64..127), fp32
-        float keep[64];
+        // keep = R (rows 0..63) or e^gamma nq Q h (rows 64..127), fp32, 32 columns
+        float keep[32];
         {
-            float d1[64];
-            tmem_row64(tmem + lane_off + colD1, d1);
-            if (tid < 64) {
-                const float br = S.bet[r];
-                const float cr = expf(S.gam[r]) * S.nk[r];
+            float d1[32];
+            tmem_row32(tmem + lane_off + colD1 + ch, d1);
+            if (row < 64) {
+                const float br = bet[r];
+                const float cr = __expf(gam[r]) * nk[r];
                 const bool live = r < L;
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
+                for (int cc = 0; cc < 4; ++cc) {
                     float vv[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(S.v[st] + tc::swz(r, cc)), vv);
+                    unpack8(*reinterpret_cast<const uint4 *>(S.v[st] + tc::swz(r, half * 4 + cc)), vv);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         keep[8 * cc + e] = live ? br * (vv[e] - cr * d1[8 * cc + e]) : 0.f;
                 }
-                pack_row64(S.rb, r, keep);
+                pack_row<32>(S.rb, r, half * 4, keep);
             } else {
-                const float cq = expf(S.gam[r]) * S.nq[r];
+                const float cq = __expf(gam[r]) * nq[r];
 #pragma unroll
-                for (int j = 0; j < 64; ++j) keep[j] = cq * d1[j];
+                for (int j = 0; j < 32; ++j) keep[j] = cq * d1[j];
             }
         }
         tc::fence_async_smem();
@@ -572,25 +567,25 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         if (!ok) break;
         tc::fence_after_sync();
         {
-            float d2[64];
-            tmem_row64(tmem + lane_off + colD2, d2);
-            if (tid < 64) {
-                const float dc = r < L ? expf(gL - S.gam[r]) * S.nk[r] : 0.f;
-                float hi[64], lo[64];
+            float d2[32];
+            tmem_row32(tmem + lane_off + colD2 + ch, d2);
+            if (row < 64) {
+                const float dc = r < L ? __expf(gL - gam[r]) * nk[r] : 0.f;
+                float hi[32], lo[32];
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
+                for (int j = 0; j < 32; ++j) {
                     const float x = dc * (keep[j] + d2[j]);
                     const float xh = __bfloat162float(__float2bfloat16_rn(x));
                     hi[j] = xh;
                     lo[j] = x - xh;
                 }
-                pack_row64(S.dvh, r, hi);
-                pack_row64(S.dvl, r, lo);
+                pack_row<32>(S.dvh, r, half * 4, hi);
+                pack_row<32>(S.dvl, r, half * 4, lo);
             } else if (r < L) {
                 uint4 *dst = reinterpret_cast<uint4 *>(p.o + (size_t)(t0 + r) * p.o_tok +
-                                                       (size_t)hv * kD + j0);
+                                                       (size_t)hv * kD + j0 + ch);
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
+                for (int cc = 0; cc < 4; ++cc) {
                     float f[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) f[e] = p.scale * (keep[8 * cc + e] + d2[8 * cc + e]);
@@ -620,11 +615,11 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
     if (ok && nch > 0) ok = wait_all(&S.bar_d3, (nch - 1) & 1);
     if (ok && p.hT) {
         tc::fence_after_sync();
-        float h[64];
-        tmem_row64(tmem + lane_off + colH, h);
-        float4 *dst = reinterpret_cast<float4 *>(p.hT + hoff + (size_t)tid * kD + j0);
+        float h[32];
+        tmem_row32(tmem + lane_off + colH + ch, h);
+        float4 *dst = reinterpret_cast<float4 *>(p.hT + hoff + (size_t)row * kD + j0 + ch);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < 8; ++i)
             dst[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
     }
     if (!ok && tid == 0) report(p.status, GDN_ERR_TIMEOUT);
@@ -679,7 +674,7 @@ bool chunk_tc_supported(int32_t dk, int32_t dv, int32_t chunk, int in_f32) {
 size_t chunk_tc_workspace(int32_t N, int64_t T, int32_t Hk, int32_t Hv) {
     (void)Hk;
     const size_t slots = (size_t)((T + gdn::kC - 1) / gdn::kC) + (size_t)N + 1;
-    return slots * (size_t)Hv * gdn::kXTile;
+    return slots * (size_t)Hv * gdn::kWsTile;
 }
 
 gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStream_t st) {
@@ -719,11 +714,11 @@ gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStre
     }
     const int slots = (int)((a.T + gdn::kC - 1) / gdn::kC) + a.N;
     if (slots > 0) {
-        dim3 g1(slots, a.Hk);
-        gdn::chunk_prep_kernel<<<g1, gdn::kTcThreads, prep_smem, st>>>(maps, p);
+        dim3 g1(slots, a.Hv);
+        gdn::chunk_prep_kernel<<<g1, gdn::kPrepThreads, prep_smem, st>>>(maps, p);
     }
     dim3 g2(gdn::kD / gdn::kDVT, a.Hv, a.N);
-    gdn::chunk_state_kernel<<<g2, gdn::kTcThreads, state_smem, st>>>(maps, p);
+    gdn::chunk_state_kernel<<<g2, gdn::kStateThreads, state_smem, st>>>(maps, p);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

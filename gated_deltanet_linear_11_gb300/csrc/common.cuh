@@ -30,7 +30,9 @@ __device__ __forceinline__ uint4 pack8(const float f[8]) {
     return u;
 }
 
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+// SiLU with the fast exponential and divide intrinsics: the result is rounded to bf16,
+// whose unit roundoff (2^-9) is far above the intrinsics' error.
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 template <typename T> __device__ __forceinline__ float to_f32(T x);
 template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
@@ -49,8 +51,8 @@ __device__ __forceinline__ void report(int32_t *status, int32_t code) {
 
 // Host-side launch helpers (defined in api.cu).
 namespace gdn_host {
-gdn_status_t launch_conv1d_fwd(const void *x, int32_t C, const void *w, const void *bias,
-                               const int32_t *cu, int32_t N, int32_t max_len,
+gdn_status_t launch_conv1d_fwd(const void *x, int64_t T, int32_t C, const void *w,
+                               const void *bias, const int32_t *cu, int32_t N,
                                const void *s_in, void *s_out, void *y, cudaStream_t st);
 gdn_status_t launch_conv1d_update(const void *x, int32_t N, int32_t C, const void *w,
                                   const void *bias, void *state, int32_t P,
