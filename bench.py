@@ -65,6 +65,24 @@ def decode_bytes(N, Hk, Hv, dk, dv, C):
     return state + act + conv, state
 
 
+def kernel_traffic(src_name):
+    """DRAM bytes per launch (read + write) from the last ncu capture of a kernel file,
+    if that capture was taken from the current source (matched by sha1), else None."""
+    import hashlib
+    src = os.path.join(ROOT, "gated_deltanet_linear_11_gb300", "csrc", src_name)
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(src, "rb") as f:
+            digest = hashlib.sha1(f.read()).hexdigest()
+        with open(path) as f:
+            rec = json.load(f).get(src_name)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("sha1") != digest:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     out = dict(FALLBACK_PEAKS)
@@ -309,7 +327,7 @@ def run_ours(args, world, rank, local):
                                "achieved": dec_b / (ddec_ms * 1e-3) / 1e9,
                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                "frac": dec_b / (ddec_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                               "traffic": None}}
+                               "traffic": kernel_traffic("decode.cu")}}
 
     e2e = None
     if "e2e" in legs:
@@ -376,7 +394,8 @@ def run_ours(args, world, rank, local):
             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
             "frac": achieved_tf / peaks["bf16_tflops"],
             "peak_source": "%s (bf16 dense burst)" % peaks["source"],
-            "traffic": None,
+            "traffic": kernel_traffic("chunk_tc.cu"),
+            "traffic_note": "dram bytes of prep + state kernels per launch pair (ncu)",
             "algorithmic_flops_per_launch": flops,
             "algorithmic_bytes_per_launch": scan_b,
             "hbm_gbs_equiv": scan_b / (scan_avg * 1e-3) / 1e9}

@@ -99,8 +99,10 @@ gdn_status_t gdn_conv1d_fwd(const void *x, int64_t T, int32_t C, const void *w,
     int32_t max_len = 0;
     gdn_status_t s = check_seqlens(cu_seqlens_host, N, T, &max_len);
     if (s != GDN_OK) return s;
-    return gdn_host::launch_conv1d_fwd(x, T, C, w, bias, cu_seqlens_dev, N, conv_state_in,
-                                       conv_state_out, y, (cudaStream_t)stream);
+    if ((max_len + 15) / 16 > 65535) return GDN_ERR_SHAPE;
+    return gdn_host::launch_conv1d_fwd(x, C, w, bias, cu_seqlens_dev, N, max_len,
+                                       conv_state_in, conv_state_out, y,
+                                       (cudaStream_t)stream);
 }
 
 gdn_status_t gdn_conv1d_update(const void *x, int32_t N, int32_t C, const void *w,

@@ -137,12 +137,40 @@ __device__ __forceinline__ float row_sumsq(const uint8_t *tile, int row, uint32_
 }
 
 // ------------------------------------------------------------------ Tinv (fp32)
-// T = (I + A)^{-1} for a 64x64 strictly lower A (row stride 65), by 16x16 blocks:
-// diagonal blocks by forward substitution (one thread per column), then block rows
-// i = 1..3 from  T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.  All 128 threads call this.
-__device__ void tinv64(float (*A)[65], float (*T)[65], float (*Y)[65]) {
+// T = (I + A)^{-1} for a 64x64 strictly lower A, row stride kLd (even, for float2 loads),
+// by 16x16 blocks.  With T_ii the inverses of the diagonal blocks (I + A_ii) and, for the
+// two 32x32 halves, T0 = [[T00,0],[T10,T11]], T1 = [[T22,0],[T32,T33]]:
+//     T10 = -T11 A10 T00,   T32 = -T33 A32 T22,
+//     [T20 T21; T30 T31] = -T1 [A20 A21; A30 A31] T0.
+// Every product is a 16x16 block computed by 64 threads holding 2x2 register tiles.
+// All 128 threads call this; Y is a scratch of the same shape.
+constexpr int kLd = 66;
+
+// acc += A[ar.., ac..] (16x16) * B[br.., bc..] (16x16) for this thread's 2x2 tile.
+__device__ __forceinline__ void blk_mma(float (&acc)[2][2], const float (*A)[kLd], int ar, int ac,
+                                        const float (*B)[kLd], int br, int bc, int tr, int tc) {
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        const float a0 = A[ar + 2 * tr][ac + m], a1 = A[ar + 2 * tr + 1][ac + m];
+        const float2 bb = *reinterpret_cast<const float2 *>(&B[br + m][bc + 2 * tc]);
+        acc[0][0] = fmaf(a0, bb.x, acc[0][0]);
+        acc[0][1] = fmaf(a0, bb.y, acc[0][1]);
+        acc[1][0] = fmaf(a1, bb.x, acc[1][0]);
+        acc[1][1] = fmaf(a1, bb.y, acc[1][1]);
+    }
+}
+
+__device__ __forceinline__ void blk_store(float (*D)[kLd], int dr, int dc, int tr, int tc,
+                                          const float (&acc)[2][2], float sgn) {
+    *reinterpret_cast<float2 *>(&D[dr + 2 * tr][dc + 2 * tc]) = make_float2(sgn * acc[0][0], sgn * acc[0][1]);
+    *reinterpret_cast<float2 *>(&D[dr + 2 * tr + 1][dc + 2 * tc]) = make_float2(sgn * acc[1][0], sgn * acc[1][1]);
+}
+
+__device__ void tinv64(const float (*A)[kLd], float (*T)[kLd], float (*Y)[kLd]) {
     const int tid = threadIdx.x;
+    const int half = tid >> 6, t = tid & 63, tr = t >> 3, tc = t & 7;
     if (tid < 64) {
+        // diagonal blocks by forward substitution, one column per thread
         const int b = tid >> 4, j = tid & 15, o = 16 * b;
         float x[16];
 #pragma unroll
@@ -151,68 +179,76 @@ __device__ void tinv64(float (*A)[65], float (*T)[65], float (*Y)[65]) {
         for (int r = 1; r < 16; ++r) {
             float acc = x[r];
 #pragma unroll
-            for (int s = 0; s < r; ++s) acc = fmaf(-A[o + r][o + s], x[s], acc);
+            for (int q = 0; q < r; ++q) acc = fmaf(-A[o + r][o + q], x[q], acc);
             x[r] = acc;
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) T[o + r][o + j] = x[r];
-    } else {
-        // zero the blocks above the diagonal
-        for (int e = tid - 64; e < 64 * 64; e += 64) {
-            const int r = e >> 6, c = e & 63;
-            if ((c >> 4) > (r >> 4)) T[r][c] = 0.f;
-        }
     }
     __syncthreads();
-    // Each thread computes two adjacent columns of one output row per pass.
-    for (int i = 1; i < 4; ++i) {
-        // Y_j = sum_{k=j}^{i-1} A_ik T_kj   for j < i   (16x16 each)
-        for (int e = tid; e < i * 128; e += kPrepThreads) {
-            const int j = e >> 7, rr = (e >> 3) & 15, cc = (e & 7) * 2;
-            float a0 = 0.f, a1 = 0.f;
-            for (int k = j; k < i; ++k) {
-#pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const float av = A[16 * i + rr][16 * k + m];
-                    a0 = fmaf(av, T[16 * k + m][16 * j + cc], a0);
-                    a1 = fmaf(av, T[16 * k + m][16 * j + cc + 1], a1);
-                }
-            }
-            Y[16 * j + rr][cc] = a0;
-            Y[16 * j + rr][cc + 1] = a1;
-        }
-        __syncthreads();
-        for (int e = tid; e < i * 128; e += kPrepThreads) {
-            const int j = e >> 7, rr = (e >> 3) & 15, cc = (e & 7) * 2;
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const float tv = T[16 * i + rr][16 * i + m];
-                a0 = fmaf(tv, Y[16 * j + m][cc], a0);
-                a1 = fmaf(tv, Y[16 * j + m][cc + 1], a1);
-            }
-            T[16 * i + rr][16 * j + cc] = -a0;
-            T[16 * i + rr][16 * j + cc + 1] = -a1;
-        }
-        __syncthreads();
+    {   // X = A10 T00 (half 0) and A32 T22 (half 1), into Y rows 32.. and 48..
+        float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        const int o = 32 * half;
+        blk_mma(acc, A, o + 16, o, T, o, o, tr, tc);
+        blk_store(Y, 32 + 16 * half, 0, tr, tc, acc, 1.f);
     }
+    __syncthreads();
+    {   // T10 = -T11 X,  T32 = -T33 X
+        float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        const int o = 32 * half;
+        blk_mma(acc, T, o + 16, o + 16, Y, 32 + 16 * half, 0, tr, tc);
+        blk_store(T, o + 16, o, tr, tc, acc, -1.f);
+    }
+    __syncthreads();
+    {   // Z = [A20 A21; A30 A31] T0 into Y[0:32][0:32]; half h makes block row h
+        const int ar = 32 + 16 * half;
+        float z0[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, z1[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        blk_mma(z0, A, ar, 0, T, 0, 0, tr, tc);     // A_r0 T00
+        blk_mma(z0, A, ar, 16, T, 16, 0, tr, tc);   // + A_r1 T10
+        blk_mma(z1, A, ar, 16, T, 16, 16, tr, tc);  // A_r1 T11
+        blk_store(Y, 16 * half, 0, tr, tc, z0, 1.f);
+        blk_store(Y, 16 * half, 16, tr, tc, z1, 1.f);
+    }
+    __syncthreads();
+    {   // [T20 T21; T30 T31] = -T1 Z; half h makes block row 2 + h
+        float w0[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, w1[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        if (half == 0) {
+            blk_mma(w0, T, 32, 32, Y, 0, 0, tr, tc);    // T22 Z20
+            blk_mma(w1, T, 32, 32, Y, 0, 16, tr, tc);   // T22 Z21
+        } else {
+            blk_mma(w0, T, 48, 32, Y, 0, 0, tr, tc);    // T32 Z20
+            blk_mma(w0, T, 48, 48, Y, 16, 0, tr, tc);   // + T33 Z30
+            blk_mma(w1, T, 48, 32, Y, 0, 16, tr, tc);   // T32 Z21
+            blk_mma(w1, T, 48, 48, Y, 16, 16, tr, tc);  // + T33 Z31
+        }
+        blk_store(T, 32 + 16 * half, 0, tr, tc, w0, -1.f);
+        blk_store(T, 32 + 16 * half, 16, tr, tc, w1, -1.f);
+    }
+    __syncthreads();
 }
 
 // ================================================================ chunk_prep kernel
 
 struct PrepSmem {
-    uint8_t kq[32768];       // [K;Q] K-major, 2 K blocks of [128 rows][128 B]
-    uint8_t x[kXTile];       // [Lo ; M]
-    float A[64][65];
-    float T[64][65];
-    float Y[64][65];
+    // [K;Q] K-major tile (2 K blocks of [128 rows][128 B]); once P = [K;Q]K^T and the norms
+    // are taken it is dead and holds the inverse's scratch Y.
+    union {
+        uint8_t kq[32768];
+        float Y[64][kLd];
+    };
+    // A (fp32) until the inverse is done, then the bf16 tile X = [Lo ; M].
+    union {
+        float A[64][kLd];
+        uint8_t x[kXTile];
+    };
+    float T[64][kLd];
     float gam[64], bet[64], nk[64], nq[64];
     float carry;
     uint64_t bar_tma, bar_mma;
     uint32_t tmem;
 };
 
-__global__ void __launch_bounds__(kPrepThreads)
+__global__ void __launch_bounds__(kPrepThreads, 3)
 chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     PrepSmem &S = *reinterpret_cast<PrepSmem *>(
@@ -301,6 +337,7 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
             S.nq[r] = r < L ? f : 0.f;
         }
     }
+    // (this wait also orders the norm reads of kq before its reuse as Y)
     if (ok) ok = wait_all(&S.bar_mma, 0);
     float P[64];
     if (ok) {
@@ -321,7 +358,6 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
 #pragma unroll
             for (int s = 0; s < 64; ++s)
                 Mrow[s] = (s <= r && r < L) ? nr * __expf(gr - S.gam[s]) * S.nk[s] * P[s] : 0.f;
-            pack_row<64>(S.x, tid, 0, Mrow);
         }
         // per-token scalars for the state kernel
         float *ws_s = reinterpret_cast<float *>(wtile + kXTile);
@@ -334,17 +370,21 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
         }
     }
     __syncthreads();
-    if (ok) tinv64(S.A, S.T, S.Y);
-    if (ok && tid < 64) {
-        float lrow[64];
+    if (ok) tinv64(S.A, S.T, S.Y);   // ends with a barrier: A is dead from here
+    if (ok) {
+        if (tid < 64) {
+            float lrow[64];
 #pragma unroll
-        for (int t = 0; t < 64; ++t) lrow[t] = (t == r) ? 0.f : S.T[r][t];
-        pack_row<64>(S.x, tid, 0, lrow);
-        // Lo rows go to the workspace as they are
+            for (int t = 0; t < 64; ++t) lrow[t] = (t < r) ? S.T[r][t] : 0.f;
+            pack_row<64>(S.x, tid, 0, lrow);
+            // Lo rows go to the workspace as they are
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-            *reinterpret_cast<uint4 *>(wtile + tc::swz(tid, cc)) =
-                *reinterpret_cast<const uint4 *>(S.x + tc::swz(tid, cc));
+            for (int cc = 0; cc < 8; ++cc)
+                *reinterpret_cast<uint4 *>(wtile + tc::swz(tid, cc)) =
+                    *reinterpret_cast<const uint4 *>(S.x + tc::swz(tid, cc));
+        } else {
+            pack_row<64>(S.x, tid, 0, Mrow);
+        }
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
@@ -416,6 +456,12 @@ __device__ __forceinline__ void issue_chunk_loads(StateSmem &S, const TcMaps &ma
                     "r"(tc::smem_u32(bar)) : "memory");
 }
 
+// Named barrier over the four warps that own TMEM lanes 0..63 (warps 0, 1, 4, 5): the rows
+// that feed the state chain.  The other four warps only produce outputs.
+__device__ __forceinline__ void chain_barrier() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kStateThreads, 1)
 chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -425,6 +471,7 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
     const int quad = warp & 3;           // TMEM lane quarter
     const int half = warp >> 2;          // which 32 of the 64 dv columns
     const int row = quad * 32 + lane;    // TMEM lane = tile row
+    const bool chain = quad < 2;         // rows 0..63: tokens of the chain / dk rows 0..63
     const int jt = blockIdx.x, hv = blockIdx.y, n = blockIdx.z;
     const int hk = hv / (p.Hv / p.Hk);
     const int j0 = jt * kDVT;
@@ -454,63 +501,49 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
     const uint32_t tmem = S.tmem;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t ch = half * 32;       // this thread's column offset
-    const uint32_t colH = 0, colD1 = 64, colD2 = 128;
+    const uint32_t colS = 0, colD1 = 64, colD2 = 128;
 
-    // Initial state: thread (row, half) holds dk row `row`, columns ch..ch+31.
-    {
-        float h[32];
-        if (p.h0) {
-            const float4 *src = reinterpret_cast<const float4 *>(p.h0 + hoff + (size_t)row * kD + j0 + ch);
+    // fp32 master state in registers: dk row `row`, dv columns j0+ch .. +31.
+    float h[32];
+    if (p.h0) {
+        const float4 *src = reinterpret_cast<const float4 *>(p.h0 + hoff + (size_t)row * kD + j0 + ch);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 f = src[i];
-                h[4 * i] = f.x; h[4 * i + 1] = f.y; h[4 * i + 2] = f.z; h[4 * i + 3] = f.w;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) h[i] = 0.f;
+        for (int i = 0; i < 8; ++i) {
+            const float4 f = src[i];
+            h[4 * i] = f.x; h[4 * i + 1] = f.y; h[4 * i + 2] = f.z; h[4 * i + 3] = f.w;
         }
-        tc::tmem_st32(tmem + lane_off + colH + ch, h);
-        tc::tmem_wait_st();
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) h[i] = 0.f;
     }
     if (tid == 0 && nch > 0) issue_chunk_loads(S, maps, p, 0, start, hk, hv, j0, s0);
-    tc::fence_before_sync();
-    __syncthreads();
 
     bool ok = true;
     const int r = row & 63;
+    float aL_prev = 1.f;   // e^{gamma_L} of the previous chunk
     for (int c = 0; c < nch && ok; ++c) {
         const int st = c & 1;
         const uint32_t ph = c & 1;
         const int t0 = start + c * kC;
         const int L = min(kC, len - c * kC);
+
+        // --- A: fold the previous chunk's update into h, publish the bf16 copy
         if (c > 0) {
-            ok = wait_all(&S.bar_d3, ph ^ 1);  // previous chunk's state update done
+            ok = wait_all(&S.bar_d3, ph ^ 1);
             if (!ok) break;
+            tc::fence_after_sync();
+            float ds[32];
+            tmem_row32(tmem + lane_off + colS + ch, ds);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) h[i] = fmaf(aL_prev, h[i], ds[i]);
         }
         if (tid == 0 && c + 1 < nch)
             issue_chunk_loads(S, maps, p, st ^ 1, t0 + kC, hk, hv, j0, s0 + c + 1);
-        ok = wait_all(&S.bar_tma[st], (c >> 1) & 1);
-        if (!ok) break;
-        tc::fence_after_sync();
-        const float *sc = reinterpret_cast<const float *>(S.x[st] + kXTile);
-        const float *gam = sc, *bet = sc + 64, *nk = sc + 128, *nq = sc + 192;
-        const float gL = gam[L - 1];
-
-        // h: bf16 copy for the MMA, then scale the fp32 master by e^{gamma_L}
-        {
-            float h[32];
-            tmem_row32(tmem + lane_off + colH + ch, h);
-            pack_row<32>(S.hb, row, half * 4, h);
-            const float aL = __expf(gL);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) h[i] *= aL;
-            tc::tmem_st32(tmem + lane_off + colH + ch, h);
-            tc::tmem_wait_st();
-        }
+        pack_row<32>(S.hb, row, half * 4, h);
         tc::fence_async_smem();
         tc::fence_before_sync();
-        __syncthreads();
+        ok = wait_all(&S.bar_tma[st], (c >> 1) & 1);   // also the barrier for hb
+        if (!ok) break;
         if (tid == 0) {
             tc::fence_after_sync();
             constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
@@ -522,18 +555,22 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
                              tc::sdesc(hbb + ks * 2048, 8192, 1024), id, ks > 0);
             tc::mma_commit(&S.bar_d1);
         }
+        const float *sc = reinterpret_cast<const float *>(S.x[st] + kXTile);
+        const float *gam = sc, *bet = sc + 64, *nk = sc + 128, *nq = sc + 192;
+        const float gL = gam[L - 1];
+        const float gr = gam[r];
+
+        // --- B: R = beta (V - e^gamma nk K h) on the chain rows; e^gamma nq Q h on the rest
         ok = wait_all(&S.bar_d1, ph);
         if (!ok) break;
         tc::fence_after_sync();
-
-        // keep = R (rows 0..63) or e^gamma nq Q h (rows 64..127), fp32, 32 columns
         float keep[32];
         {
             float d1[32];
             tmem_row32(tmem + lane_off + colD1 + ch, d1);
-            if (row < 64) {
+            if (chain) {
                 const float br = bet[r];
-                const float cr = __expf(gam[r]) * nk[r];
+                const float cr = __expf(gr) * nk[r];
                 const bool live = r < L;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
@@ -544,33 +581,35 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
                         keep[8 * cc + e] = live ? br * (vv[e] - cr * d1[8 * cc + e]) : 0.f;
                 }
                 pack_row<32>(S.rb, r, half * 4, keep);
+                tc::fence_async_smem();
+                tc::fence_before_sync();
+                chain_barrier();
+                if (tid == 0) {
+                    tc::fence_after_sync();
+                    constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
+                    const uint32_t xb = tc::smem_u32(S.x[st]), rbb = tc::smem_u32(S.rb);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc::mma_bf16(tmem + colD2, tc::sdesc(xb + ks * 32, 16, 1024),
+                                     tc::sdesc(rbb + ks * 2048, 8192, 1024), id, ks > 0);
+                    tc::mma_commit(&S.bar_d2);
+                }
             } else {
-                const float cq = __expf(gam[r]) * nq[r];
+                const float cq = __expf(gr) * nq[r];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) keep[j] = cq * d1[j];
             }
         }
-        tc::fence_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            tc::fence_after_sync();
-            constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
-            const uint32_t xb = tc::smem_u32(S.x[st]), rbb = tc::smem_u32(S.rb);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tmem + colD2, tc::sdesc(xb + ks * 32, 16, 1024),
-                             tc::sdesc(rbb + ks * 2048, 8192, 1024), id, ks > 0);
-            tc::mma_commit(&S.bar_d2);
-        }
+
+        // --- C: Vn = R + Lo R -> d Vn as bf16 hi + lo; outputs on the other rows
         ok = wait_all(&S.bar_d2, ph);
         if (!ok) break;
         tc::fence_after_sync();
         {
             float d2[32];
             tmem_row32(tmem + lane_off + colD2 + ch, d2);
-            if (row < 64) {
-                const float dc = r < L ? __expf(gL - gam[r]) * nk[r] : 0.f;
+            if (chain) {
+                const float dc = r < L ? __expf(gL - gr) * nk[r] : 0.f;
                 float hi[32], lo[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
@@ -581,6 +620,24 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
                 }
                 pack_row<32>(S.dvh, r, half * 4, hi);
                 pack_row<32>(S.dvl, r, half * 4, lo);
+                tc::fence_async_smem();
+                tc::fence_before_sync();
+                chain_barrier();
+                if (tid == 0) {
+                    tc::fence_after_sync();
+                    constexpr uint32_t id = tc::idesc_bf16(128, 64, 1, 1);
+                    const uint32_t kqb = tc::smem_u32(S.kq[st]);
+                    const uint32_t hb = tc::smem_u32(S.dvh), lb = tc::smem_u32(S.dvl);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc::mma_bf16(tmem + colS, tc::sdesc(kqb + ks * 2048, 16384, 1024),
+                                     tc::sdesc(hb + ks * 2048, 8192, 1024), id, ks > 0);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc::mma_bf16(tmem + colS, tc::sdesc(kqb + ks * 2048, 16384, 1024),
+                                     tc::sdesc(lb + ks * 2048, 8192, 1024), id, 1);
+                    tc::mma_commit(&S.bar_d3);
+                }
             } else if (r < L) {
                 uint4 *dst = reinterpret_cast<uint4 *>(p.o + (size_t)(t0 + r) * p.o_tok +
                                                        (size_t)hv * kD + j0 + ch);
@@ -593,30 +650,19 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
                 }
             }
         }
-        tc::fence_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
+        aL_prev = __expf(gL);
+    }
+    if (ok && nch > 0) {
+        ok = wait_all(&S.bar_d3, (nch - 1) & 1);
+        if (ok) {
             tc::fence_after_sync();
-            constexpr uint32_t id = tc::idesc_bf16(128, 64, 1, 1);
-            const uint32_t kqb = tc::smem_u32(S.kq[st]);
-            const uint32_t hb = tc::smem_u32(S.dvh), lb = tc::smem_u32(S.dvl);
+            float ds[32];
+            tmem_row32(tmem + lane_off + colS + ch, ds);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tmem + colH, tc::sdesc(kqb + ks * 2048, 16384, 1024),
-                             tc::sdesc(hb + ks * 2048, 8192, 1024), id, 1);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tmem + colH, tc::sdesc(kqb + ks * 2048, 16384, 1024),
-                             tc::sdesc(lb + ks * 2048, 8192, 1024), id, 1);
-            tc::mma_commit(&S.bar_d3);
+            for (int i = 0; i < 32; ++i) h[i] = fmaf(aL_prev, h[i], ds[i]);
         }
     }
-    if (ok && nch > 0) ok = wait_all(&S.bar_d3, (nch - 1) & 1);
     if (ok && p.hT) {
-        tc::fence_after_sync();
-        float h[32];
-        tmem_row32(tmem + lane_off + colH + ch, h);
         float4 *dst = reinterpret_cast<float4 *>(p.hT + hoff + (size_t)row * kD + j0 + ch);
 #pragma unroll
         for (int i = 0; i < 8; ++i)

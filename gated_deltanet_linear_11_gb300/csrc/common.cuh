@@ -51,8 +51,8 @@ __device__ __forceinline__ void report(int32_t *status, int32_t code) {
 
 // Host-side launch helpers (defined in api.cu).
 namespace gdn_host {
-gdn_status_t launch_conv1d_fwd(const void *x, int64_t T, int32_t C, const void *w,
-                               const void *bias, const int32_t *cu, int32_t N,
+gdn_status_t launch_conv1d_fwd(const void *x, int32_t C, const void *w, const void *bias,
+                               const int32_t *cu, int32_t N, int32_t max_len,
                                const void *s_in, void *s_out, void *y, cudaStream_t st);
 gdn_status_t launch_conv1d_update(const void *x, int32_t N, int32_t C, const void *w,
                                   const void *bias, void *state, int32_t P,

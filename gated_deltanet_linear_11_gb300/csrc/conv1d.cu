@@ -14,7 +14,8 @@
 namespace gdn {
 
 constexpr int kConvThreads = 128;   // threads per block, 8 channels each
-constexpr int kConvGroup = 4;       // token rows loaded together; the next group is in flight
+constexpr int kConvTile = 16;       // tokens per thread (anchored at the sequence start)
+constexpr int kConvGroup = 4;       // tokens loaded together; the next group is in flight
 
 struct Taps {
     float w[8][4];
@@ -54,89 +55,59 @@ __device__ __forceinline__ uint4 conv_out(const Taps &tp, const float x0[8], con
     return pack8(r);
 }
 
-// Prefill conv.  Block b owns the 1024-channel strip b % ncb and an even share of the
-// T packed token rows, so every block streams the same number of bytes whatever the
-// sequence lengths.  A thread walks its rows in order with a 3-row window, resetting the
-// window from the sequence's conv state (or zeros) at every sequence start; loads of
-// the next group of rows are issued before the current group is computed.  Each output
-// depends only on its own sequence's rows and the fixed tap order, never on the split.
-// grid: ncb * parts blocks.
+// grid: (ceil(C / (8*kConvThreads)), ceil(max_len / kConvTile) (>=1), N)
 __global__ void __launch_bounds__(kConvThreads, 4)
 conv1d_fwd_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
-                  const bf16 *__restrict__ bias, const int32_t *__restrict__ cu, int N,
-                  int64_t T, const bf16 *__restrict__ s_in, bf16 *__restrict__ y, int C,
-                  int ncb, int parts) {
-    const int strip = blockIdx.x % ncb;
-    const int part = blockIdx.x / ncb;
-    const int c0 = (strip * kConvThreads + threadIdx.x) * 8;
+                  const bf16 *__restrict__ bias, const int32_t *__restrict__ cu,
+                  const bf16 *s_in, bf16 *s_out, bf16 *__restrict__ y, int C) {
+    const int n = blockIdx.z;
+    const int tile = blockIdx.y;
+    const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * 8;
     if (c0 >= C) return;
-    const int64_t per = (T + parts - 1) / parts;
-    const int64_t t_begin = (int64_t)part * per;
-    const int64_t t_end = min(T, t_begin + per);
-    if (t_begin >= t_end) return;
+    const int start = cu[n];
+    const int L = cu[n + 1] - start;
+    const int t0 = tile * kConvTile;
+    if (t0 >= L && tile > 0) return;
 
     Taps tp;
     load_taps(tp, w, bias, c0);
 
-    // sequence of the first row: the last n with cu[n] <= t_begin (and a nonempty tail)
-    int lo = 0, hi = N - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (cu[mid] <= t_begin) lo = mid; else hi = mid - 1;
-    }
-    int n = lo;
-    int seq_start = cu[n], seq_end = cu[n + 1];
-    while (seq_end <= t_begin) {  // skip empty sequences ending here
-        ++n;
-        seq_start = cu[n];
-        seq_end = cu[n + 1];
-    }
-
+    // Window of the three conv inputs before token t0 (state rows when t0 - 3 + j < 0).
     float win[3][8];
-    auto window_from = [&](int64_t t) {
 #pragma unroll
-        for (int j = 0; j < 3; ++j) {
-            const int64_t p = t - 3 + j;
-            if (p >= seq_start) {
-                unpack8(*reinterpret_cast<const uint4 *>(x + (size_t)p * C + c0), win[j]);
-            } else if (s_in) {
-                const int row = 3 + (int)(p - seq_start);
-                unpack8(*reinterpret_cast<const uint4 *>(s_in + ((size_t)n * 3 + row) * C + c0), win[j]);
-            } else {
+    for (int j = 0; j < 3; ++j) {
+        const int p = t0 - 3 + j;
+        if (p >= 0) {
+            unpack8(*reinterpret_cast<const uint4 *>(x + (size_t)(start + p) * C + c0), win[j]);
+        } else if (s_in) {
+            unpack8(*reinterpret_cast<const uint4 *>(s_in + ((size_t)n * 3 + (3 + p)) * C + c0), win[j]);
+        } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) win[j][i] = 0.f;
-            }
+            for (int i = 0; i < 8; ++i) win[j][i] = 0.f;
         }
-    };
-    window_from(t_begin);
+    }
 
+    // Tokens are processed in groups of kConvGroup; the loads of group g+1 are issued
+    // before group g is computed, so a thread always has a group of rows in flight.
+    const int cnt = min(kConvTile, L - t0);
     uint4 cur_g[kConvGroup], nxt_g[kConvGroup];
 #pragma unroll
     for (int i = 0; i < kConvGroup; ++i)
-        if (t_begin + i < t_end) cur_g[i] = *reinterpret_cast<const uint4 *>(x + (size_t)(t_begin + i) * C + c0);
+        if (i < cnt) cur_g[i] = *reinterpret_cast<const uint4 *>(x + (size_t)(start + t0 + i) * C + c0);
 #pragma unroll 1
-    for (int64_t base = t_begin; base < t_end; base += kConvGroup) {
-        const int64_t nb = base + kConvGroup;
+    for (int base = 0; base < cnt; base += kConvGroup) {
+        const int nb = base + kConvGroup;
 #pragma unroll
         for (int i = 0; i < kConvGroup; ++i)
-            if (nb + i < t_end)
-                nxt_g[i] = *reinterpret_cast<const uint4 *>(x + (size_t)(nb + i) * C + c0);
+            if (nb + i < cnt)
+                nxt_g[i] = *reinterpret_cast<const uint4 *>(x + (size_t)(start + t0 + nb + i) * C + c0);
 #pragma unroll
         for (int i = 0; i < kConvGroup; ++i) {
-            const int64_t t = base + i;
-            if (t < t_end) {
-                if (t >= seq_end) {  // next sequence starts here (skipping empty ones)
-                    do {
-                        ++n;
-                        seq_start = cu[n];
-                        seq_end = cu[n + 1];
-                    } while (seq_end <= t);
-                    window_from(t);
-                }
+            if (base + i < cnt) {
                 float cur[8];
                 unpack8(cur_g[i], cur);
                 const uint4 out = conv_out(tp, win[0], win[1], win[2], cur);
-                *reinterpret_cast<uint4 *>(y + (size_t)t * C + c0) = out;
+                *reinterpret_cast<uint4 *>(y + (size_t)(start + t0 + base + i) * C + c0) = out;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     win[0][e] = win[1][e];
@@ -148,30 +119,22 @@ conv1d_fwd_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
 #pragma unroll
         for (int i = 0; i < kConvGroup; ++i) cur_g[i] = nxt_g[i];
     }
-}
 
-// New conv state of every sequence: xs = [old(3) ; x_seq], state = xs[L], xs[L+1], xs[L+2].
-// Runs after the conv kernel, so the old state has been read; row j is written after
-// old row L+j >= j was read by the same thread, so s_out == s_in is safe.
-// grid: (ceil(C / (8*kConvThreads)), N)
-__global__ void __launch_bounds__(kConvThreads)
-conv1d_tail_kernel(const bf16 *__restrict__ x, const int32_t *__restrict__ cu,
-                   const bf16 *s_in, bf16 *s_out, int C) {
-    const int n = blockIdx.y;
-    const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * 8;
-    if (c0 >= C) return;
-    const int start = cu[n];
-    const int L = cu[n + 1] - start;
+    // The first tile of a sequence is the only reader of the old conv state, so it also
+    // writes the new one.  xs = [old(3) ; x_seq]; the new state is xs[L], xs[L+1],
+    // xs[L+2].  Row j is written after old row L+j >= j was read, so s_out == s_in is safe.
+    if (tile == 0 && s_out) {
 #pragma unroll
-    for (int j = 0; j < 3; ++j) {
-        const int m = L + j;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (m >= 3) {
-            val = *reinterpret_cast<const uint4 *>(x + (size_t)(start + m - 3) * C + c0);
-        } else if (s_in) {
-            val = *reinterpret_cast<const uint4 *>(s_in + ((size_t)n * 3 + m) * C + c0);
+        for (int j = 0; j < 3; ++j) {
+            const int m = L + j;
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (m >= 3) {
+                val = *reinterpret_cast<const uint4 *>(x + (size_t)(start + m - 3) * C + c0);
+            } else if (s_in) {
+                val = *reinterpret_cast<const uint4 *>(s_in + ((size_t)n * 3 + m) * C + c0);
+            }
+            *reinterpret_cast<uint4 *>(s_out + ((size_t)n * 3 + j) * C + c0) = val;
         }
-        *reinterpret_cast<uint4 *>(s_out + ((size_t)n * 3 + j) * C + c0) = val;
     }
 }
 
@@ -233,33 +196,15 @@ conv1d_update_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
 
 namespace gdn_host {
 
-gdn_status_t launch_conv1d_fwd(const void *x, int64_t T, int32_t C, const void *w,
-                               const void *bias, const int32_t *cu, int32_t N,
+gdn_status_t launch_conv1d_fwd(const void *x, int32_t C, const void *w, const void *bias,
+                               const int32_t *cu, int32_t N, int32_t max_len,
                                const void *s_in, void *s_out, void *y, cudaStream_t st) {
     if (N == 0) return GDN_OK;
-    const int ncb = (C / 8 + gdn::kConvThreads - 1) / gdn::kConvThreads;
-    if (T > 0) {
-        static int sms = 0;
-        if (!sms) {
-            int dev = 0;
-            if (cudaGetDevice(&dev) != cudaSuccess ||
-                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-                return GDN_ERR_CUDA;
-        }
-        // 4 resident blocks per SM; every block gets the same share of rows
-        int parts = (sms * 4) / ncb;
-        if (parts < 1) parts = 1;
-        const int64_t max_parts = (T + gdn::kConvGroup - 1) / gdn::kConvGroup;
-        if (parts > max_parts) parts = (int)max_parts;
-        gdn::conv1d_fwd_kernel<<<ncb * parts, gdn::kConvThreads, 0, st>>>(
-            (const gdn::bf16 *)x, (const gdn::bf16 *)w, (const gdn::bf16 *)bias, cu, N, T,
-            (const gdn::bf16 *)s_in, (gdn::bf16 *)y, C, ncb, parts);
-    }
-    if (s_out) {
-        dim3 grid(ncb, N);
-        gdn::conv1d_tail_kernel<<<grid, gdn::kConvThreads, 0, st>>>(
-            (const gdn::bf16 *)x, cu, (const gdn::bf16 *)s_in, (gdn::bf16 *)s_out, C);
-    }
+    const int tiles = max_len > 0 ? (max_len + gdn::kConvTile - 1) / gdn::kConvTile : 1;
+    dim3 grid((C / 8 + gdn::kConvThreads - 1) / gdn::kConvThreads, tiles, N);
+    gdn::conv1d_fwd_kernel<<<grid, gdn::kConvThreads, 0, st>>>(
+        (const gdn::bf16 *)x, (const gdn::bf16 *)w, (const gdn::bf16 *)bias, cu,
+        (const gdn::bf16 *)s_in, (gdn::bf16 *)s_out, (gdn::bf16 *)y, C);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
