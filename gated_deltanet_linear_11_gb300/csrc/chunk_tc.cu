@@ -437,7 +437,24 @@ struct StateSmem {
     uint8_t dvl[8192];       // bf16 lo
     uint64_t bar_tma[2], bar_d1, bar_d2, bar_d3;
     uint32_t tmem;
+    int abort;               // set by the first thread whose wait runs out
 };
+
+// Bounded wait by one thread.  Gives up (false) when the phase has not completed within
+// kWaitNs, or as soon as another thread of the CTA has given up; the caller then skips
+// its work but keeps reaching every barrier, so the CTA still drains and exits.
+__device__ __forceinline__ bool wait_one(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = now_ns();
+    for (;;) {
+        if (tc::mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (now_ns() - t0 > kWaitNs) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
 
 __device__ __forceinline__ void issue_chunk_loads(StateSmem &S, const TcMaps &maps,
                                                   const TcParams &p, int stage, int t0,
@@ -490,6 +507,7 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         tc::mbar_init(&S.bar_d1, 1);
         tc::mbar_init(&S.bar_d2, 1);
         tc::mbar_init(&S.bar_d3, 1);
+        S.abort = 0;
         tc::mbar_fence_init();
         tc::prefetch_tmap(&maps.k);
         tc::prefetch_tmap(&maps.q);
@@ -502,6 +520,17 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t ch = half * 32;       // this thread's column offset
     const uint32_t colS = 0, colD1 = 64, colD2 = 128;
+    volatile int *abort = &S.abort;
+
+    // Shared-memory descriptors, built once; a byte offset o is added as o >> 4.
+    // Stage b of a double buffer sits b * (buffer bytes) after stage 0.
+    const uint64_t dKQ0 = tc::sdesc(tc::smem_u32(S.kq[0]), 16, 1024);      // [K;Q], K-major
+    const uint64_t dKQt0 = tc::sdesc(tc::smem_u32(S.kq[0]), 16384, 1024);  // K^T, MN-major
+    const uint64_t dX0 = tc::sdesc(tc::smem_u32(S.x[0]), 16, 1024);        // [Lo;Mt], K-major
+    const uint64_t dH = tc::sdesc(tc::smem_u32(S.hb), 8192, 1024);
+    const uint64_t dR = tc::sdesc(tc::smem_u32(S.rb), 8192, 1024);
+    const uint64_t dVh = tc::sdesc(tc::smem_u32(S.dvh), 8192, 1024);
+    const uint64_t dVl = tc::sdesc(tc::smem_u32(S.dvl), 8192, 1024);
 
     // fp32 master state in registers: dk row `row`, dv columns j0+ch .. +31.
     float h[32];
@@ -521,38 +550,37 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
     bool ok = true;
     const int r = row & 63;
     float aL_prev = 1.f;   // e^{gamma_L} of the previous chunk
-    for (int c = 0; c < nch && ok; ++c) {
+    for (int c = 0; c < nch; ++c) {
         const int st = c & 1;
         const uint32_t ph = c & 1;
         const int t0 = start + c * kC;
         const int L = min(kC, len - c * kC);
 
         // --- A: fold the previous chunk's update into h, publish the bf16 copy
-        if (c > 0) {
-            ok = wait_all(&S.bar_d3, ph ^ 1);
-            if (!ok) break;
-            tc::fence_after_sync();
-            float ds[32];
-            tmem_row32(tmem + lane_off + colS + ch, ds);
+        if (c > 0 && ok) {
+            ok = wait_one(&S.bar_d3, ph ^ 1, abort);
+            if (ok) {
+                tc::fence_after_sync();
+                float ds[32];
+                tmem_row32(tmem + lane_off + colS + ch, ds);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) h[i] = fmaf(aL_prev, h[i], ds[i]);
+                for (int i = 0; i < 32; ++i) h[i] = fmaf(aL_prev, h[i], ds[i]);
+            }
         }
-        if (tid == 0 && c + 1 < nch)
-            issue_chunk_loads(S, maps, p, st ^ 1, t0 + kC, hk, hv, j0, s0 + c + 1);
         pack_row<32>(S.hb, row, half * 4, h);
         tc::fence_async_smem();
         tc::fence_before_sync();
-        ok = wait_all(&S.bar_tma[st], (c >> 1) & 1);   // also the barrier for hb
-        if (!ok) break;
-        if (tid == 0) {
+        __syncthreads();
+        if (ok) ok = wait_one(&S.bar_tma[st], (c >> 1) & 1, abort);
+        if (tid == 0 && ok) {
             tc::fence_after_sync();
+            if (c + 1 < nch)
+                issue_chunk_loads(S, maps, p, st ^ 1, t0 + kC, hk, hv, j0, s0 + c + 1);
             constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
-            const uint32_t kqb = tc::smem_u32(S.kq[st]), hbb = tc::smem_u32(S.hb);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                tc::mma_bf16(tmem + colD1,
-                             tc::sdesc(kqb + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                             tc::sdesc(hbb + ks * 2048, 8192, 1024), id, ks > 0);
+                tc::mma_bf16(tmem + colD1, dKQ0 + ((st * 32768 + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                             dH + ((ks * 2048) >> 4), id, ks > 0);
             tc::mma_commit(&S.bar_d1);
         }
         const float *sc = reinterpret_cast<const float *>(S.x[st] + kXTile);
@@ -561,13 +589,17 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         const float gr = gam[r];
 
         // --- B: R = beta (V - e^gamma nk K h) on the chain rows; e^gamma nq Q h on the rest
-        ok = wait_all(&S.bar_d1, ph);
-        if (!ok) break;
-        tc::fence_after_sync();
+        if (ok) ok = wait_one(&S.bar_d1, ph, abort);
         float keep[32];
         {
             float d1[32];
-            tmem_row32(tmem + lane_off + colD1 + ch, d1);
+            if (ok) {
+                tc::fence_after_sync();
+                tmem_row32(tmem + lane_off + colD1 + ch, d1);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) d1[j] = 0.f;
+            }
             if (chain) {
                 const float br = bet[r];
                 const float cr = __expf(gr) * nk[r];
@@ -584,14 +616,13 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
                 tc::fence_async_smem();
                 tc::fence_before_sync();
                 chain_barrier();
-                if (tid == 0) {
+                if (tid == 0 && ok && !*abort) {
                     tc::fence_after_sync();
                     constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
-                    const uint32_t xb = tc::smem_u32(S.x[st]), rbb = tc::smem_u32(S.rb);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        tc::mma_bf16(tmem + colD2, tc::sdesc(xb + ks * 32, 16, 1024),
-                                     tc::sdesc(rbb + ks * 2048, 8192, 1024), id, ks > 0);
+                        tc::mma_bf16(tmem + colD2, dX0 + ((st * kXStage + ks * 32) >> 4),
+                                     dR + ((ks * 2048) >> 4), id, ks > 0);
                     tc::mma_commit(&S.bar_d2);
                 }
             } else {
@@ -602,12 +633,16 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         }
 
         // --- C: Vn = R + Lo R -> d Vn as bf16 hi + lo; outputs on the other rows
-        ok = wait_all(&S.bar_d2, ph);
-        if (!ok) break;
-        tc::fence_after_sync();
+        if (ok) ok = wait_one(&S.bar_d2, ph, abort);
         {
             float d2[32];
-            tmem_row32(tmem + lane_off + colD2 + ch, d2);
+            if (ok) {
+                tc::fence_after_sync();
+                tmem_row32(tmem + lane_off + colD2 + ch, d2);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) d2[j] = 0.f;
+            }
             if (chain) {
                 const float dc = r < L ? __expf(gL - gr) * nk[r] : 0.f;
                 float hi[32], lo[32];
@@ -623,22 +658,20 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
                 tc::fence_async_smem();
                 tc::fence_before_sync();
                 chain_barrier();
-                if (tid == 0) {
+                if (tid == 0 && ok && !*abort) {
                     tc::fence_after_sync();
                     constexpr uint32_t id = tc::idesc_bf16(128, 64, 1, 1);
-                    const uint32_t kqb = tc::smem_u32(S.kq[st]);
-                    const uint32_t hb = tc::smem_u32(S.dvh), lb = tc::smem_u32(S.dvl);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        tc::mma_bf16(tmem + colS, tc::sdesc(kqb + ks * 2048, 16384, 1024),
-                                     tc::sdesc(hb + ks * 2048, 8192, 1024), id, ks > 0);
+                        tc::mma_bf16(tmem + colS, dKQt0 + ((st * 32768 + ks * 2048) >> 4),
+                                     dVh + ((ks * 2048) >> 4), id, ks > 0);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        tc::mma_bf16(tmem + colS, tc::sdesc(kqb + ks * 2048, 16384, 1024),
-                                     tc::sdesc(lb + ks * 2048, 8192, 1024), id, 1);
+                        tc::mma_bf16(tmem + colS, dKQt0 + ((st * 32768 + ks * 2048) >> 4),
+                                     dVl + ((ks * 2048) >> 4), id, 1);
                     tc::mma_commit(&S.bar_d3);
                 }
-            } else if (r < L) {
+            } else if (r < L && ok) {
                 uint4 *dst = reinterpret_cast<uint4 *>(p.o + (size_t)(t0 + r) * p.o_tok +
                                                        (size_t)hv * kD + j0 + ch);
 #pragma unroll
@@ -653,7 +686,7 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         aL_prev = __expf(gL);
     }
     if (ok && nch > 0) {
-        ok = wait_all(&S.bar_d3, (nch - 1) & 1);
+        ok = wait_one(&S.bar_d3, (nch - 1) & 1, abort);
         if (ok) {
             tc::fence_after_sync();
             float ds[32];
@@ -662,15 +695,15 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
             for (int i = 0; i < 32; ++i) h[i] = fmaf(aL_prev, h[i], ds[i]);
         }
     }
-    if (ok && p.hT) {
+    tc::fence_before_sync();
+    __syncthreads();
+    if (!*abort && p.hT) {
         float4 *dst = reinterpret_cast<float4 *>(p.hT + hoff + (size_t)row * kD + j0 + ch);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             dst[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
     }
-    if (!ok && tid == 0) report(p.status, GDN_ERR_TIMEOUT);
-    tc::fence_before_sync();
-    __syncthreads();
+    if (*abort && tid == 0) report(p.status, GDN_ERR_TIMEOUT);
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
