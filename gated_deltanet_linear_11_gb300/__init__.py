@@ -163,7 +163,7 @@ def gdn_chunk_prefill_noalloc(q, k, v, g, beta, cu_seqlens, chunk=64, scale=1.0,
                               o=None, final_state=None, simt=False, cu_seqlens_host=None,
                               status=None):
     """gdn_chunk_prefill for callers that cannot allocate device scratch: the library
-    uses its own fixed 64 MiB device array instead of a workspace (see include/gdn.h).
+    uses its own fixed 128 MiB device array instead of a workspace (see include/gdn.h).
     Output tensors are still the caller's; pass ``o``/``final_state`` to avoid any
     allocation on the Python side as well.  Returns (o, final_state)."""
     lib = _lib.load()

@@ -23,7 +23,7 @@ EXPORTS = ("gdn_status_string", "gdn_version", "gdn_conv1d_fwd", "gdn_conv1d_upd
            "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill",
            "gdn_chunk_prefill_noalloc", "gdn_recurrent_decode")
 
-NOALLOC_SCRATCH_BYTES = 64 << 20
+NOALLOC_SCRATCH_BYTES = 128 << 20
 
 
 class GdnTensor(ctypes.Structure):

@@ -41,7 +41,7 @@
 
 namespace gdn {
 
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 128;
 constexpr int kStateThreads = 256;
 constexpr int kC = 64;          // chunk
 constexpr int kD = 128;         // dk = dv
@@ -168,7 +168,7 @@ __device__ __forceinline__ void blk_store(float (*D)[kLd], int dr, int dc, int t
 
 __device__ void tinv64(const float (*A)[kLd], float (*T)[kLd], float (*Y)[kLd]) {
     const int tid = threadIdx.x;
-    const int blk = tid >> 6, t = tid & 63, tr = t >> 3, tc = t & 7;
+    const int half = tid >> 6, t = tid & 63, tr = t >> 3, tc = t & 7;
     if (tid < 64) {
         // diagonal blocks by forward substitution, one column per thread
         const int b = tid >> 4, j = tid & 15, o = 16 * b;
@@ -186,42 +186,43 @@ __device__ void tinv64(const float (*A)[kLd], float (*T)[kLd], float (*Y)[kLd]) 
         for (int r = 0; r < 16; ++r) T[o + r][o + j] = x[r];
     }
     __syncthreads();
-    if (blk < 2) {   // X = A10 T00 (block 0) and A32 T22 (block 1), into Y rows 32.. / 48..
+    {   // X = A10 T00 (half 0) and A32 T22 (half 1), into Y rows 32.. and 48..
         float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-        const int o = 32 * blk;
+        const int o = 32 * half;
         blk_mma(acc, A, o + 16, o, T, o, o, tr, tc);
-        blk_store(Y, 32 + 16 * blk, 0, tr, tc, acc, 1.f);
+        blk_store(Y, 32 + 16 * half, 0, tr, tc, acc, 1.f);
     }
     __syncthreads();
-    if (blk < 2) {   // T10 = -T11 X,  T32 = -T33 X
+    {   // T10 = -T11 X,  T32 = -T33 X
         float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-        const int o = 32 * blk;
-        blk_mma(acc, T, o + 16, o + 16, Y, 32 + 16 * blk, 0, tr, tc);
+        const int o = 32 * half;
+        blk_mma(acc, T, o + 16, o + 16, Y, 32 + 16 * half, 0, tr, tc);
         blk_store(T, o + 16, o, tr, tc, acc, -1.f);
     }
     __syncthreads();
-    {   // Z = [A20 A21; A30 A31] T0 into Y[0:32][0:32]; block b makes Z(b>>1, b&1)
-        const int zr = blk >> 1, zc = blk & 1, ar = 32 + 16 * zr;
-        float z[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-        if (zc == 0) {
-            blk_mma(z, A, ar, 0, T, 0, 0, tr, tc);     // A_r0 T00
-            blk_mma(z, A, ar, 16, T, 16, 0, tr, tc);   // + A_r1 T10
-        } else {
-            blk_mma(z, A, ar, 16, T, 16, 16, tr, tc);  // A_r1 T11
-        }
-        blk_store(Y, 16 * zr, 16 * zc, tr, tc, z, 1.f);
+    {   // Z = [A20 A21; A30 A31] T0 into Y[0:32][0:32]; half h makes block row h
+        const int ar = 32 + 16 * half;
+        float z0[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, z1[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        blk_mma(z0, A, ar, 0, T, 0, 0, tr, tc);     // A_r0 T00
+        blk_mma(z0, A, ar, 16, T, 16, 0, tr, tc);   // + A_r1 T10
+        blk_mma(z1, A, ar, 16, T, 16, 16, tr, tc);  // A_r1 T11
+        blk_store(Y, 16 * half, 0, tr, tc, z0, 1.f);
+        blk_store(Y, 16 * half, 16, tr, tc, z1, 1.f);
     }
     __syncthreads();
-    {   // [T20 T21; T30 T31] = -T1 Z; block b makes T(2 + (b>>1), b&1)
-        const int wr = blk >> 1, wc = blk & 1;
-        float w[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-        if (wr == 0) {
-            blk_mma(w, T, 32, 32, Y, 0, 16 * wc, tr, tc);    // T22 Z2c
+    {   // [T20 T21; T30 T31] = -T1 Z; half h makes block row 2 + h
+        float w0[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, w1[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+        if (half == 0) {
+            blk_mma(w0, T, 32, 32, Y, 0, 0, tr, tc);    // T22 Z20
+            blk_mma(w1, T, 32, 32, Y, 0, 16, tr, tc);   // T22 Z21
         } else {
-            blk_mma(w, T, 48, 32, Y, 0, 16 * wc, tr, tc);    // T32 Z2c
-            blk_mma(w, T, 48, 48, Y, 16, 16 * wc, tr, tc);   // + T33 Z3c
+            blk_mma(w0, T, 48, 32, Y, 0, 0, tr, tc);    // T32 Z20
+            blk_mma(w0, T, 48, 48, Y, 16, 0, tr, tc);   // + T33 Z30
+            blk_mma(w1, T, 48, 32, Y, 0, 16, tr, tc);   // T32 Z21
+            blk_mma(w1, T, 48, 48, Y, 16, 16, tr, tc);  // + T33 Z31
         }
-        blk_store(T, 32 + 16 * wr, 16 * wc, tr, tc, w, -1.f);
+        blk_store(T, 32 + 16 * half, 0, tr, tc, w0, -1.f);
+        blk_store(T, 32 + 16 * half, 16, tr, tc, w1, -1.f);
     }
     __syncthreads();
 }
@@ -247,15 +248,12 @@ struct PrepSmem {
     uint32_t tmem;
 };
 
-__global__ void __launch_bounds__(kPrepThreads, 2)
+__global__ void __launch_bounds__(kPrepThreads, 3)
 chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     PrepSmem &S = *reinterpret_cast<PrepSmem *>(
         (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3, half = warp >> 2;
-    const int row = quad * 32 + lane;    // TMEM lane / tile row
-    const int ch = half * 32;            // this thread's 32 columns
     const int slot = blockIdx.x, hv = blockIdx.y;
     const int hk = hv / (p.Hv / p.Hk);
 
@@ -294,7 +292,7 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = S.tmem;
-    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const uint32_t colP = 0, colM = 64;
     bool ok = true;
 
@@ -326,14 +324,14 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
         }
         tc::mma_commit(&S.bar_mma);
     }
-    const int r = row & 63;
-    if (ok && half == 0) {
-        // L2-norm factors of this chunk's k rows (rows 0..63) and q rows (64..127)
-        const float ss = row_sumsq(S.kq, row, 16384);
+    const int r = tid & 63;
+    if (ok) {
+        // L2-norm factors of this chunk's k rows (threads 0..63) and q rows (64..127)
+        const float ss = row_sumsq(S.kq, tid, 16384);
         const float f = p.l2norm ? rsqrtf(ss + 1e-6f) : 1.f;
-        if (row < 64) {
+        if (tid < 64) {
             S.nk[r] = r < L ? f : 0.f;
-            S.gam[r] = row >= 32 ? gs + S.carry : gs;
+            S.gam[r] = tid >= 32 ? gs + S.carry : gs;
             S.bet[r] = bx;
         } else {
             S.nq[r] = r < L ? f : 0.f;
@@ -341,57 +339,51 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     }
     // (this wait also orders the norm reads of kq before its reuse as Y)
     if (ok) ok = wait_all(&S.bar_mma, 0);
-    float P[32];
+    float P[64];
     if (ok) {
         tc::fence_after_sync();
-        tmem_row32(tmem + lane_off + colP + ch, P);  // row: k_r.k_s (rows<64) or q_r.k_s
+        tmem_row64(tmem + lane_off + colP, P);  // row tid: k_r.k_s (tid<64) or q_r.k_s
     }
     uint8_t *wtile = p.ws + ((size_t)slot * p.Hv + hv) * kWsTile;
-    float Mrow[32];
+    float Mrow[64];
     if (ok) {
         const float gr = S.gam[r];
-        if (row < 64) {
+        if (tid < 64) {
             const float br = S.bet[r] * S.nk[r];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int s_ = ch + j;
-                S.A[r][s_] = (s_ < r && r < L) ? br * __expf(gr - S.gam[s_]) * S.nk[s_] * P[j] : 0.f;
-            }
+            for (int s = 0; s < 64; ++s)
+                S.A[r][s] = (s < r && r < L) ? br * __expf(gr - S.gam[s]) * S.nk[s] * P[s] : 0.f;
         } else {
             const float nr = S.nq[r];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int s_ = ch + j;
-                Mrow[j] = (s_ <= r && r < L) ? nr * __expf(gr - S.gam[s_]) * S.nk[s_] * P[j] : 0.f;
-            }
+            for (int s = 0; s < 64; ++s)
+                Mrow[s] = (s <= r && r < L) ? nr * __expf(gr - S.gam[s]) * S.nk[s] * P[s] : 0.f;
         }
         // per-token scalars for the state kernel
         float *ws_s = reinterpret_cast<float *>(wtile + kXTile);
-        if (half == 0) {
-            if (row < 64) {
-                ws_s[r] = S.gam[r];
-                ws_s[64 + r] = S.bet[r];
-                ws_s[128 + r] = S.nk[r];
-            } else {
-                ws_s[192 + r] = S.nq[r];
-            }
+        if (tid < 64) {
+            ws_s[r] = S.gam[r];
+            ws_s[64 + r] = S.bet[r];
+            ws_s[128 + r] = S.nk[r];
+        } else {
+            ws_s[192 + r] = S.nq[r];
         }
     }
     __syncthreads();
     if (ok) tinv64(S.A, S.T, S.Y);   // ends with a barrier: A is dead from here
     if (ok) {
-        if (row < 64) {
-            float lrow[32];
+        if (tid < 64) {
+            float lrow[64];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) lrow[j] = (ch + j < r) ? S.T[r][ch + j] : 0.f;
-            pack_row<32>(S.x, row, half * 4, lrow);
+            for (int t = 0; t < 64; ++t) lrow[t] = (t < r) ? S.T[r][t] : 0.f;
+            pack_row<64>(S.x, tid, 0, lrow);
             // Lo rows go to the workspace as they are
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-                *reinterpret_cast<uint4 *>(wtile + tc::swz(row, half * 4 + cc)) =
-                    *reinterpret_cast<const uint4 *>(S.x + tc::swz(row, half * 4 + cc));
+            for (int cc = 0; cc < 8; ++cc)
+                *reinterpret_cast<uint4 *>(wtile + tc::swz(tid, cc)) =
+                    *reinterpret_cast<const uint4 *>(S.x + tc::swz(tid, cc));
         } else {
-            pack_row<32>(S.x, row, half * 4, Mrow);
+            pack_row<64>(S.x, tid, 0, Mrow);
         }
     }
     tc::fence_async_smem();
@@ -411,17 +403,17 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     if (ok) ok = wait_all(&S.bar_mma, 1);
     if (ok) {
         tc::fence_after_sync();
-        if (row >= 64) {
-            float mt[32];
-            tmem_row32(tmem + lane_off + colM + ch, mt);
+        if (tid >= 64) {
+            float mt[64];
+            tmem_row64(tmem + lane_off + colM, mt);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) mt[j] += Mrow[j];   // Mt = M + M Lo
+            for (int s = 0; s < 64; ++s) mt[s] += Mrow[s];   // Mt = M + M Lo
             float f[8];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int cc = 0; cc < 8; ++cc) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) f[e] = mt[8 * cc + e];
-                *reinterpret_cast<uint4 *>(wtile + tc::swz(row, half * 4 + cc)) = pack8(f);
+                *reinterpret_cast<uint4 *>(wtile + tc::swz(tid, cc)) = pack8(f);
             }
         }
     }

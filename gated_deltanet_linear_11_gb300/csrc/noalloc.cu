@@ -8,7 +8,7 @@
 // callers for a workspace; this entry point instead uses a fixed scratch array that lives
 // in this library's device image, so the caller passes only inputs and outputs.
 //
-// The array is GDN_NOALLOC_SCRATCH_BYTES (64 MiB).  Every GPU that loads the library
+// The array is GDN_NOALLOC_SCRATCH_BYTES (128 MiB).  Every GPU that loads the library
 // holds it until the process exits.  Host code cannot use the array's name as a device
 // address: the first call on each device looks the address up with cudaGetSymbolAddress
 // (with that device current) and caches it.

@@ -170,7 +170,7 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t *q, const gdn_tensor_t *k,
  * caller.  Each call writes every scratch byte it later reads, so stale contents from an
  * earlier call do not matter.
  */
-#define GDN_NOALLOC_SCRATCH_BYTES (64u << 20)
+#define GDN_NOALLOC_SCRATCH_BYTES (128u << 20)
 
 gdn_status_t gdn_chunk_prefill_noalloc(const gdn_tensor_t *q, const gdn_tensor_t *k,
                                        const gdn_tensor_t *v, const float *g,
