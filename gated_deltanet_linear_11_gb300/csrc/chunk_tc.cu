@@ -38,6 +38,7 @@
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
+#include "tmap.cuh"
 
 namespace gdn {
 
@@ -723,20 +724,7 @@ namespace gdn_host {
 
 namespace {
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() { return tensor_map_encoder(); }
 
 // [T, H, 128] bf16 token-major view -> 3-D map (d, head, token), box (64, 1, 64), 128B swizzle.
 bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int H, int64_t tok_stride) {

@@ -10,7 +10,8 @@ a file that pytest collects last and passes both alone and after the other tests
 import pytest
 import torch
 
-from gated_deltanet_linear_11_gb300 import _lib, inputs
+from gated_deltanet_linear_11_gb300 import _lib as gdn_lib
+from gated_deltanet_linear_11_gb300 import inputs
 from gpu_util import assert_out_close, assert_state_close, np64
 
 pytestmark = pytest.mark.gpu
@@ -59,7 +60,7 @@ def test_noalloc_rejects_requests_beyond_its_scratch():
     x = inputs.scan_inputs(73, [T], Hk, Hv, 128, 128)
     xg = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     need = gdn.gdn_chunk_prefill_workspace_size(1, T, Hk, Hv, 128, 128)
-    assert need > _lib.NOALLOC_SCRATCH_BYTES
+    assert need > gdn_lib.NOALLOC_SCRATCH_BYTES
     with pytest.raises(gdn.GdnError) as e:
         gdn.gdn_chunk_prefill_noalloc(xg["q"], xg["k"], xg["v"], xg["g"], xg["beta"],
                                       xg["cu_seqlens"], cu_seqlens_host=x["cu_seqlens"])
