@@ -29,12 +29,15 @@
 //    The last product takes diag(.)Vn as a bf16 hi + lo pair (two MMAs) so the state
 //    keeps fp32-level accuracy; q/k L2 norms and decays are per-token fp32 scalars applied
 //    outside the MMAs, so the raw bf16 inputs are the only operands that are not split.
-//    Eight warps: warps w and w+4 share TMEM lanes 32(w%4).. and take 32 columns each.
+//    Eight compute warps: warps w and w+4 share TMEM lanes 32(w%4).. and take 32
+//    columns each; a ninth warp issues all TMA loads and MMAs.
 //
 // Every wait on an mbarrier is bounded in time; on expiry the CTA records GDN_ERR_TIMEOUT
 // in the status word, stops issuing work, frees its TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <atomic>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -43,7 +46,6 @@
 namespace gdn {
 
 constexpr int kPrepThreads = 128;
-constexpr int kStateThreads = 256;
 constexpr int kC = 64;          // chunk
 constexpr int kD = 128;         // dk = dv
 constexpr int kDVT = 64;        // dv columns per state CTA
@@ -53,7 +55,7 @@ constexpr uint32_t kWsTile = kXTile + kScal;  // one workspace tile per (slot, v
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s bound on any single wait
 
 struct TcMaps {
-    CUtensorMap q, k, v;
+    CUtensorMap q, k, v, o;
 };
 
 struct TcParams {
@@ -436,7 +438,8 @@ struct StateSmem {
     uint8_t rb[8192];        // bf16 R  [64 tokens][64 dv]    (MN-major B)
     uint8_t dvh[8192];       // bf16 hi of diag(dcy) Vn
     uint8_t dvl[8192];       // bf16 lo
-    uint64_t bar_tma[2], bar_d1, bar_d2, bar_d3;
+    uint8_t ob[2][8192];     // bf16 O tile [64 tokens][64 dv] per stage, stored by TMA
+    uint64_t bar_tma[2], bar_d1, bar_d2, bar_d3, bar_fin;
     uint32_t tmem;
     int abort;               // set by the first thread whose wait runs out
 };
@@ -457,6 +460,14 @@ __device__ __forceinline__ bool wait_one(uint64_t *bar, uint32_t parity, volatil
     }
 }
 
+// Bounded wait that ignores the abort flag: used on the way out, for work already issued.
+__device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = now_ns();
+    while (!tc::mbar_try_wait(bar, parity))
+        if (now_ns() - t0 > kWaitNs) return false;
+    return true;
+}
+
 __device__ __forceinline__ void issue_chunk_loads(StateSmem &S, const TcMaps &maps,
                                                   const TcParams &p, int stage, int t0,
                                                   int hk, int hv, int j0, int slot) {
@@ -474,22 +485,33 @@ __device__ __forceinline__ void issue_chunk_loads(StateSmem &S, const TcMaps &ma
                     "r"(tc::smem_u32(bar)) : "memory");
 }
 
-// Named barrier over the four warps that own TMEM lanes 0..63 (warps 0, 1, 4, 5): the rows
-// that feed the state chain.  The other four warps only produce outputs.
+// Named barrier between the four warps that own TMEM lanes 0..63 (warps 0, 1, 4, 5: the
+// rows that feed the state chain) and the issuer warp.  The other four compute warps only
+// produce outputs and never wait on it.
+constexpr int kComputeThreads = 256;        // warps 0..7: two per TMEM lane quarter
+constexpr int kIssuerWarp = kComputeThreads / 32;
+constexpr int kStateThreads = kComputeThreads + 32;
+
 __device__ __forceinline__ void chain_barrier() {
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("bar.sync 1, %0;" :: "n"(128 + 32) : "memory");
 }
 
+// Named barrier over the four output warps (2, 3, 6, 7); thread kOutLeader issues the
+// tensor stores of the O tile.
+constexpr int kOutLeader = 64;
+__device__ __forceinline__ void out_barrier() {
+    asm volatile("bar.sync 2, 128;" ::: "memory");
+}
+
+// One CTA per (sequence, v-head, 64-wide dv tile).  Warp 8 issues every TMA load and
+// every MMA, so no compute warp ever stalls behind an issue queue; warps 0..7 hold the
+// fp32 state rows and do the elementwise work of each chunk.
 __global__ void __launch_bounds__(kStateThreads, 1)
 chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     StateSmem &S = *reinterpret_cast<StateSmem *>(
         (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3;           // TMEM lane quarter
-    const int half = warp >> 2;          // which 32 of the 64 dv columns
-    const int row = quad * 32 + lane;    // TMEM lane = tile row
-    const bool chain = quad < 2;         // rows 0..63: tokens of the chain / dk rows 0..63
     const int jt = blockIdx.x, hv = blockIdx.y, n = blockIdx.z;
     const int hk = hv / (p.Hv / p.Hk);
     const int j0 = jt * kDVT;
@@ -508,30 +530,117 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         tc::mbar_init(&S.bar_d1, 1);
         tc::mbar_init(&S.bar_d2, 1);
         tc::mbar_init(&S.bar_d3, 1);
+        tc::mbar_init(&S.bar_fin, 1);
         S.abort = 0;
         tc::mbar_fence_init();
         tc::prefetch_tmap(&maps.k);
         tc::prefetch_tmap(&maps.q);
         tc::prefetch_tmap(&maps.v);
+        tc::prefetch_tmap(&maps.o);
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = S.tmem;
-    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t ch = half * 32;       // this thread's column offset
     const uint32_t colS = 0, colD1 = 64, colD2 = 128;
     volatile int *abort = &S.abort;
 
-    // Shared-memory descriptors, built once; a byte offset o is added as o >> 4.
-    // Stage b of a double buffer sits b * (buffer bytes) after stage 0.
-    const uint64_t dKQ0 = tc::sdesc(tc::smem_u32(S.kq[0]), 16, 1024);      // [K;Q], K-major
-    const uint64_t dKQt0 = tc::sdesc(tc::smem_u32(S.kq[0]), 16384, 1024);  // K^T, MN-major
-    const uint64_t dX0 = tc::sdesc(tc::smem_u32(S.x[0]), 16, 1024);        // [Lo;Mt], K-major
-    const uint64_t dH = tc::sdesc(tc::smem_u32(S.hb), 8192, 1024);
-    const uint64_t dR = tc::sdesc(tc::smem_u32(S.rb), 8192, 1024);
-    const uint64_t dVh = tc::sdesc(tc::smem_u32(S.dvh), 8192, 1024);
-    const uint64_t dVl = tc::sdesc(tc::smem_u32(S.dvl), 8192, 1024);
+    if (warp == kIssuerWarp) {
+        // ------------------------------------------------------------ issuer warp
+        // Shared-memory descriptors, built once; a byte offset o is added as o >> 4.
+        // Stage b of a double buffer sits b * (buffer bytes) after stage 0.
+        const uint64_t dKQ0 = tc::sdesc(tc::smem_u32(S.kq[0]), 16, 1024);      // [K;Q], K-major
+        const uint64_t dKQt0 = tc::sdesc(tc::smem_u32(S.kq[0]), 16384, 1024);  // K^T, MN-major
+        const uint64_t dX0 = tc::sdesc(tc::smem_u32(S.x[0]), 16, 1024);        // [Lo;Mt], K-major
+        const uint64_t dH = tc::sdesc(tc::smem_u32(S.hb), 8192, 1024);
+        const uint64_t dR = tc::sdesc(tc::smem_u32(S.rb), 8192, 1024);
+        const uint64_t dVh = tc::sdesc(tc::smem_u32(S.dvh), 8192, 1024);
+        const uint64_t dVl = tc::sdesc(tc::smem_u32(S.dvl), 8192, 1024);
+        constexpr uint32_t id1 = tc::idesc_bf16(128, 64, 0, 1);
+        constexpr uint32_t id3 = tc::idesc_bf16(128, 64, 1, 1);
+        const bool leader = lane == 0;
+        bool ok = true;
+        int issued = 0;                                        // chunks 0..issued-1 are loaded
+        if (leader && nch > 0) {
+            issue_chunk_loads(S, maps, p, 0, start, hk, hv, j0, s0);
+            issued = 1;
+        }
+        for (int c = 0; c < nch; ++c) {
+            const int st = c & 1;
+            const int t0 = start + c * kC;
+            __syncthreads();                                   // h published as bf16
+            if (leader) {
+                if (ok) ok = wait_one(&S.bar_tma[st], (c >> 1) & 1, abort);
+                if (ok && !*abort) {
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_bf16(tmem + colD1,
+                                     dKQ0 + ((st * 32768 + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                                     dH + ((ks * 2048) >> 4), id1, ks > 0);
+                    tc::mma_commit(&S.bar_d1);
+                }
+                // the next chunk's loads go out behind D1: stage st^1 was last read by the
+                // previous chunk, which every warp finished before the barrier above
+                if (ok && !*abort && c + 1 < nch) {
+                    issue_chunk_loads(S, maps, p, st ^ 1, t0 + kC, hk, hv, j0, s0 + c + 1);
+                    issued = c + 2;
+                }
+            }
+            __syncwarp();
+            chain_barrier();                                   // R ready
+            if (leader && ok && !*abort) {
+                tc::fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tmem + colD2, dX0 + ((st * kXStage + ks * 32) >> 4),
+                                 dR + ((ks * 2048) >> 4), id1, ks > 0);
+                tc::mma_commit(&S.bar_d2);
+            }
+            __syncwarp();
+            chain_barrier();                                   // hi of d Vn ready
+            if (leader && ok && !*abort) {
+                tc::fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tmem + colS, dKQt0 + ((st * 32768 + ks * 2048) >> 4),
+                                 dVh + ((ks * 2048) >> 4), id3, ks > 0);
+            }
+            __syncwarp();
+            chain_barrier();                                   // lo of d Vn ready
+            if (leader && ok && !*abort) {
+                tc::fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tmem + colS, dKQt0 + ((st * 32768 + ks * 2048) >> 4),
+                                 dVl + ((ks * 2048) >> 4), id3, 1);
+                tc::mma_commit(&S.bar_d3);
+            }
+            __syncwarp();
+        }
+        if (leader) {
+            // Nothing this warp started may still run when the CTA exits: wait (bounded) for
+            // the last load into each stage and for every MMA it issued.
+            for (int s = 0; s < 2; ++s) {
+                const int last = issued - 1 - ((issued - 1 - s) & 1);   // last chunk into stage s
+                if (last >= 0) wait_bounded(&S.bar_tma[s], (last >> 1) & 1);
+            }
+            tc::mma_commit(&S.bar_fin);
+            wait_bounded(&S.bar_fin, 0);
+        }
+        __syncwarp();
+        tc::fence_before_sync();
+        __syncthreads();
+        return;
+    }
+
+    // ---------------------------------------------------------------- compute warps
+    const int quad = warp & 3;           // TMEM lane quarter
+    const int half = warp >> 2;          // which 32 of the 64 dv columns
+    const int row = quad * 32 + lane;    // TMEM lane = tile row
+    const bool chain = quad < 2;         // rows 0..63: tokens of the chain / dk rows 0..63
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t ch = half * 32;       // this thread's column offset
 
     // fp32 master state in registers: dk row `row`, dv columns j0+ch .. +31.
     float h[32];
@@ -546,7 +655,6 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
 #pragma unroll
         for (int i = 0; i < 32; ++i) h[i] = 0.f;
     }
-    if (tid == kStateThreads - 32 && nch > 0) issue_chunk_loads(S, maps, p, 0, start, hk, hv, j0, s0);
 
     bool ok = true;
     const int r = row & 63;
@@ -572,19 +680,7 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
-        // the next chunk's loads go out from an output warp, off the MMA issuer's path
-        if (tid == kStateThreads - 32 && ok && c + 1 < nch)
-            issue_chunk_loads(S, maps, p, st ^ 1, t0 + kC, hk, hv, j0, s0 + c + 1);
         if (ok) ok = wait_one(&S.bar_tma[st], (c >> 1) & 1, abort);
-        if (tid == 0 && ok) {
-            tc::fence_after_sync();
-            constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                tc::mma_bf16(tmem + colD1, dKQ0 + ((st * 32768 + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                             dH + ((ks * 2048) >> 4), id, ks > 0);
-            tc::mma_commit(&S.bar_d1);
-        }
         const float *sc = reinterpret_cast<const float *>(S.x[st] + kXTile);
         const float *gam = sc, *bet = sc + 64, *nk = sc + 128, *nq = sc + 192;
         const float gL = gam[L - 1];
@@ -618,15 +714,6 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
                 tc::fence_async_smem();
                 tc::fence_before_sync();
                 chain_barrier();
-                if (tid == 0 && ok && !*abort) {
-                    tc::fence_after_sync();
-                    constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        tc::mma_bf16(tmem + colD2, dX0 + ((st * kXStage + ks * 32) >> 4),
-                                     dR + ((ks * 2048) >> 4), id, ks > 0);
-                    tc::mma_commit(&S.bar_d2);
-                }
             } else {
                 const float cq = __expf(gr) * nq[r];
 #pragma unroll
@@ -647,40 +734,54 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
             }
             if (chain) {
                 const float dc = r < L ? __expf(gL - gr) * nk[r] : 0.f;
-                float x[32], hi[32];
+                // hi = bf16(x) two at a time (the paired conversion issues at several times
+                // the rate of the single one); lo = x - hi is exact in fp32
+                uint32_t hp[16];
+                float lo[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    x[j] = dc * (keep[j] + d2[j]);
-                    hi[j] = __bfloat162float(__float2bfloat16_rn(x[j]));
+                for (int jj = 0; jj < 16; ++jj) {
+                    const float x0 = dc * (keep[2 * jj] + d2[2 * jj]);
+                    const float x1 = dc * (keep[2 * jj + 1] + d2[2 * jj + 1]);
+                    const __nv_bfloat162 hb2 = __floats2bfloat162_rn(x0, x1);
+                    hp[jj] = *reinterpret_cast<const uint32_t *>(&hb2);
+                    lo[2 * jj] = x0 - __uint_as_float(hp[jj] << 16);
+                    lo[2 * jj + 1] = x1 - __uint_as_float(hp[jj] & 0xffff0000u);
                 }
-                // hi part first: its MMAs run while the lo part is formed
-                pack_row<32>(S.dvh, r, half * 4, hi);
+                // hi part first: its MMAs run while the lo part is packed
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    *reinterpret_cast<uint4 *>(S.dvh + tc::swz(r, half * 4 + cc)) =
+                        make_uint4(hp[4 * cc], hp[4 * cc + 1], hp[4 * cc + 2], hp[4 * cc + 3]);
                 tc::fence_async_smem();
                 tc::fence_before_sync();
                 chain_barrier();
-                constexpr uint32_t id3 = tc::idesc_bf16(128, 64, 1, 1);
-                if (tid == 0 && ok && !*abort) {
-                    tc::fence_after_sync();
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        tc::mma_bf16(tmem + colS, dKQt0 + ((st * 32768 + ks * 2048) >> 4),
-                                     dVh + ((ks * 2048) >> 4), id3, ks > 0);
-                }
-#pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] -= hi[j];
-                pack_row<32>(S.dvl, r, half * 4, x);
+                pack_row<32>(S.dvl, r, half * 4, lo);
                 tc::fence_async_smem();
                 tc::fence_before_sync();
                 chain_barrier();
-                if (tid == 0 && ok && !*abort) {
-                    tc::fence_after_sync();
+            } else if (L == kC) {
+                // A full chunk's O tile goes out through shared memory with one tensor store,
+                // keeping 64 scattered row writes per warp off the load/store pipeline that
+                // the chain warps' shared-memory traffic shares.  Stage st was last stored
+                // two chunks ago; allowing one group in flight covers the previous chunk.
+                uint8_t *ob = S.ob[st];
+                if (tid == kOutLeader) tc::bulk_wait_read<1>();
+                out_barrier();
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        tc::mma_bf16(tmem + colS, dKQt0 + ((st * 32768 + ks * 2048) >> 4),
-                                     dVl + ((ks * 2048) >> 4), id3, 1);
-                    tc::mma_commit(&S.bar_d3);
+                for (int cc = 0; cc < 4; ++cc) {
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = p.scale * (keep[8 * cc + e] + d2[8 * cc + e]);
+                    *reinterpret_cast<uint4 *>(ob + tc::swz(r, half * 4 + cc)) = pack8(f);
+                }
+                tc::fence_async_smem();
+                out_barrier();
+                if (tid == kOutLeader && ok && !*abort) {
+                    tc::tma_store_3d(&maps.o, ob, j0, hv, t0);
+                    tc::bulk_commit();
                 }
             } else if (r < L && ok) {
+                // the last, partial chunk of a sequence: rows past L belong to the next one
                 uint4 *dst = reinterpret_cast<uint4 *>(p.o + (size_t)(t0 + r) * p.o_tok +
                                                        (size_t)hv * kD + j0 + ch);
 #pragma unroll
@@ -691,6 +792,7 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
                     dst[cc] = pack8(f);
                 }
             }
+            tc::fence_before_sync();
         }
         aL_prev = __expf(gL);
     }
@@ -704,6 +806,7 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
             for (int i = 0; i < 32; ++i) h[i] = fmaf(aL_prev, h[i], ds[i]);
         }
     }
+    if (tid == kOutLeader) tc::bulk_wait_all();   // O tiles written before the CTA exits
     tc::fence_before_sync();
     __syncthreads();
     if (!*abort && p.hT) {
@@ -723,6 +826,8 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
 namespace gdn_host {
 
 namespace {
+
+constexpr int kMaxDevices = 64;
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() { return tensor_map_encoder(); }
 
@@ -758,7 +863,7 @@ gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStre
     if (a.out_f32) return GDN_ERR_DTYPE;
     gdn::TcMaps maps;
     if (!make_map(&maps.q, a.q, a.T, a.Hk, a.q_tok) || !make_map(&maps.k, a.k, a.T, a.Hk, a.k_tok) ||
-        !make_map(&maps.v, a.v, a.T, a.Hv, a.v_tok))
+        !make_map(&maps.v, a.v, a.T, a.Hv, a.v_tok) || !make_map(&maps.o, a.o, a.T, a.Hv, a.o_tok))
         return GDN_ERR_CUDA;
     gdn::TcParams p;
     p.g = a.g;
@@ -778,14 +883,17 @@ gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStre
 
     const size_t prep_smem = sizeof(gdn::PrepSmem) + 1024;
     const size_t state_smem = sizeof(gdn::StateSmem) + 1024;
-    static bool attr_set = false;
-    if (!attr_set) {
+    // the shared-memory opt-in is a per-device attribute: set it once on each device
+    static std::atomic<bool> attr_set[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(gdn::chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)prep_smem) != cudaSuccess ||
             cudaFuncSetAttribute(gdn::chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)state_smem) != cudaSuccess)
             return GDN_ERR_CUDA;
-        attr_set = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     const int slots = (int)((a.T + gdn::kC - 1) / gdn::kC) + a.N;
     if (slots > 0) {
