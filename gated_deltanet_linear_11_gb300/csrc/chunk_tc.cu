@@ -26,8 +26,8 @@
 //      Vn = R + Lo R                     (identity part of Tinv applied exactly in fp32)
 //      O  = scale (diag(e^gamma nq) Q h + Mt R)
 //      h <- e^{gamma_L} h + K^T diag(e^{gamma_L-gamma} nk) Vn
-//    The last product takes diag(.)Vn as a bf16 hi + lo pair (two MMAs) so the state
-//    keeps fp32-level accuracy; q/k L2 norms and decays are per-token fp32 scalars applied
+//    The last product takes diag(.)Vn as a bf16 hi + lo pair (one N = 128 MMA pass over
+//    [hi | lo], the halves summed in fp32) so the state keeps fp32-level accuracy; q/k L2 norms and decays are per-token fp32 scalars applied
 //    outside the MMAs, so the raw bf16 inputs are the only operands that are not split.
 //    Eight compute warps: warps w and w+4 share TMEM lanes 32(w%4).. and take 32
 //    columns each; a ninth warp issues all TMA loads and MMAs.
@@ -443,6 +443,8 @@ struct StateSmem {
     uint32_t tmem;
     int abort;               // set by the first thread whose wait runs out
 };
+static_assert(offsetof(StateSmem, dvl) == offsetof(StateSmem, dvh) + 8192,
+              "the [hi | lo] operand is one MN-major tile with a 8192-byte block stride");
 
 // Bounded wait by one thread.  Gives up (false) when the phase has not completed within
 // kWaitNs, or as soon as another thread of the CTA has given up; the caller then skips
@@ -483,6 +485,17 @@ __device__ __forceinline__ void issue_chunk_loads(StateSmem &S, const TcMaps &ma
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  :: "r"(tc::smem_u32(S.x[stage])), "l"(src), "r"(kWsTile),
                     "r"(tc::smem_u32(bar)) : "memory");
+}
+
+// h <- a h + (K^T hi + K^T lo) for this thread's 32 columns: the two halves of the state
+// update sit 64 TMEM columns apart.
+__device__ __forceinline__ void fold_update(float (&h)[32], float a, uint32_t taddr) {
+    float u[32], w[32];
+    tc::tmem_ld32(taddr, u);
+    tc::tmem_ld32(taddr + 64, w);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) h[i] = fmaf(a, h[i], u[i] + w[i]);
 }
 
 // Named barrier between the four warps that own TMEM lanes 0..63 (warps 0, 1, 4, 5: the
@@ -542,7 +555,8 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = S.tmem;
-    const uint32_t colS = 0, colD1 = 64, colD2 = 128;
+    // TMEM columns: D1 [K;Q]h, D2 [Lo;Mt]R, and the state update as a hi | lo pair
+    const uint32_t colD1 = 0, colD2 = 64, colS = 128;
     volatile int *abort = &S.abort;
 
     if (warp == kIssuerWarp) {
@@ -554,10 +568,10 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         const uint64_t dX0 = tc::sdesc(tc::smem_u32(S.x[0]), 16, 1024);        // [Lo;Mt], K-major
         const uint64_t dH = tc::sdesc(tc::smem_u32(S.hb), 8192, 1024);
         const uint64_t dR = tc::sdesc(tc::smem_u32(S.rb), 8192, 1024);
-        const uint64_t dVh = tc::sdesc(tc::smem_u32(S.dvh), 8192, 1024);
-        const uint64_t dVl = tc::sdesc(tc::smem_u32(S.dvl), 8192, 1024);
+        // [hi | lo] of d Vn as one N = 128 MN-major operand: lo is the second 64-wide block
+        const uint64_t dVhl = tc::sdesc(tc::smem_u32(S.dvh), 8192, 1024);
         constexpr uint32_t id1 = tc::idesc_bf16(128, 64, 0, 1);
-        constexpr uint32_t id3 = tc::idesc_bf16(128, 64, 1, 1);
+        constexpr uint32_t id3 = tc::idesc_bf16(128, 128, 1, 1);
         const bool leader = lane == 0;
         bool ok = true;
         int issued = 0;                                        // chunks 0..issued-1 are loaded
@@ -598,22 +612,14 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
                 tc::mma_commit(&S.bar_d2);
             }
             __syncwarp();
-            chain_barrier();                                   // hi of d Vn ready
+            chain_barrier();                                   // hi | lo of d Vn ready
             if (leader && ok && !*abort) {
+                // K^T [hi | lo]: both halves of the update in one pass, summed in fp32 later
                 tc::fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     tc::mma_bf16(tmem + colS, dKQt0 + ((st * 32768 + ks * 2048) >> 4),
-                                 dVh + ((ks * 2048) >> 4), id3, ks > 0);
-            }
-            __syncwarp();
-            chain_barrier();                                   // lo of d Vn ready
-            if (leader && ok && !*abort) {
-                tc::fence_after_sync();
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(tmem + colS, dKQt0 + ((st * 32768 + ks * 2048) >> 4),
-                                 dVl + ((ks * 2048) >> 4), id3, 1);
+                                 dVhl + ((ks * 2048) >> 4), id3, ks > 0);
                 tc::mma_commit(&S.bar_d3);
             }
             __syncwarp();
@@ -670,10 +676,7 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
             ok = wait_one(&S.bar_d3, ph ^ 1, abort);
             if (ok) {
                 tc::fence_after_sync();
-                float ds[32];
-                tmem_row32(tmem + lane_off + colS + ch, ds);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) h[i] = fmaf(aL_prev, h[i], ds[i]);
+                fold_update(h, aL_prev, tmem + lane_off + colS + ch);
             }
         }
         pack_row<32>(S.hb, row, half * 4, h);
@@ -747,14 +750,10 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
                     lo[2 * jj] = x0 - __uint_as_float(hp[jj] << 16);
                     lo[2 * jj + 1] = x1 - __uint_as_float(hp[jj] & 0xffff0000u);
                 }
-                // hi part first: its MMAs run while the lo part is packed
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
                     *reinterpret_cast<uint4 *>(S.dvh + tc::swz(r, half * 4 + cc)) =
                         make_uint4(hp[4 * cc], hp[4 * cc + 1], hp[4 * cc + 2], hp[4 * cc + 3]);
-                tc::fence_async_smem();
-                tc::fence_before_sync();
-                chain_barrier();
                 pack_row<32>(S.dvl, r, half * 4, lo);
                 tc::fence_async_smem();
                 tc::fence_before_sync();
@@ -800,10 +799,7 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         ok = wait_one(&S.bar_d3, (nch - 1) & 1, abort);
         if (ok) {
             tc::fence_after_sync();
-            float ds[32];
-            tmem_row32(tmem + lane_off + colS + ch, ds);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) h[i] = fmaf(aL_prev, h[i], ds[i]);
+            fold_update(h, aL_prev, tmem + lane_off + colS + ch);
         }
     }
     if (tid == kOutLeader) tc::bulk_wait_all();   // O tiles written before the CTA exits
