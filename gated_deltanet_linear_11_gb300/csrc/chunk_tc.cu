@@ -139,6 +139,15 @@ __device__ __forceinline__ float row_sumsq(const uint8_t *tile, int row, uint32_
     return acc;
 }
 
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x by the hardware approximation (relative error about 2^-22; 0 for x = -inf).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ------------------------------------------------------------------ Tinv (fp32)
 // T = (I + A)^{-1} for a 64x64 strictly lower A, row stride kLd (even, for float2 loads),
 // by 16x16 blocks.  With T_ii the inverses of the diagonal blocks (I + A_ii) and, for the
@@ -246,6 +255,7 @@ struct PrepSmem {
     };
     float T[64][kLd];
     float gam[64], bet[64], nk[64], nq[64];
+    float c2[64];            // gamma_s log2(e) - log2(nk_s): the key-side exponent
     float carry;
     uint64_t bar_tma, bar_mma;
     uint32_t tmem;
@@ -333,9 +343,14 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
         const float ss = row_sumsq(S.kq, tid, 16384);
         const float f = p.l2norm ? rsqrtf(ss + 1e-6f) : 1.f;
         if (tid < 64) {
-            S.nk[r] = r < L ? f : 0.f;
-            S.gam[r] = tid >= 32 ? gs + S.carry : gs;
+            const float nkr = r < L ? f : 0.f;
+            const float gamr = tid >= 32 ? gs + S.carry : gs;
+            S.nk[r] = nkr;
+            S.gam[r] = gamr;
             S.bet[r] = bx;
+            // e^{gamma_r - gamma_s} nk_s = 2^(gamma_r log2 e - c2_s); nk_s = 0 gives +inf here
+            // and an exact 0 below
+            S.c2[r] = nkr > 0.f ? gamr * kLog2e - __log2f(nkr) : __int_as_float(0x7f800000);
         } else {
             S.nq[r] = r < L ? f : 0.f;
         }
@@ -350,17 +365,28 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     uint8_t *wtile = p.ws + ((size_t)slot * p.Hv + hv) * kWsTile;
     float Mrow[64];
     if (ok) {
+        // A_rs = beta_r nk_r e^{gamma_r - gamma_s} nk_s P_rs (s < r), M_rs likewise with nq_r
+        // (s <= r).  Rows 0..31 have no entries past column 31: that half is written as
+        // zeros by the whole warp.
         const float gr = S.gam[r];
+        const float g2r = gr * kLog2e;
+        const bool low = (r & 63) < 32;             // warp-uniform
         if (tid < 64) {
             const float br = S.bet[r] * S.nk[r];
 #pragma unroll
-            for (int s = 0; s < 64; ++s)
-                S.A[r][s] = (s < r && r < L) ? br * __expf(gr - S.gam[s]) * S.nk[s] * P[s] : 0.f;
+            for (int s = 0; s < 64; s += 2) {
+                float2 a = make_float2(0.f, 0.f);
+                if (s < 32 || !low) {
+                    a.x = (s < r && r < L) ? br * P[s] * fast_exp2(g2r - S.c2[s]) : 0.f;
+                    a.y = (s + 1 < r && r < L) ? br * P[s + 1] * fast_exp2(g2r - S.c2[s + 1]) : 0.f;
+                }
+                *reinterpret_cast<float2 *>(&S.A[r][s]) = a;
+            }
         } else {
             const float nr = S.nq[r];
 #pragma unroll
             for (int s = 0; s < 64; ++s)
-                Mrow[s] = (s <= r && r < L) ? nr * __expf(gr - S.gam[s]) * S.nk[s] * P[s] : 0.f;
+                Mrow[s] = ((s < 32 || !low) && s <= r && r < L) ? nr * P[s] * fast_exp2(g2r - S.c2[s]) : 0.f;
         }
         // per-token scalars for the state kernel
         float *ws_s = reinterpret_cast<float *>(wtile + kXTile);
@@ -380,11 +406,6 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
 #pragma unroll
             for (int t = 0; t < 64; ++t) lrow[t] = (t < r) ? S.T[r][t] : 0.f;
             pack_row<64>(S.x, tid, 0, lrow);
-            // Lo rows go to the workspace as they are
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc)
-                *reinterpret_cast<uint4 *>(wtile + tc::swz(tid, cc)) =
-                    *reinterpret_cast<const uint4 *>(S.x + tc::swz(tid, cc));
         } else {
             pack_row<64>(S.x, tid, 0, Mrow);
         }
@@ -411,14 +432,17 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
             tmem_row64(tmem + lane_off + colM, mt);
 #pragma unroll
             for (int s = 0; s < 64; ++s) mt[s] += Mrow[s];   // Mt = M + M Lo
-            float f[8];
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = mt[8 * cc + e];
-                *reinterpret_cast<uint4 *>(wtile + tc::swz(tid, cc)) = pack8(f);
-            }
+            pack_row<64>(S.x, tid, 0, mt);                   // over M, which the MMA has read
         }
+    }
+    // The finished [Lo ; Mt] tile leaves in one bulk copy: 128 threads writing their own
+    // 128-byte rows would cost a load/store wavefront per row per instruction.
+    tc::fence_async_smem();
+    __syncthreads();
+    if (ok && tid == 0) {
+        tc::bulk_store(wtile, S.x, kXTile);
+        tc::bulk_commit();
+        tc::bulk_wait_all();
     }
     if (!ok && tid == 0) report(p.status, GDN_ERR_TIMEOUT);
     tc::fence_before_sync();
