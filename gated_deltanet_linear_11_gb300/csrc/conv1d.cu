@@ -15,7 +15,6 @@ namespace gdn {
 
 constexpr int kConvThreads = 128;   // threads per block, 8 channels each
 constexpr int kConvTile = 16;       // tokens per thread (anchored at the sequence start)
-constexpr int kConvGroup = 4;       // tokens loaded together; the next group is in flight
 
 struct Taps {
     float w[8][4];
@@ -56,7 +55,7 @@ __device__ __forceinline__ uint4 conv_out(const Taps &tp, const float x0[8], con
 }
 
 // grid: (ceil(C / (8*kConvThreads)), ceil(max_len / kConvTile) (>=1), N)
-__global__ void __launch_bounds__(kConvThreads, 4)
+__global__ void __launch_bounds__(kConvThreads, 5)
 conv1d_fwd_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
                   const bf16 *__restrict__ bias, const int32_t *__restrict__ cu,
                   const bf16 *s_in, bf16 *s_out, bf16 *__restrict__ y, int C) {
@@ -68,6 +67,8 @@ conv1d_fwd_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
     const int L = cu[n + 1] - start;
     const int t0 = tile * kConvTile;
     if (t0 >= L && tile > 0) return;
+
+    __shared__ uint4 conv_tile_buf[kConvTile][kConvThreads];   // 32 KiB
 
     Taps tp;
     load_taps(tp, w, bias, c0);
@@ -87,37 +88,52 @@ conv1d_fwd_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
         }
     }
 
-    // Tokens are processed in groups of kConvGroup; the loads of group g+1 are issued
-    // before group g is computed, so a thread always has a group of rows in flight.
     const int cnt = min(kConvTile, L - t0);
-    uint4 cur_g[kConvGroup], nxt_g[kConvGroup];
+    if (cnt == kConvTile) {
+        // Full tile: every row goes to shared memory by an asynchronous 16-byte copy at
+        // once (in two commit groups), so a CTA keeps its whole tile in flight without
+        // holding registers; each thread reads back only the slots it copied itself.
+        // Straight-line code keeps the sliding window in renamed registers.
+        const bf16 *xp = x + (size_t)(start + t0) * C + c0;
+        bf16 *yp = y + (size_t)(start + t0) * C + c0;
+        const uint32_t slot0 = (uint32_t)__cvta_generic_to_shared(&conv_tile_buf[0][threadIdx.x]);
 #pragma unroll
-    for (int i = 0; i < kConvGroup; ++i)
-        if (i < cnt) cur_g[i] = *reinterpret_cast<const uint4 *>(x + (size_t)(start + t0 + i) * C + c0);
-#pragma unroll 1
-    for (int base = 0; base < cnt; base += kConvGroup) {
-        const int nb = base + kConvGroup;
-#pragma unroll
-        for (int i = 0; i < kConvGroup; ++i)
-            if (nb + i < cnt)
-                nxt_g[i] = *reinterpret_cast<const uint4 *>(x + (size_t)(start + t0 + nb + i) * C + c0);
-#pragma unroll
-        for (int i = 0; i < kConvGroup; ++i) {
-            if (base + i < cnt) {
-                float cur[8];
-                unpack8(cur_g[i], cur);
-                const uint4 out = conv_out(tp, win[0], win[1], win[2], cur);
-                *reinterpret_cast<uint4 *>(y + (size_t)(start + t0 + base + i) * C + c0) = out;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    win[0][e] = win[1][e];
-                    win[1][e] = win[2][e];
-                    win[2][e] = cur[e];
-                }
-            }
+        for (int i = 0; i < kConvTile; ++i) {
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                         :: "r"(slot0 + (uint32_t)(i * kConvThreads * 16)), "l"(xp + (size_t)i * C)
+                         : "memory");
+            if (i == kConvTile / 2 - 1 || i == kConvTile - 1)
+                asm volatile("cp.async.commit_group;" ::: "memory");
         }
 #pragma unroll
-        for (int i = 0; i < kConvGroup; ++i) cur_g[i] = nxt_g[i];
+        for (int i = 0; i < kConvTile; ++i) {
+            if (i == 0) asm volatile("cp.async.wait_group 1;" ::: "memory");
+            if (i == kConvTile / 2) asm volatile("cp.async.wait_group 0;" ::: "memory");
+            float cur[8];
+            unpack8(conv_tile_buf[i][threadIdx.x], cur);
+            *reinterpret_cast<uint4 *>(yp + (size_t)i * C) = conv_out(tp, win[0], win[1], win[2], cur);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                win[0][e] = win[1][e];
+                win[1][e] = win[2][e];
+                win[2][e] = cur[e];
+            }
+        }
+    } else {
+        // Partial tile (the last of a sequence): a plain row loop.
+#pragma unroll 1
+        for (int i = 0; i < cnt; ++i) {
+            float cur[8];
+            unpack8(*reinterpret_cast<const uint4 *>(x + (size_t)(start + t0 + i) * C + c0), cur);
+            *reinterpret_cast<uint4 *>(y + (size_t)(start + t0 + i) * C + c0) =
+                conv_out(tp, win[0], win[1], win[2], cur);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                win[0][e] = win[1][e];
+                win[1][e] = win[2][e];
+                win[2][e] = cur[e];
+            }
+        }
     }
 
     // The first tile of a sequence is the only reader of the old conv state, so it also
