@@ -149,18 +149,22 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // ------------------------------------------------------------------ Tinv (fp32)
-// T = (I + A)^{-1} for a 64x64 strictly lower A, row stride kLd (even, for float2 loads),
-// by 16x16 blocks.  With T_ii the inverses of the diagonal blocks (I + A_ii) and, for the
-// two 32x32 halves, T0 = [[T00,0],[T10,T11]], T1 = [[T22,0],[T32,T33]]:
+// T = (I + A)^{-1} for a 64x64 strictly lower A, computed in place (T replaces A) by 16x16
+// blocks.  With T_ii the inverses of the diagonal blocks (I + A_ii) and, for the two
+// 32x32 halves, T0 = [[T00,0],[T10,T11]], T1 = [[T22,0],[T32,T33]]:
 //     T10 = -T11 A10 T00,   T32 = -T33 A32 T22,
 //     [T20 T21; T30 T31] = -T1 [A20 A21; A30 A31] T0.
-// Every product is a 16x16 block computed by 64 threads holding 2x2 register tiles.
-// All 128 threads call this; Y is a scratch of the same shape.
+// Each block of A is read for the last time before the block of T at the same place is
+// written, with a barrier in between.  Every product is a 16x16 block computed by 64
+// threads holding 2x2 register tiles.  All 128 threads call this; Y ([64][kLdY]) is a
+// scratch for the 16- and 32-column intermediates.
 constexpr int kLd = 66;
+constexpr int kLdY = 34;
 
 // acc += A[ar.., ac..] (16x16) * B[br.., bc..] (16x16) for this thread's 2x2 tile.
-__device__ __forceinline__ void blk_mma(float (&acc)[2][2], const float (*A)[kLd], int ar, int ac,
-                                        const float (*B)[kLd], int br, int bc, int tr, int tc) {
+template <int LA, int LB>
+__device__ __forceinline__ void blk_mma(float (&acc)[2][2], const float (*A)[LA], int ar, int ac,
+                                        const float (*B)[LB], int br, int bc, int tr, int tc) {
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
         const float a0 = A[ar + 2 * tr][ac + m], a1 = A[ar + 2 * tr + 1][ac + m];
@@ -172,69 +176,75 @@ __device__ __forceinline__ void blk_mma(float (&acc)[2][2], const float (*A)[kLd
     }
 }
 
-__device__ __forceinline__ void blk_store(float (*D)[kLd], int dr, int dc, int tr, int tc,
+template <int LD>
+__device__ __forceinline__ void blk_store(float (*D)[LD], int dr, int dc, int tr, int tc,
                                           const float (&acc)[2][2], float sgn) {
     *reinterpret_cast<float2 *>(&D[dr + 2 * tr][dc + 2 * tc]) = make_float2(sgn * acc[0][0], sgn * acc[0][1]);
     *reinterpret_cast<float2 *>(&D[dr + 2 * tr + 1][dc + 2 * tc]) = make_float2(sgn * acc[1][0], sgn * acc[1][1]);
 }
 
-__device__ void tinv64(const float (*A)[kLd], float (*T)[kLd], float (*Y)[kLd]) {
+__device__ void tinv64_inplace(float (*AT)[kLd], float (*Y)[kLdY]) {
     const int tid = threadIdx.x;
     const int half = tid >> 6, t = tid & 63, tr = t >> 3, tc = t & 7;
-    if (tid < 64) {
-        // diagonal blocks by forward substitution, one column per thread
-        const int b = tid >> 4, j = tid & 15, o = 16 * b;
+    {   // diagonal blocks by forward substitution, one column per thread
+        const int b = (tid >> 4) & 3, j = tid & 15, o = 16 * b;
         float x[16];
+        if (tid < 64) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
+            for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
 #pragma unroll
-        for (int r = 1; r < 16; ++r) {
-            float acc = x[r];
+            for (int r = 1; r < 16; ++r) {
+                float acc = x[r];
 #pragma unroll
-            for (int q = 0; q < r; ++q) acc = fmaf(-A[o + r][o + q], x[q], acc);
-            x[r] = acc;
+                for (int q = 0; q < r; ++q) acc = fmaf(-AT[o + r][o + q], x[q], acc);
+                x[r] = acc;
+            }
         }
+        __syncthreads();                       // every read of the A_ii is done
+        if (tid < 64) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) T[o + r][o + j] = x[r];
+            for (int r = 0; r < 16; ++r) AT[o + r][o + j] = x[r];
+        }
     }
     __syncthreads();
     {   // X = A10 T00 (half 0) and A32 T22 (half 1), into Y rows 32.. and 48..
         float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
         const int o = 32 * half;
-        blk_mma(acc, A, o + 16, o, T, o, o, tr, tc);
+        blk_mma(acc, AT, o + 16, o, AT, o, o, tr, tc);
         blk_store(Y, 32 + 16 * half, 0, tr, tc, acc, 1.f);
     }
     __syncthreads();
-    {   // T10 = -T11 X,  T32 = -T33 X
+    {   // T10 = -T11 X over A10,  T32 = -T33 X over A32
         float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
         const int o = 32 * half;
-        blk_mma(acc, T, o + 16, o + 16, Y, 32 + 16 * half, 0, tr, tc);
-        blk_store(T, o + 16, o, tr, tc, acc, -1.f);
+        blk_mma(acc, AT, o + 16, o + 16, Y, 32 + 16 * half, 0, tr, tc);
+        blk_store(AT, o + 16, o, tr, tc, acc, -1.f);
     }
     __syncthreads();
     {   // Z = [A20 A21; A30 A31] T0 into Y[0:32][0:32]; half h makes block row h
         const int ar = 32 + 16 * half;
         float z0[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, z1[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-        blk_mma(z0, A, ar, 0, T, 0, 0, tr, tc);     // A_r0 T00
-        blk_mma(z0, A, ar, 16, T, 16, 0, tr, tc);   // + A_r1 T10
-        blk_mma(z1, A, ar, 16, T, 16, 16, tr, tc);  // A_r1 T11
+        blk_mma(z0, AT, ar, 0, AT, 0, 0, tr, tc);     // A_r0 T00
+        blk_mma(z0, AT, ar, 16, AT, 16, 0, tr, tc);   // + A_r1 T10
+        blk_mma(z1, AT, ar, 16, AT, 16, 16, tr, tc);  // A_r1 T11
         blk_store(Y, 16 * half, 0, tr, tc, z0, 1.f);
         blk_store(Y, 16 * half, 16, tr, tc, z1, 1.f);
     }
     __syncthreads();
-    {   // [T20 T21; T30 T31] = -T1 Z; half h makes block row 2 + h
+    {   // [T20 T21; T30 T31] = -T1 Z over A2x, A3x; half h makes block row 2 + h
         float w0[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, w1[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
         if (half == 0) {
-            blk_mma(w0, T, 32, 32, Y, 0, 0, tr, tc);    // T22 Z20
-            blk_mma(w1, T, 32, 32, Y, 0, 16, tr, tc);   // T22 Z21
+            blk_mma(w0, AT, 32, 32, Y, 0, 0, tr, tc);    // T22 Z20
+            blk_mma(w1, AT, 32, 32, Y, 0, 16, tr, tc);   // T22 Z21
         } else {
-            blk_mma(w0, T, 48, 32, Y, 0, 0, tr, tc);    // T32 Z20
-            blk_mma(w0, T, 48, 48, Y, 16, 0, tr, tc);   // + T33 Z30
-            blk_mma(w1, T, 48, 32, Y, 0, 16, tr, tc);   // T32 Z21
-            blk_mma(w1, T, 48, 48, Y, 16, 16, tr, tc);  // + T33 Z31
+            blk_mma(w0, AT, 48, 32, Y, 0, 0, tr, tc);    // T32 Z20
+            blk_mma(w0, AT, 48, 48, Y, 16, 0, tr, tc);   // + T33 Z30
+            blk_mma(w1, AT, 48, 32, Y, 0, 16, tr, tc);   // T32 Z21
+            blk_mma(w1, AT, 48, 48, Y, 16, 16, tr, tc);  // + T33 Z31
         }
-        blk_store(T, 32 + 16 * half, 0, tr, tc, w0, -1.f);
-        blk_store(T, 32 + 16 * half, 16, tr, tc, w1, -1.f);
+        // the stores go to columns 0..31, which no thread reads in this step
+        blk_store(AT, 32 + 16 * half, 0, tr, tc, w0, -1.f);
+        blk_store(AT, 32 + 16 * half, 16, tr, tc, w1, -1.f);
     }
     __syncthreads();
 }
@@ -242,26 +252,28 @@ __device__ void tinv64(const float (*A)[kLd], float (*T)[kLd], float (*Y)[kLd]) 
 // ================================================================ chunk_prep kernel
 
 struct PrepSmem {
-    // [K;Q] K-major tile (2 K blocks of [128 rows][128 B]); once P = [K;Q]K^T and the norms
-    // are taken it is dead and holds the inverse's scratch Y.
+    // The [K;Q] K-major tile until P = [K;Q]K^T and the norms are taken; after that its
+    // first 16 KB hold the bf16 tile X = [Lo ; M] (then [Lo ; Mt]) and the rest the
+    // inverse's scratch Y.
     union {
         uint8_t kq[32768];
-        float Y[64][kLd];
+        struct {
+            uint8_t x[kXTile];
+            float Y[64][kLdY];
+        } post;
     };
-    // A (fp32) until the inverse is done, then the bf16 tile X = [Lo ; M].
-    union {
-        float A[64][kLd];
-        uint8_t x[kXTile];
-    };
-    float T[64][kLd];
+    float AT[64][kLd];       // A, then T = (I + A)^{-1} in place
     float gam[64], bet[64], nk[64], nq[64];
     float c2[64];            // gamma_s log2(e) - log2(nk_s): the key-side exponent
     float carry;
     uint64_t bar_tma, bar_mma;
     uint32_t tmem;
 };
+static_assert(sizeof(PrepSmem) + 1024 <= 53 * 1024, "four prep CTAs fit on one SM");
 
-__global__ void __launch_bounds__(kPrepThreads, 3)
+// One CTA per (chunk slot, v-head); four CTAs per SM.  TMEM (128 columns): P = [K;Q]K^T
+// in columns 0..63, whose M rows are then replaced by the fp32 M itself; M Lo in 64..127.
+__global__ void __launch_bounds__(kPrepThreads, 4)
 chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     PrepSmem &S = *reinterpret_cast<PrepSmem *>(
@@ -355,39 +367,45 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
             S.nq[r] = r < L ? f : 0.f;
         }
     }
-    // (this wait also orders the norm reads of kq before its reuse as Y)
+    // (this wait also orders the norm reads of kq before the region is reused)
     if (ok) ok = wait_all(&S.bar_mma, 0);
-    float P[64];
+    uint8_t *wtile = p.ws + ((size_t)slot * p.Hv + hv) * kWsTile;
+    // Rows 0..31 of A and M have no entries past column 31 (warp-uniform).
+    const bool low = r < 32;
     if (ok) {
         tc::fence_after_sync();
-        tmem_row64(tmem + lane_off + colP, P);  // row tid: k_r.k_s (tid<64) or q_r.k_s
-    }
-    uint8_t *wtile = p.ws + ((size_t)slot * p.Hv + hv) * kWsTile;
-    float Mrow[64];
-    if (ok) {
-        // A_rs = beta_r nk_r e^{gamma_r - gamma_s} nk_s P_rs (s < r), M_rs likewise with nq_r
-        // (s <= r).  Rows 0..31 have no entries past column 31: that half is written as
-        // zeros by the whole warp.
-        const float gr = S.gam[r];
-        const float g2r = gr * kLog2e;
-        const bool low = (r & 63) < 32;             // warp-uniform
-        if (tid < 64) {
-            const float br = S.bet[r] * S.nk[r];
+        // A_rs = beta_r nk_r e^{gamma_r - gamma_s} nk_s P_rs (s < r); M_rs likewise with nq_r
+        // (s <= r).  Two 32-column halves keep the register footprint small.
+        const float g2r = S.gam[r] * kLog2e;
+        const bool arow = tid < 64;                 // warp-uniform
+        const float rowf = arow ? S.bet[r] * S.nk[r] : S.nq[r];
+        const int lim = arow ? r : r + 1;           // entries s < lim
 #pragma unroll
-            for (int s = 0; s < 64; s += 2) {
-                float2 a = make_float2(0.f, 0.f);
-                if (s < 32 || !low) {
-                    a.x = (s < r && r < L) ? br * P[s] * fast_exp2(g2r - S.c2[s]) : 0.f;
-                    a.y = (s + 1 < r && r < L) ? br * P[s + 1] * fast_exp2(g2r - S.c2[s + 1]) : 0.f;
+        for (int hf = 0; hf < 2; ++hf) {
+            float v[32];
+            if (hf == 1 && low) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            } else {
+                float pv[32];
+                tmem_row32(tmem + lane_off + colP + 32 * hf, pv);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int s = 32 * hf + i;
+                    v[i] = (s < lim && r < L) ? rowf * pv[i] * fast_exp2(g2r - S.c2[s]) : 0.f;
                 }
-                *reinterpret_cast<float2 *>(&S.A[r][s]) = a;
             }
-        } else {
-            const float nr = S.nq[r];
+            if (arow) {
 #pragma unroll
-            for (int s = 0; s < 64; ++s)
-                Mrow[s] = ((s < 32 || !low) && s <= r && r < L) ? nr * P[s] * fast_exp2(g2r - S.c2[s]) : 0.f;
+                for (int i = 0; i < 32; i += 2)
+                    *reinterpret_cast<float2 *>(&S.AT[r][32 * hf + i]) = make_float2(v[i], v[i + 1]);
+            } else {
+                // fp32 M over the P half just read (for Mt = M + M Lo); bf16 M into X
+                if (!(hf == 1 && low)) tc::tmem_st32(tmem + lane_off + colP + 32 * hf, v);
+                pack_row<32>(S.post.x, tid, 4 * hf, v);
+            }
         }
+        if (!arow) tc::tmem_wait_st();
         // per-token scalars for the state kernel
         float *ws_s = reinterpret_cast<float *>(wtile + kXTile);
         if (tid < 64) {
@@ -399,15 +417,15 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
         }
     }
     __syncthreads();
-    if (ok) tinv64(S.A, S.T, S.Y);   // ends with a barrier: A is dead from here
-    if (ok) {
-        if (tid < 64) {
-            float lrow[64];
+    if (ok) tinv64_inplace(S.AT, S.post.Y);   // ends with a barrier
+    if (ok && tid < 64) {
+        // Lo = T - I: the strictly lower part of T
 #pragma unroll
-            for (int t = 0; t < 64; ++t) lrow[t] = (t < r) ? S.T[r][t] : 0.f;
-            pack_row<64>(S.x, tid, 0, lrow);
-        } else {
-            pack_row<64>(S.x, tid, 0, Mrow);
+        for (int hf = 0; hf < 2; ++hf) {
+            float lrow[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) lrow[i] = (32 * hf + i < r) ? S.AT[r][32 * hf + i] : 0.f;
+            pack_row<32>(S.post.x, tid, 4 * hf, lrow);
         }
     }
     tc::fence_async_smem();
@@ -417,7 +435,7 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
         tc::fence_after_sync();
         // D[128x64] = X[128 x 64] * Lo[64 x 64]  (B = rows 0..63 of X, MN-major)
         constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
-        const uint32_t xb = tc::smem_u32(S.x);
+        const uint32_t xb = tc::smem_u32(S.post.x);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
             tc::mma_bf16(tmem + colM, tc::sdesc(xb + ks * 32, 16, 1024),
@@ -425,14 +443,19 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
         tc::mma_commit(&S.bar_mma);
     }
     if (ok) ok = wait_all(&S.bar_mma, 1);
-    if (ok) {
+    if (ok && tid >= 64) {
         tc::fence_after_sync();
-        if (tid >= 64) {
-            float mt[64];
-            tmem_row64(tmem + lane_off + colM, mt);
 #pragma unroll
-            for (int s = 0; s < 64; ++s) mt[s] += Mrow[s];   // Mt = M + M Lo
-            pack_row<64>(S.x, tid, 0, mt);                   // over M, which the MMA has read
+        for (int hf = 0; hf < 2; ++hf) {
+            float mt[32];
+            tmem_row32(tmem + lane_off + colM + 32 * hf, mt);
+            if (!(hf == 1 && low)) {
+                float m[32];
+                tmem_row32(tmem + lane_off + colP + 32 * hf, m);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mt[i] += m[i];   // Mt = M + M Lo
+            }
+            pack_row<32>(S.post.x, tid, 4 * hf, mt);          // over M, which the MMA has read
         }
     }
     // The finished [Lo ; Mt] tile leaves in one bulk copy: 128 threads writing their own
@@ -440,7 +463,7 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     tc::fence_async_smem();
     __syncthreads();
     if (ok && tid == 0) {
-        tc::bulk_store(wtile, S.x, kXTile);
+        tc::bulk_store(wtile, S.post.x, kXTile);
         tc::bulk_commit();
         tc::bulk_wait_all();
     }
@@ -908,8 +931,11 @@ gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStre
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
     if (!attr_set[dev].load(std::memory_order_acquire)) {
+        // four prep CTAs per SM need the largest shared-memory carveout
         if (cudaFuncSetAttribute(gdn::chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)prep_smem) != cudaSuccess ||
+            cudaFuncSetAttribute(gdn::chunk_prep_kernel,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess ||
             cudaFuncSetAttribute(gdn::chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)state_smem) != cudaSuccess)
             return GDN_ERR_CUDA;
