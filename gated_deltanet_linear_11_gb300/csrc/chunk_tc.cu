@@ -278,6 +278,8 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     PrepSmem &S = *reinterpret_cast<PrepSmem *>(
         (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023));
+    grid_dependents_launch();
+    grid_dependency_wait();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int slot = blockIdx.x, hv = blockIdx.y;
     const int hk = hv / (p.Hv / p.Hk);
@@ -571,6 +573,8 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     StateSmem &S = *reinterpret_cast<StateSmem *>(
         (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023));
+    grid_dependents_launch();
+    grid_dependency_wait();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int jt = blockIdx.x, hv = blockIdx.y, n = blockIdx.z;
     const int hk = hv / (p.Hv / p.Hk);
@@ -944,11 +948,15 @@ gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStre
     const int slots = (int)((a.T + gdn::kC - 1) / gdn::kC) + a.N;
     if (slots > 0) {
         dim3 g1(slots, a.Hv);
-        gdn::chunk_prep_kernel<<<g1, gdn::kPrepThreads, prep_smem, st>>>(maps, p);
+        if (launch_dependent(gdn::chunk_prep_kernel, g1, dim3(gdn::kPrepThreads), prep_smem, st,
+                             maps, p) != cudaSuccess)
+            return GDN_ERR_CUDA;
     }
     dim3 g2(gdn::kD / gdn::kDVT, a.Hv, a.N);
-    gdn::chunk_state_kernel<<<g2, gdn::kStateThreads, state_smem, st>>>(maps, p);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    if (launch_dependent(gdn::chunk_state_kernel, g2, dim3(gdn::kStateThreads), state_smem, st,
+                         maps, p) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    return GDN_OK;
 }
 
 }  // namespace gdn_host

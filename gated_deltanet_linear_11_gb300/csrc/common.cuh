@@ -47,7 +47,37 @@ __device__ __forceinline__ void report(int32_t *status, int32_t code) {
     if (status) atomicCAS(status, 0, code);
 }
 
+// Programmatic dependent launch.  The prefill kernels are launched so that they may start
+// while the previous kernel of the stream drains; before touching global memory each
+// grid waits until every prerequisite grid has completed and its writes are visible, and
+// it lets its own dependents start launching as soon as all of its CTAs are running.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependents_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace gdn
+
+namespace gdn_host {
+// cudaLaunchKernelEx with programmatic stream serialization allowed.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+}  // namespace gdn_host
 
 // Host-side launch helpers (defined in api.cu).
 namespace gdn_host {

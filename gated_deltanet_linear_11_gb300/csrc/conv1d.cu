@@ -59,6 +59,8 @@ __global__ void __launch_bounds__(kConvThreads, 5)
 conv1d_fwd_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
                   const bf16 *__restrict__ bias, const int32_t *__restrict__ cu,
                   const bf16 *s_in, bf16 *s_out, bf16 *__restrict__ y, int C) {
+    grid_dependents_launch();
+    grid_dependency_wait();
     const int n = blockIdx.z;
     const int tile = blockIdx.y;
     const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * 8;
@@ -218,10 +220,11 @@ gdn_status_t launch_conv1d_fwd(const void *x, int32_t C, const void *w, const vo
     if (N == 0) return GDN_OK;
     const int tiles = max_len > 0 ? (max_len + gdn::kConvTile - 1) / gdn::kConvTile : 1;
     dim3 grid((C / 8 + gdn::kConvThreads - 1) / gdn::kConvThreads, tiles, N);
-    gdn::conv1d_fwd_kernel<<<grid, gdn::kConvThreads, 0, st>>>(
-        (const gdn::bf16 *)x, (const gdn::bf16 *)w, (const gdn::bf16 *)bias, cu,
-        (const gdn::bf16 *)s_in, (gdn::bf16 *)s_out, (gdn::bf16 *)y, C);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    const cudaError_t e = launch_dependent(
+        gdn::conv1d_fwd_kernel, grid, dim3(gdn::kConvThreads), 0, st, (const gdn::bf16 *)x,
+        (const gdn::bf16 *)w, (const gdn::bf16 *)bias, cu, (const gdn::bf16 *)s_in,
+        (gdn::bf16 *)s_out, (gdn::bf16 *)y, C);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 gdn_status_t launch_conv1d_update(const void *x, int32_t N, int32_t C, const void *w,
