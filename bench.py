@@ -402,7 +402,8 @@ def run_ours(args, world, rank, local):
         result["conv_roofline"] = {
             "bound": "hbm", "achieved": conv_b / (conv_avg * 1e-3) / 1e9,
             "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": conv_b / (conv_avg * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+            "frac": conv_b / (conv_avg * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "traffic": kernel_traffic("conv1d.cu")}
         result["clocks"] = clk
         result["wall_s_timed_region"] = t_wall
     if decode is not None:
