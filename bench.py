@@ -329,6 +329,39 @@ def run_ours(args, world, rank, local):
                                "frac": dec_b / (ddec_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                                "traffic": kernel_traffic("decode.cu")}}
 
+        # ---------------- the same step in one launch: gdn_fused_decode from gate logits
+        grng = np.random.default_rng(7)
+        a_raw = torch.from_numpy(grng.standard_normal((Nd, s["Hv"])) + 2.0).float().to(dev)
+        b_raw = torch.from_numpy(grng.standard_normal((Nd, s["Hv"]))).float().to(dev)
+        dx_c = dx.contiguous()
+
+        def fused_step():
+            gdn.gdn_fused_decode(dx_c, dw, None, a_raw, b_raw, dcs, pool, s["Hk"], s["Hv"],
+                                 s["dk"], s["dv"], state_idx=idx, l2norm=True, o=do,
+                                 status=dstatus)
+
+        for _ in range(args.warmup):
+            fused_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            fevs[i][0].record(stream)
+            fused_step()
+            fevs[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        launches += 2 * args.steps
+        fused_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in fevs), world)
+        assert int(dstatus.item()) == 0
+        decode["fused"] = {"kernel": "fused_decode (conv update + gates + recurrent step)",
+                           "ms_per_step": fused_ms,
+                           "state_gbs": dstate / (fused_ms * 1e-3) / 1e9,
+                           "roofline": {"bound": "hbm",
+                                        "achieved": dbytes / (fused_ms * 1e-3) / 1e9,
+                                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                        "frac": dbytes / (fused_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}}
+
     e2e = None
     if "e2e" in legs:
         # ---------------- e2e: pinned host inputs in, outputs out, through the public API

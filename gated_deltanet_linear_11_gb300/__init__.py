@@ -8,6 +8,8 @@ in this package's CUDA kernels.  The functions keep the C entry points' names:
 * :func:`gdn_conv1d_update`    -- decode conv step on a pool of conv states
 * :func:`gdn_chunk_prefill`    -- chunked gated delta rule over packed sequences
 * :func:`gdn_recurrent_decode` -- one-token gated delta rule step on a state pool
+* :func:`gdn_fused_decode`     -- conv update + gates from raw logits + recurrent step,
+  one call
 
 plus :func:`gdn_layer_prefill` / :func:`gdn_layer_decode`, which chain the conv and the
 scan over the packed q||k||v channels (q, k, v are strided views of the conv output;
@@ -26,7 +28,7 @@ from ._lib import GDN_PREFILL_SIMT, GDN_QK_L2NORM, GdnError  # noqa: F401
 
 __all__ = ["gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
            "gdn_chunk_prefill_noalloc",
-           "gdn_recurrent_decode", "gdn_chunk_prefill_workspace_size",
+           "gdn_recurrent_decode", "gdn_fused_decode", "gdn_chunk_prefill_workspace_size",
            "gdn_layer_prefill", "gdn_layer_decode", "GdnError", "load"]
 
 _DT = {torch.bfloat16: _lib.GDN_BF16, torch.float32: _lib.GDN_F32}
@@ -200,6 +202,29 @@ def gdn_recurrent_decode(q, k, v, g, beta, state, state_idx=None, scale=1.0, l2n
         _vp(beta.contiguous()), _vp(state), state.shape[0], _vp(state_idx), float(scale),
         GDN_QK_L2NORM if l2norm else 0, ctypes.byref(do), _vp(status), _stream())
     _lib.check(rc, "gdn_recurrent_decode")
+    return o
+
+
+def gdn_fused_decode(x_qkv, conv_w, conv_bias, a_raw, b_raw, conv_state, state, Hk, Hv, dk,
+                     dv, state_idx=None, scale=1.0, l2norm=True, o=None, status=None):
+    """The whole one-token decode step in one call: conv update (conv_state shifted in
+    place), q/k/v split, optional q/k L2 norm, beta = sigmoid(b_raw), g = -softplus(a_raw),
+    recurrent step (state updated in place).  x_qkv [N, C] bf16; a_raw, b_raw [N, Hv] fp32.
+    Returns o [N, Hv, dv] bf16."""
+    lib = _lib.load()
+    _need_cuda(x_qkv, conv_w, conv_bias, a_raw, b_raw, conv_state, state, state_idx, o, status)
+    N = x_qkv.shape[0]
+    if o is None:
+        o = torch.empty((N, Hv, dv), dtype=torch.bfloat16, device=x_qkv.device)
+    for t in (x_qkv, conv_w, conv_state, state, o):
+        if not t.is_contiguous():
+            raise ValueError("gdn_fused_decode takes contiguous tensors")
+    rc = lib.gdn_fused_decode(
+        _vp(x_qkv), N, Hk, Hv, dk, dv, _vp(conv_w), _vp(conv_bias), _vp(conv_state),
+        _vp(a_raw.contiguous()), _vp(b_raw.contiguous()), _vp(state), state.shape[0],
+        _vp(state_idx), float(scale), GDN_QK_L2NORM if l2norm else 0, _vp(o), _vp(status),
+        _stream())
+    _lib.check(rc, "gdn_fused_decode")
     return o
 
 

@@ -21,7 +21,7 @@ STATUS = {
 
 EXPORTS = ("gdn_status_string", "gdn_version", "gdn_conv1d_fwd", "gdn_conv1d_update",
            "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill",
-           "gdn_chunk_prefill_noalloc", "gdn_recurrent_decode")
+           "gdn_chunk_prefill_noalloc", "gdn_recurrent_decode", "gdn_fused_decode")
 
 NOALLOC_SCRATCH_BYTES = 128 << 20
 
@@ -66,6 +66,8 @@ def load(path: str = LIB_PATH):
                                        tp, vp, vp, vp], i32),
         "gdn_recurrent_decode": ([tp, tp, tp, vp, vp, vp, i32, vp, f32, u32, tp, vp, vp],
                                  i32),
+        "gdn_fused_decode": ([vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp,
+                              f32, u32, vp, vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)

@@ -207,4 +207,29 @@ gdn_status_t gdn_recurrent_decode(const gdn_tensor_t *q, const gdn_tensor_t *k,
     return gdn_host::launch_decode(a, (cudaStream_t)stream);
 }
 
+gdn_status_t gdn_fused_decode(const void *x, int32_t N, int32_t Hk, int32_t Hv, int32_t dk,
+                              int32_t dv, const void *conv_w, const void *conv_bias,
+                              void *conv_state, const float *a_raw, const float *b_raw,
+                              float *state, int32_t P, const int32_t *state_idx, float scale,
+                              uint32_t flags, void *o, int32_t *status_dev, void *stream) {
+    if (N < 0 || P < 0 || N > 65535 || Hk <= 0 || Hv <= 0 || Hk > 65535) return GDN_ERR_SHAPE;
+    if (Hv % Hk != 0) return GDN_ERR_SHAPE;
+    if (dk != 128 || dv != 128) return GDN_ERR_UNSUPPORTED;
+    if (N == 0) return GDN_OK;
+    if (!x || !conv_w || !conv_state || !a_raw || !b_raw || !state || !o) return GDN_ERR_NULL;
+    if (!state_idx && P < N) return GDN_ERR_SHAPE;
+    const int64_t C = 2 * (int64_t)Hk * dk + (int64_t)Hv * dv;
+    if (C > (int64_t)1 << 30) return GDN_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(conv_w) || !aligned16(conv_bias) || !aligned16(conv_state) ||
+        !aligned16(state) || !aligned16(o))
+        return GDN_ERR_LAYOUT;
+    gdn_host::FusedDecodeArgs a;
+    memset(&a, 0, sizeof(a));
+    a.x = x; a.w = conv_w; a.bias = conv_bias; a.conv_state = conv_state;
+    a.a_raw = a_raw; a.b_raw = b_raw; a.state = state; a.idx = state_idx; a.o = o;
+    a.N = N; a.P = P; a.Hk = Hk; a.Hv = Hv; a.C = (int32_t)C;
+    a.scale = scale; a.flags = flags; a.status = status_dev;
+    return gdn_host::launch_fused_decode(a, (cudaStream_t)stream);
+}
+
 }  // extern "C"

@@ -126,4 +126,18 @@ struct DecodeArgs {
     int32_t *status;
 };
 gdn_status_t launch_decode(const DecodeArgs &a, cudaStream_t st);
+
+struct FusedDecodeArgs {
+    const void *x, *w, *bias;   // x [N, C] bf16; w [C, 4] bf16; bias [C] bf16 or NULL
+    void *conv_state;           // [P, 3, C] bf16, shifted in place
+    const float *a_raw, *b_raw; // [N, Hv] fp32 gate logits
+    float *state;               // [P, Hv, 128, 128] fp32, in place
+    const int32_t *idx;         // [N] or NULL (identity)
+    void *o;                    // [N, Hv, 128] bf16
+    int32_t N, P, Hk, Hv, C;
+    float scale;
+    uint32_t flags;
+    int32_t *status;
+};
+gdn_status_t launch_fused_decode(const FusedDecodeArgs &a, cudaStream_t st);
 }  // namespace gdn_host

@@ -149,3 +149,27 @@ def mix_lengths(seed=5, n_each=20, lo=12, hi=32768):
     rng = _rng(seed)
     fresh = [int(x) for x in rng.integers(lo, hi + 1, n_each)]
     return fresh, [2048] * n_each, [1] * n_each
+
+
+def fused_decode_inputs(seed=6, N=256, pool=None, Hk=16, Hv=48, d=128, with_bias=False):
+    """Raw inputs of one decode step for the fused entry: x_qkv [N, C] bf16 (q|k|v before
+    the conv), conv weights [C, 4] (and bias), conv state pool [P, 3, C] bf16, gate logits
+    a_raw = N(0,1) + 2 and b_raw = N(0,1) [N, Hv] fp32 (their -softplus and sigmoid follow
+    the g and beta distributions of the decode workload), fp32 state pool
+    [P, Hv, d, d] ~ N(0, 0.02), and state_idx: N distinct slots of P in random order."""
+    rng = _rng(seed)
+    P = N if pool is None else int(pool)
+    C = conv_channels(Hk, Hv, d, d)
+    x = rng.standard_normal((N, C))
+    w = rng.uniform(-0.5, 0.5, (C, 4))
+    b = rng.uniform(-0.5, 0.5, (C,)) if with_bias else None
+    cs = rng.standard_normal((P, 3, C))
+    a_raw = rng.standard_normal((N, Hv)) + 2.0
+    b_raw = rng.standard_normal((N, Hv))
+    st = rng.standard_normal((P, Hv, d, d)).astype(np.float32) * np.float32(0.02)
+    idx = rng.permutation(P)[:N].astype(np.int32)
+    return dict(x=_t(x, DTYPE_BF16), w=_t(w, DTYPE_BF16),
+                bias=None if b is None else _t(b, DTYPE_BF16), conv_state=_t(cs, DTYPE_BF16),
+                a_raw=_t(a_raw, torch.float32), b_raw=_t(b_raw, torch.float32),
+                state_pool=torch.from_numpy(st), state_idx=torch.from_numpy(idx),
+                Hk=Hk, Hv=Hv, d=d)

@@ -201,6 +201,35 @@ gdn_status_t gdn_recurrent_decode(const gdn_tensor_t *q, const gdn_tensor_t *k,
                                   const gdn_tensor_t *o, int32_t *status_dev,
                                   void *stream);
 
+/*
+ * gdn_fused_decode -- the whole decode step of one token per sequence in one call:
+ * conv update, q/k/v split, optional q/k L2 norm, gates from raw logits, recurrent step.
+ * One kernel does all of it per (sequence, v-head); a second, small one then shifts the
+ * conv-state rows of the q and k channels, which several v-heads read.
+ * Source: the decode path of "[Feature] Add batch invariance support to GDN_ATTN
+ * backend - #45819", which names the fused_sigmoid_gating_delta_rule_update entry
+ * and the state pool indexed by ssm_state_indices; the pages give the name only, so the
+ * gates are taken in their plainest form:
+ *
+ *   beta = sigmoid(b_raw),   g = -softplus(a_raw)   (so exp(g) = 1 / (1 + exp(a_raw)))
+ *
+ * followed by exactly gdn_conv1d_update and gdn_recurrent_decode (same conv bits, the
+ * conv output rounded to bf16 before use).
+ *
+ * x [N, C] bf16 with C = 2*Hk*dk + Hv*dv channels in the order q | k | v, rows contiguous;
+ * conv_w [C, 4] bf16; conv_bias [C] bf16 or NULL; conv_state [P, 3, C] bf16, shifted in
+ * place; a_raw, b_raw [N, Hv] fp32; state [P, Hv, dk, dv] fp32, read once and written
+ * once; state_idx [N] int32 (device, one slot for both pools) or NULL for identity (then
+ * P >= N); o [N, Hv, dv] bf16, rows contiguous.  dk = dv = 128 and Hv % Hk == 0.  All
+ * pointers 16-byte aligned.  Two tokens of one call must not share a slot.  Indices
+ * outside [0, P) set *status_dev = GDN_ERR_INDEX and skip that sequence.
+ */
+gdn_status_t gdn_fused_decode(const void *x, int32_t N, int32_t Hk, int32_t Hv, int32_t dk,
+                              int32_t dv, const void *conv_w, const void *conv_bias,
+                              void *conv_state, const float *a_raw, const float *b_raw,
+                              float *state, int32_t P, const int32_t *state_idx, float scale,
+                              uint32_t flags, void *o, int32_t *status_dev, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -245,3 +245,38 @@ def layer_prefill(x, w, bias, g, beta, cu_seqlens, Hk, Hv, dk, dv, conv_state=No
         outs.append(o)
         states.append(hT)
     return np.concatenate(outs, 1), np.concatenate(states, 1), s_out
+
+
+# ----------------------------------------------------------------- fused decode step
+
+def sigmoid(x):
+    """1 / (1 + e^{-x}) in fp64, evaluated on the side that cannot overflow."""
+    x = _f64(x)
+    e = np.exp(-np.abs(x))
+    return np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+
+
+def softplus(x):
+    """log(1 + e^x) in fp64: max(x, 0) + log1p(e^{-|x|})."""
+    x = _f64(x)
+    return np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
+
+
+def gates_from_logits(a_raw, b_raw):
+    """The fused decode entry's gates ("[Feature] Add batch invariance support to GDN_ATTN
+    backend - #45819" names fused_sigmoid_gating_delta_rule_update and gives no formula;
+    the plainest reading): beta = sigmoid(b_raw), g = -softplus(a_raw).  Returns (g, beta)."""
+    return -softplus(a_raw), sigmoid(b_raw)
+
+
+def fused_decode(x, w, bias, a_raw, b_raw, conv_state_pool, state_pool, Hk, Hv, dk, dv,
+                 state_idx=None, scale=1.0, l2norm=True, nthreads=None):
+    """One decode step from raw inputs: conv update (the output taken as the bf16
+    activation the conv stores), q/k/v split, gates from logits, recurrent step.
+    Returns (o [N, Hv, dv], new conv pool, new state pool)."""
+    y, conv_pool = conv1d_update(x, w, bias, conv_state_pool, state_idx)
+    q, k, v = split_qkv(round_to_bf16(y), Hk, Hv, dk, dv)
+    g, beta = gates_from_logits(a_raw, b_raw)
+    o, pool = recurrent_decode(q, k, v, g, beta, state_pool, state_idx, scale, l2norm,
+                               nthreads)
+    return o, conv_pool, pool

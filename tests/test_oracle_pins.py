@@ -279,3 +279,67 @@ def test_thread_count_does_not_change_result():
     b = oracle.gated_delta_rule(*case[:6], initial_state=case[6], nthreads=5)
     np.testing.assert_array_equal(a[0], b[0])
     np.testing.assert_array_equal(a[1], b[1])
+
+
+# ------------------------------------------------------------- fused decode gates
+
+def test_gate_functions_closed_forms():
+    """sigmoid and softplus against values the mathematics fixes: sigmoid(0) = 1/2 with
+    slope 1/4, sigmoid(x) + sigmoid(-x) = 1; softplus(0) = ln 2 with slope 1/2,
+    softplus(x) - softplus(-x) = x, softplus(x) -> x for large x and e^x for very
+    negative x; and e^{-softplus(a)} = sigmoid(-a).  A wrong sign, a missing log or a
+    scaled argument fails one of these."""
+    x = np.linspace(-30.0, 30.0, 121)
+    s = oracle.sigmoid(x)
+    assert abs(oracle.sigmoid(np.array([0.0]))[0] - 0.5) < 1e-15
+    h = 1e-6
+    slope = (oracle.sigmoid(np.array([h]))[0] - oracle.sigmoid(np.array([-h]))[0]) / (2 * h)
+    assert abs(slope - 0.25) < 1e-9
+    np.testing.assert_allclose(s + oracle.sigmoid(-x), 1.0, rtol=0, atol=1e-15)
+    assert np.all(np.diff(s) > 0)
+    sp = oracle.softplus(x)
+    assert abs(oracle.softplus(np.array([0.0]))[0] - np.log(2.0)) < 1e-15
+    slope = (oracle.softplus(np.array([h]))[0] - oracle.softplus(np.array([-h]))[0]) / (2 * h)
+    assert abs(slope - 0.5) < 1e-9
+    np.testing.assert_allclose(sp - oracle.softplus(-x), x, rtol=0, atol=1e-12)
+    assert abs(oracle.softplus(np.array([50.0]))[0] - 50.0) < 1e-20
+    assert abs(oracle.softplus(np.array([-50.0]))[0] / np.exp(-50.0) - 1.0) < 1e-12
+    np.testing.assert_allclose(np.exp(-sp), oracle.sigmoid(-x), rtol=1e-13, atol=0)
+    g, beta = oracle.gates_from_logits(np.array([[0.0, 3.0]]), np.array([[0.0, -3.0]]))
+    np.testing.assert_allclose(g, -np.log1p(np.exp([[0.0, 3.0]])), rtol=1e-15)
+    np.testing.assert_allclose(beta, [[0.5, 1.0 / (1.0 + np.exp(3.0))]], rtol=1e-15)
+
+
+def test_fused_decode_equals_one_token_layer_prefill():
+    """The fused decode oracle from raw logits equals, per sequence, the prefill-layer
+    oracle (conv over [conv state ; x] + token recurrence, an independent code path) run
+    on a one-token sequence from the same conv state and recurrent state, with the gates
+    of the logits.  Catches a slip in the channel split, the pool indexing or the gates."""
+    rng = np.random.default_rng(41)
+    N, P, Hk, Hv, d = 3, 5, 2, 4, 8
+    C = 2 * Hk * d + Hv * d
+    x = rng.standard_normal((N, C))
+    w = rng.uniform(-0.5, 0.5, (C, 4))
+    bias = rng.uniform(-0.5, 0.5, (C,))
+    conv_pool = rng.standard_normal((P, 3, C))
+    pool = rng.standard_normal((P, Hv, d, d)) * 0.3
+    a_raw = rng.standard_normal((N, Hv)) + 1.0
+    b_raw = rng.standard_normal((N, Hv))
+    idx = np.array([4, 0, 2], np.int32)
+    o, conv_new, pool_new = oracle.fused_decode(x, w, bias, a_raw, b_raw, conv_pool, pool,
+                                                Hk, Hv, d, d, state_idx=idx, scale=0.5,
+                                                l2norm=True)
+    g, beta = oracle.gates_from_logits(a_raw, b_raw)
+    for n in range(N):
+        s = idx[n]
+        o1, h1, c1 = oracle.layer_prefill(x[n:n + 1], w, bias, g[n:n + 1], beta[n:n + 1],
+                                          np.array([0, 1], np.int32), Hk, Hv, d, d,
+                                          conv_state=conv_pool[s:s + 1],
+                                          initial_state=pool[s:s + 1], scale=0.5,
+                                          l2norm=True)
+        np.testing.assert_allclose(o[n], o1[0], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(pool_new[s], h1[0], rtol=1e-12, atol=1e-12)
+        np.testing.assert_array_equal(conv_new[s], c1[0])
+    untouched = [s for s in range(P) if s not in set(idx.tolist())]
+    np.testing.assert_array_equal(pool_new[untouched], pool[untouched])
+    np.testing.assert_array_equal(conv_new[untouched], conv_pool[untouched])
