@@ -22,7 +22,7 @@ struct View {
 };
 
 gdn_status_t view_of(const gdn_tensor_t *t, View &out) {
-    if (!t || !t->ptr) return GDN_ERR_NULL;
+    if (!t) return GDN_ERR_NULL;
     int off;
     if (t->ndim == 3) {
         off = 0;
@@ -36,6 +36,16 @@ gdn_status_t view_of(const gdn_tensor_t *t, View &out) {
     const int64_t T = t->shape[off], H = t->shape[off + 1], D = t->shape[off + 2];
     const int64_t st = t->stride[off], sh = t->stride[off + 1], sd = t->stride[off + 2];
     if (T < 0 || H <= 0 || D <= 0) return GDN_ERR_SHAPE;
+    if (T == 0) {   // an empty view touches no memory: no storage or strides to check
+        out.ptr = t->ptr;
+        out.T = 0;
+        out.H = H;
+        out.D = D;
+        out.tok = H * D;
+        out.dtype = t->dtype;
+        return GDN_OK;
+    }
+    if (!t->ptr) return GDN_ERR_NULL;
     if (T > 1 && H > 1 && sh > st) return GDN_ERR_LAYOUT;  // head-first
     if (sd != 1 || sh != D) return GDN_ERR_LAYOUT;
     if (T > 1 && st < H * D) return GDN_ERR_LAYOUT;
@@ -142,7 +152,7 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t *q, const gdn_tensor_t *k,
     if ((s = view_of(k, K)) != GDN_OK) return s;
     if ((s = view_of(v, V)) != GDN_OK) return s;
     if ((s = view_of(o, O)) != GDN_OK) return s;
-    if (!g || !beta || !cu_seqlens_dev || !cu_seqlens_host) return GDN_ERR_NULL;
+    if ((Q.T > 0 && (!g || !beta)) || !cu_seqlens_dev || !cu_seqlens_host) return GDN_ERR_NULL;
     if (N < 0 || N > 65535) return GDN_ERR_SHAPE;
     if (K.T != Q.T || V.T != Q.T || O.T != Q.T || K.H != Q.H || K.D != Q.D ||
         O.H != V.H || O.D != V.D)
@@ -152,6 +162,19 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t *q, const gdn_tensor_t *k,
     if (!aligned16(initial_state) || !aligned16(final_state)) return GDN_ERR_LAYOUT;
     int32_t max_len = 0;
     if ((s = check_seqlens(cu_seqlens_host, N, Q.T, &max_len)) != GDN_OK) return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (Q.T == 0) {
+        // no tokens: every sequence is empty and keeps its initial state
+        if (final_state && N > 0) {
+            const size_t bytes = (size_t)N * V.H * Q.D * V.D * sizeof(float);
+            const cudaError_t e =
+                initial_state ? cudaMemcpyAsync(final_state, initial_state, bytes,
+                                                cudaMemcpyDeviceToDevice, st)
+                              : cudaMemsetAsync(final_state, 0, bytes, st);
+            if (e != cudaSuccess) return GDN_ERR_CUDA;
+        }
+        return GDN_OK;
+    }
 
     gdn_host::ScanArgs a;
     memset(&a, 0, sizeof(a));
@@ -164,7 +187,6 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t *q, const gdn_tensor_t *k,
     a.scale = scale; a.flags = flags;
     a.in_f32 = Q.dtype == GDN_F32; a.out_f32 = O.dtype == GDN_F32;
     a.status = status_dev; a.ws = workspace; a.ws_bytes = workspace_bytes;
-    cudaStream_t st = (cudaStream_t)stream;
 
     if (!(flags & GDN_PREFILL_SIMT) && gdn_host::chunk_tc_supported(a.dk, a.dv, chunk, a.in_f32)) {
         const size_t need = gdn_host::chunk_tc_workspace(N, Q.T, a.Hk, a.Hv);

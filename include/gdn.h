@@ -129,7 +129,9 @@ gdn_status_t gdn_conv1d_update(const void *x, int32_t N, int32_t C, const void *
  * NULL (not written).  initial_state == final_state is allowed (updated in place).
  * chunk: the chunk length; chunks are anchored at every sequence start, so a sequence's
  * result never depends on its neighbours, and a continuation split at a multiple of
- * `chunk` reproduces the unsplit run bit for bit.
+ * `chunk` reproduces the unsplit run bit for bit.  Zero-length sequences keep their
+ * initial state; with T = 0 the views may have no storage and final_state is a copy of
+ * initial_state (zeros without one).
  * Kernels: q/k/v bf16 with dk = dv = 128 and chunk = 64 run on the tensor cores
  * (tcgen05, TMEM, TMA); q/k/v bf16 or fp32 with dk = dv in {16, 32, 64, 128} and chunk in
  * {16, 32, 64} run on a CUDA-core fp32 kernel when flags has GDN_PREFILL_SIMT or the

@@ -174,6 +174,29 @@ def test_prefill_bf16_d128_parity(simt, l2norm):
 
 
 @pytest.mark.parametrize("simt", [True, False])
+def test_prefill_empty_sequences_keep_their_state(simt):
+    """Zero-length sequences inside a packed batch: their final state is their initial
+    state, bit for bit, and the neighbours match the oracle."""
+    lens = [0, 70, 0, 1, 0]
+    x = inputs.scan_inputs(47, lens, 2, 6, 128, 128, init_state_std=0.02)
+    o, hT = run_prefill(x, simt=simt)
+    o_ref, h_ref = ref_prefill(x)
+    assert_out_close(o, o_ref)
+    assert_state_close(hT, h_ref)
+    for n in (0, 2, 4):
+        assert torch.equal(hT[n].cpu(), x["initial_state"][n])
+
+
+@pytest.mark.parametrize("simt", [True, False])
+def test_prefill_no_tokens_at_all(simt):
+    """T = 0 with N = 2 sequences: nothing to scan; final states equal initial states."""
+    x = inputs.scan_inputs(48, [0, 0], 2, 6, 128, 128, init_state_std=0.02)
+    o, hT = run_prefill(x, simt=simt)
+    assert o.shape[0] == 0
+    assert torch.equal(hT.cpu(), x["initial_state"])
+
+
+@pytest.mark.parametrize("simt", [True, False])
 def test_prefill_weak_decay_long(simt):
     """g = -softplus(N(0,1) - 3): long memory, errors carried across many chunks."""
     x = inputs.scan_inputs(43, [777], 1, 3, 128, 128, g_shift=-3.0, init_state_std=0.02)
