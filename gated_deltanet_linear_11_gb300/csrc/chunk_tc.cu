@@ -29,8 +29,9 @@
 //    The last product takes diag(.)Vn as a bf16 hi + lo pair (one N = 128 MMA pass over
 //    [hi | lo], the halves summed in fp32) so the state keeps fp32-level accuracy; q/k L2 norms and decays are per-token fp32 scalars applied
 //    outside the MMAs, so the raw bf16 inputs are the only operands that are not split.
-//    Eight compute warps: warps w and w+4 share TMEM lanes 32(w%4).. and take 32
-//    columns each; a ninth warp issues all TMA loads and MMAs.
+//    One CTA per (sequence, v-head, dv tile of 64, 48 or 32 columns).  Eight compute
+//    warps: warps w and w+4 share TMEM lanes 32(w%4).. and take half the tile's columns
+//    each; a ninth warp issues all TMA loads and MMAs.
 //
 // Every wait on an mbarrier is bounded in time; on expiry the CTA records GDN_ERR_TIMEOUT
 // in the status word, stops issuing work, frees its TMEM and returns.
@@ -48,7 +49,6 @@ namespace gdn {
 constexpr int kPrepThreads = 128;
 constexpr int kC = 64;          // chunk
 constexpr int kD = 128;         // dk = dv
-constexpr int kDVT = 64;        // dv columns per state CTA
 constexpr uint32_t kXTile = 16384;            // bf16 [128 rows][64] swizzled
 constexpr uint32_t kScal = 4 * kC * 4;        // gamma, beta, nk, nq (fp32 x 64 each)
 constexpr uint32_t kWsTile = kXTile + kScal;  // one workspace tile per (slot, v-head)
@@ -56,6 +56,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s bound on any single wait
 
 struct TcMaps {
     CUtensorMap q, k, v, o;
+    CUtensorMap o48, o32;   // O as 48- and 32-column plain (unswizzled) boxes
 };
 
 struct TcParams {
@@ -69,6 +70,7 @@ struct TcParams {
     int N, Hk, Hv;
     float scale;
     int l2norm;
+    int ntiles;              // dv tiles per head in the state kernel: 2 or 3
     int32_t *status;
 };
 
@@ -536,15 +538,30 @@ __device__ __forceinline__ void issue_chunk_loads(StateSmem &S, const TcMaps &ma
                     "r"(tc::smem_u32(bar)) : "memory");
 }
 
-// h <- a h + (K^T hi + K^T lo) for this thread's 32 columns: the two halves of the state
-// update sit 64 TMEM columns apart.
-__device__ __forceinline__ void fold_update(float (&h)[32], float a, uint32_t taddr) {
-    float u[32], w[32];
-    tc::tmem_ld32(taddr, u);
-    tc::tmem_ld32(taddr + 64, w);
+// NC consecutive TMEM columns of this thread's lane (NC = 32, 24 or 16).
+template <int NC>
+__device__ __forceinline__ void tmem_cols(uint32_t taddr, float (&v)[NC]) {
+    if constexpr (NC == 32) {
+        tc::tmem_ld32(taddr, v);
+    } else if constexpr (NC == 24) {
+        tc::tmem_ld16(taddr, v);
+        tc::tmem_ld8(taddr + 16, v + 16);
+    } else {
+        static_assert(NC == 16, "column count");
+        tc::tmem_ld16(taddr, v);
+    }
     tc::tmem_wait_ld();
+}
+
+// h <- a h + (K^T hi + K^T lo) for this thread's NC columns: the two halves of the state
+// update sit NT = 2 NC TMEM columns apart.
+template <int NC>
+__device__ __forceinline__ void fold_update(float (&h)[NC], float a, uint32_t taddr) {
+    float u[NC], w[NC];
+    tmem_cols<NC>(taddr, u);
+    tmem_cols<NC>(taddr + 2 * NC, w);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) h[i] = fmaf(a, h[i], u[i] + w[i]);
+    for (int i = 0; i < NC; ++i) h[i] = fmaf(a, h[i], u[i] + w[i]);
 }
 
 // Named barrier between the four warps that own TMEM lanes 0..63 (warps 0, 1, 4, 5: the
@@ -565,46 +582,23 @@ __device__ __forceinline__ void out_barrier() {
     asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
-// One CTA per (sequence, v-head, 64-wide dv tile).  Warp 8 issues every TMA load and
-// every MMA, so no compute warp ever stalls behind an issue queue; warps 0..7 hold the
-// fp32 state rows and do the elementwise work of each chunk.
-__global__ void __launch_bounds__(kStateThreads, 1)
-chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    StateSmem &S = *reinterpret_cast<StateSmem *>(
-        (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023));
-    grid_dependents_launch();
-    grid_dependency_wait();
+// The per-CTA program for one dv tile of NT columns starting at column j0 (NT = 64, 48
+// or 32).  Warp 8 issues every TMA load and every MMA, so no compute warp ever stalls
+// behind an issue queue; warps 0..7 hold the fp32 state rows and do the elementwise work.
+// Operand tiles are 64 columns wide in shared memory whatever NT is; an NT-wide MMA reads
+// only the first NT columns.  [hi | lo] is one 2 NT-wide MN-major operand whose 64-column
+// blocks are S.dvh and S.dvl.
+template <int NT>
+__device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, const TcParams &p,
+                                          const CUtensorMap *omap, int j0, int hv, int n) {
+    constexpr int NC = NT / 2;               // columns per thread
+    constexpr int NCH = NC / 8;              // 16-byte chunks per thread row
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int jt = blockIdx.x, hv = blockIdx.y, n = blockIdx.z;
     const int hk = hv / (p.Hv / p.Hk);
-    const int j0 = jt * kDVT;
     const int start = p.cu[n], len = p.cu[n + 1] - start;
     const int nch = (len + kC - 1) / kC;
     const int s0 = slot0(p.cu, n);
     const size_t hoff = ((size_t)n * p.Hv + hv) * kD * kD;
-
-    if (warp == 0) {
-        tc::tmem_alloc(&S.tmem, 256);
-        tc::tmem_relinquish();
-    }
-    if (tid == 0) {
-        tc::mbar_init(&S.bar_tma[0], 1);
-        tc::mbar_init(&S.bar_tma[1], 1);
-        tc::mbar_init(&S.bar_d1, 1);
-        tc::mbar_init(&S.bar_d2, 1);
-        tc::mbar_init(&S.bar_d3, 1);
-        tc::mbar_init(&S.bar_fin, 1);
-        S.abort = 0;
-        tc::mbar_fence_init();
-        tc::prefetch_tmap(&maps.k);
-        tc::prefetch_tmap(&maps.q);
-        tc::prefetch_tmap(&maps.v);
-        tc::prefetch_tmap(&maps.o);
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
     const uint32_t tmem = S.tmem;
     // TMEM columns: D1 [K;Q]h, D2 [Lo;Mt]R, and the state update as a hi | lo pair
     const uint32_t colD1 = 0, colD2 = 64, colS = 128;
@@ -619,10 +613,9 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         const uint64_t dX0 = tc::sdesc(tc::smem_u32(S.x[0]), 16, 1024);        // [Lo;Mt], K-major
         const uint64_t dH = tc::sdesc(tc::smem_u32(S.hb), 8192, 1024);
         const uint64_t dR = tc::sdesc(tc::smem_u32(S.rb), 8192, 1024);
-        // [hi | lo] of d Vn as one N = 128 MN-major operand: lo is the second 64-wide block
         const uint64_t dVhl = tc::sdesc(tc::smem_u32(S.dvh), 8192, 1024);
-        constexpr uint32_t id1 = tc::idesc_bf16(128, 64, 0, 1);
-        constexpr uint32_t id3 = tc::idesc_bf16(128, 128, 1, 1);
+        constexpr uint32_t id1 = tc::idesc_bf16(128, NT, 0, 1);
+        constexpr uint32_t id3 = tc::idesc_bf16(128, 2 * NT, 1, 1);
         const bool leader = lane == 0;
         bool ok = true;
         int issued = 0;                                        // chunks 0..issued-1 are loaded
@@ -693,24 +686,25 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
 
     // ---------------------------------------------------------------- compute warps
     const int quad = warp & 3;           // TMEM lane quarter
-    const int half = warp >> 2;          // which 32 of the 64 dv columns
+    const int half = warp >> 2;          // which NC of the NT dv columns
     const int row = quad * 32 + lane;    // TMEM lane = tile row
     const bool chain = quad < 2;         // rows 0..63: tokens of the chain / dk rows 0..63
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t ch = half * 32;       // this thread's column offset
+    const uint32_t ch = half * NC;       // this thread's column offset in the tile
+    const int c0 = half * NCH;           // ... in 16-byte chunks
 
-    // fp32 master state in registers: dk row `row`, dv columns j0+ch .. +31.
-    float h[32];
+    // fp32 master state in registers: dk row `row`, dv columns j0+ch .. +NC-1.
+    float h[NC];
     if (p.h0) {
         const float4 *src = reinterpret_cast<const float4 *>(p.h0 + hoff + (size_t)row * kD + j0 + ch);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < NC / 4; ++i) {
             const float4 f = src[i];
             h[4 * i] = f.x; h[4 * i + 1] = f.y; h[4 * i + 2] = f.z; h[4 * i + 3] = f.w;
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) h[i] = 0.f;
+        for (int i = 0; i < NC; ++i) h[i] = 0.f;
     }
 
     bool ok = true;
@@ -727,10 +721,10 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
             ok = wait_one(&S.bar_d3, ph ^ 1, abort);
             if (ok) {
                 tc::fence_after_sync();
-                fold_update(h, aL_prev, tmem + lane_off + colS + ch);
+                fold_update<NC>(h, aL_prev, tmem + lane_off + colS + ch);
             }
         }
-        pack_row<32>(S.hb, row, half * 4, h);
+        pack_row<NC>(S.hb, row, c0, h);
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
@@ -742,58 +736,58 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
 
         // --- B: R = beta (V - e^gamma nk K h) on the chain rows; e^gamma nq Q h on the rest
         if (ok) ok = wait_one(&S.bar_d1, ph, abort);
-        float keep[32];
+        float keep[NC];
         {
-            float d1[32];
+            float d1[NC];
             if (ok) {
                 tc::fence_after_sync();
-                tmem_row32(tmem + lane_off + colD1 + ch, d1);
+                tmem_cols<NC>(tmem + lane_off + colD1 + ch, d1);
             } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) d1[j] = 0.f;
+                for (int j = 0; j < NC; ++j) d1[j] = 0.f;
             }
             if (chain) {
                 const float br = bet[r];
                 const float cr = __expf(gr) * nk[r];
                 const bool live = r < L;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < NCH; ++cc) {
                     float vv[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(S.v[st] + tc::swz(r, half * 4 + cc)), vv);
+                    unpack8(*reinterpret_cast<const uint4 *>(S.v[st] + tc::swz(r, c0 + cc)), vv);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         keep[8 * cc + e] = live ? br * (vv[e] - cr * d1[8 * cc + e]) : 0.f;
                 }
-                pack_row<32>(S.rb, r, half * 4, keep);
+                pack_row<NC>(S.rb, r, c0, keep);
                 tc::fence_async_smem();
                 tc::fence_before_sync();
                 chain_barrier();
             } else {
                 const float cq = __expf(gr) * nq[r];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) keep[j] = cq * d1[j];
+                for (int j = 0; j < NC; ++j) keep[j] = cq * d1[j];
             }
         }
 
         // --- C: Vn = R + Lo R -> d Vn as bf16 hi + lo; outputs on the other rows
         if (ok) ok = wait_one(&S.bar_d2, ph, abort);
         {
-            float d2[32];
+            float d2[NC];
             if (ok) {
                 tc::fence_after_sync();
-                tmem_row32(tmem + lane_off + colD2 + ch, d2);
+                tmem_cols<NC>(tmem + lane_off + colD2 + ch, d2);
             } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) d2[j] = 0.f;
+                for (int j = 0; j < NC; ++j) d2[j] = 0.f;
             }
             if (chain) {
                 const float dc = r < L ? __expf(gL - gr) * nk[r] : 0.f;
                 // hi = bf16(x) two at a time (the paired conversion issues at several times
                 // the rate of the single one); lo = x - hi is exact in fp32
-                uint32_t hp[16];
-                float lo[32];
+                uint32_t hp[NC / 2];
+                float lo[NC];
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
+                for (int jj = 0; jj < NC / 2; ++jj) {
                     const float x0 = dc * (keep[2 * jj] + d2[2 * jj]);
                     const float x1 = dc * (keep[2 * jj + 1] + d2[2 * jj + 1]);
                     const __nv_bfloat162 hb2 = __floats2bfloat162_rn(x0, x1);
@@ -802,10 +796,17 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
                     lo[2 * jj + 1] = x1 - __uint_as_float(hp[jj] & 0xffff0000u);
                 }
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    *reinterpret_cast<uint4 *>(S.dvh + tc::swz(r, half * 4 + cc)) =
+                for (int cc = 0; cc < NCH; ++cc) {
+                    // hi: elements ch + 8cc of [hi | lo]; lo: NT + ch + 8cc, in 64-wide blocks
+                    *reinterpret_cast<uint4 *>(S.dvh + tc::swz(r, c0 + cc)) =
                         make_uint4(hp[4 * cc], hp[4 * cc + 1], hp[4 * cc + 2], hp[4 * cc + 3]);
-                pack_row<32>(S.dvl, r, half * 4, lo);
+                    const int el = NT + 8 * (c0 + cc);
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = lo[8 * cc + e];
+                    *reinterpret_cast<uint4 *>((el >= 64 ? S.dvl : S.dvh) + tc::swz(r, (el & 63) >> 3)) =
+                        pack8(f);
+                }
                 tc::fence_async_smem();
                 tc::fence_before_sync();
                 chain_barrier();
@@ -814,20 +815,23 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
                 // keeping 64 scattered row writes per warp off the load/store pipeline that
                 // the chain warps' shared-memory traffic shares.  Stage st was last stored
                 // two chunks ago; allowing one group in flight covers the previous chunk.
+                // A 64-wide tile uses the 128B-swizzled layout, narrower ones plain rows.
                 uint8_t *ob = S.ob[st];
                 if (tid == kOutLeader) tc::bulk_wait_read<1>();
                 out_barrier();
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < NCH; ++cc) {
                     float f[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) f[e] = p.scale * (keep[8 * cc + e] + d2[8 * cc + e]);
-                    *reinterpret_cast<uint4 *>(ob + tc::swz(r, half * 4 + cc)) = pack8(f);
+                    const uint32_t off = NT == 64 ? tc::swz(r, c0 + cc)
+                                                  : (uint32_t)(r * NT * 2 + (c0 + cc) * 16);
+                    *reinterpret_cast<uint4 *>(ob + off) = pack8(f);
                 }
                 tc::fence_async_smem();
                 out_barrier();
                 if (tid == kOutLeader && ok && !*abort) {
-                    tc::tma_store_3d(&maps.o, ob, j0, hv, t0);
+                    tc::tma_store_3d(omap, ob, j0, hv, t0);
                     tc::bulk_commit();
                 }
             } else if (r < L && ok) {
@@ -835,7 +839,7 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
                 uint4 *dst = reinterpret_cast<uint4 *>(p.o + (size_t)(t0 + r) * p.o_tok +
                                                        (size_t)hv * kD + j0 + ch);
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < NCH; ++cc) {
                     float f[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) f[e] = p.scale * (keep[8 * cc + e] + d2[8 * cc + e]);
@@ -850,7 +854,7 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         ok = wait_one(&S.bar_d3, (nch - 1) & 1, abort);
         if (ok) {
             tc::fence_after_sync();
-            fold_update(h, aL_prev, tmem + lane_off + colS + ch);
+            fold_update<NC>(h, aL_prev, tmem + lane_off + colS + ch);
         }
     }
     if (tid == kOutLeader) tc::bulk_wait_all();   // O tiles written before the CTA exits
@@ -859,11 +863,51 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
     if (!*abort && p.hT) {
         float4 *dst = reinterpret_cast<float4 *>(p.hT + hoff + (size_t)row * kD + j0 + ch);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < NC / 4; ++i)
             dst[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
     }
     if (*abort && tid == 0) report(p.status, GDN_ERR_TIMEOUT);
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+// One CTA per (sequence, v-head, dv tile).  The tiles of a head are either two of 64
+// columns or, when that leaves SMs idle (p.ntiles == 3), 48 + 48 + 32 columns.
+__global__ void __launch_bounds__(kStateThreads, 1)
+chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    StateSmem &S = *reinterpret_cast<StateSmem *>(
+        (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023));
+    grid_dependents_launch();
+    grid_dependency_wait();
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int jt = blockIdx.x, hv = blockIdx.y, n = blockIdx.z;
+    if (warp == 0) {
+        tc::tmem_alloc(&S.tmem, 256);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        tc::mbar_init(&S.bar_tma[0], 1);
+        tc::mbar_init(&S.bar_tma[1], 1);
+        tc::mbar_init(&S.bar_d1, 1);
+        tc::mbar_init(&S.bar_d2, 1);
+        tc::mbar_init(&S.bar_d3, 1);
+        tc::mbar_init(&S.bar_fin, 1);
+        S.abort = 0;
+        tc::mbar_fence_init();
+        tc::prefetch_tmap(&maps.k);
+        tc::prefetch_tmap(&maps.q);
+        tc::prefetch_tmap(&maps.v);
+        tc::prefetch_tmap(p.ntiles == 3 ? (jt < 2 ? &maps.o48 : &maps.o32) : &maps.o);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (p.ntiles != 3)
+        state_cta<64>(S, maps, p, &maps.o, 64 * jt, hv, n);
+    else if (jt < 2)
+        state_cta<48>(S, maps, p, &maps.o48, 48 * jt, hv, n);
+    else
+        state_cta<32>(S, maps, p, &maps.o32, 96, hv, n);
 }
 
 }  // namespace gdn
@@ -878,18 +922,34 @@ constexpr int kMaxDevices = 64;
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() { return tensor_map_encoder(); }
 
-// [T, H, 128] bf16 token-major view -> 3-D map (d, head, token), box (64, 1, 64), 128B swizzle.
-bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int H, int64_t tok_stride) {
+// [T, H, 128] bf16 token-major view -> 3-D map (d, head, token), box (width, 1, 64): 64
+// columns with the 128B swizzle, or a narrower plain (unswizzled) box for output tiles.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int H, int64_t tok_stride,
+              int width = 64) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)gdn::kD, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
     cuuint64_t strides[2] = {(cuuint64_t)gdn::kD * 2, (cuuint64_t)tok_stride * 2};
-    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t box[3] = {(cuuint32_t)width, 1, 64};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    width == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count() {
+    static std::atomic<int> cached[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    int v = cached[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
 }
 
 }  // namespace
@@ -910,7 +970,9 @@ gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStre
     if (a.out_f32) return GDN_ERR_DTYPE;
     gdn::TcMaps maps;
     if (!make_map(&maps.q, a.q, a.T, a.Hk, a.q_tok) || !make_map(&maps.k, a.k, a.T, a.Hk, a.k_tok) ||
-        !make_map(&maps.v, a.v, a.T, a.Hv, a.v_tok) || !make_map(&maps.o, a.o, a.T, a.Hv, a.o_tok))
+        !make_map(&maps.v, a.v, a.T, a.Hv, a.v_tok) || !make_map(&maps.o, a.o, a.T, a.Hv, a.o_tok) ||
+        !make_map(&maps.o48, a.o, a.T, a.Hv, a.o_tok, 48) ||
+        !make_map(&maps.o32, a.o, a.T, a.Hv, a.o_tok, 32))
         return GDN_ERR_CUDA;
     gdn::TcParams p;
     p.g = a.g;
@@ -927,6 +989,11 @@ gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStre
     p.scale = a.scale;
     p.l2norm = (a.flags & GDN_QK_L2NORM) ? 1 : 0;
     p.status = a.status;
+    // Three dv tiles per head (48 + 48 + 32 columns) when they still fit one wave on the
+    // SMs, else two of 64: the tiling changes how the columns are grouped, not the
+    // arithmetic of any column.
+    const int sms = sm_count();
+    p.ntiles = (sms > 0 && (int64_t)3 * a.Hv * a.N <= sms) ? 3 : 2;
 
     const size_t prep_smem = sizeof(gdn::PrepSmem) + 1024;
     const size_t state_smem = sizeof(gdn::StateSmem) + 1024;
@@ -952,7 +1019,7 @@ gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStre
                              maps, p) != cudaSuccess)
             return GDN_ERR_CUDA;
     }
-    dim3 g2(gdn::kD / gdn::kDVT, a.Hv, a.N);
+    dim3 g2(p.ntiles, a.Hv, a.N);
     if (launch_dependent(gdn::chunk_state_kernel, g2, dim3(gdn::kStateThreads), state_smem, st,
                          maps, p) != cudaSuccess)
         return GDN_ERR_CUDA;

@@ -206,9 +206,14 @@ def test_prefill_weak_decay_long(simt):
     assert_state_close(hT, h_ref)
 
 
-@pytest.mark.parametrize("simt", [True, False])
-def test_prefill_batch_invariance_bits(simt):
-    lens = [130, 1, 64, 300, 17]
+@pytest.mark.parametrize("simt,lens", [(True, [130, 1, 64, 300, 17]),
+                                       (False, [130, 1, 64, 300, 17]),
+                                       # enough sequences that the batch runs the state
+                                       # kernel with two dv tiles per head and each
+                                       # sequence alone with three
+                                       (False, [130, 1, 64, 300, 17, 65, 2, 200, 64, 9,
+                                                128, 3, 70, 33])])
+def test_prefill_batch_invariance_bits(simt, lens):
     x = inputs.scan_inputs(44, lens, 2, 4, 128, 128, init_state_std=0.02)
     o, hT = run_prefill(x, simt=simt)
     cu = x["cu_seqlens"]
