@@ -241,19 +241,46 @@ def split_qkv(y, Hk, Hv, dk, dv):
 def gdn_layer_prefill(x_qkv, conv_w, conv_bias, g, beta, cu_seqlens, Hk, Hv, dk, dv,
                       conv_state_in=None, conv_state_out=None, initial_state=None,
                       final_state=None, scale=1.0, chunk=64, l2norm=True, y=None, o=None,
-                      cu_seqlens_host=None, workspace=None):
-    """conv1d + SiLU over packed q||k||v, then the chunked scan with in-kernel q/k L2 norm.
+                      cu_seqlens_host=None, workspace=None, status=None):
+    """conv1d + SiLU over packed q||k||v, then the chunked scan with in-kernel q/k L2 norm,
+    in one call of the C entry gdn_layer_prefill (the v channels' conv overlaps the chunk
+    preparation on a second stream; the results equal the two calls in sequence).
 
     Returns (o [T, Hv, dv], final_state [N, Hv, dk, dv], conv_state_out [N, 3, C]).
     """
+    if chunk != 64:
+        raise ValueError("gdn_layer_prefill runs the 64-token chunk scan")
+    lib = _lib.load()
+    _need_cuda(x_qkv, conv_w, conv_bias, g, beta, conv_state_in, conv_state_out,
+               initial_state, final_state, y, o, workspace, status)
+    T, C = x_qkv.shape
+    if C != 2 * Hk * dk + Hv * dv:
+        raise ValueError("x_qkv has %d channels, not 2*Hk*dk + Hv*dv" % C)
+    conv_w = conv_w.reshape(C, 4).contiguous()
     cu, cu_h = _seqlens(cu_seqlens, cu_seqlens_host)
-    y, conv_state_out = gdn_conv1d_fwd(x_qkv, conv_w, conv_bias, cu, conv_state_in,
-                                       conv_state_out, y, cu_seqlens_host=cu_h)
-    q, k, v = split_qkv(y, Hk, Hv, dk, dv)
-    o, final_state = gdn_chunk_prefill(q, k, v, g, beta, cu, chunk=chunk, scale=scale,
-                                       l2norm=l2norm, initial_state=initial_state, o=o,
-                                       final_state=final_state, cu_seqlens_host=cu_h,
-                                       workspace=workspace)
+    N = cu_h.numel() - 1
+    dev = x_qkv.device
+    if y is None:
+        y = torch.empty_like(x_qkv)
+    if conv_state_out is None:
+        conv_state_out = torch.empty((N, 3, C), dtype=x_qkv.dtype, device=dev)
+    if o is None:
+        o = torch.empty((T, Hv, dv), dtype=torch.bfloat16, device=dev)
+    if final_state is None:
+        final_state = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=dev)
+    flags = GDN_QK_L2NORM if l2norm else 0
+    ws_bytes = int(lib.gdn_chunk_prefill_workspace_size(N, T, Hk, Hv, dk, dv, 64, flags))
+    if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    for t in (x_qkv, y, o):
+        if not t.is_contiguous():
+            raise ValueError("gdn_layer_prefill takes contiguous x_qkv, y and o")
+    rc = lib.gdn_layer_prefill(
+        _vp(x_qkv), T, Hk, Hv, dk, dv, _vp(conv_w), _vp(conv_bias), _vp(cu),
+        ctypes.c_void_p(cu_h.data_ptr()), N, _vp(conv_state_in), _vp(conv_state_out), _vp(y),
+        _vp(g.contiguous()), _vp(beta.contiguous()), float(scale), flags, _vp(initial_state),
+        _vp(o), _vp(final_state), _vp(workspace), ws_bytes, _vp(status), _stream())
+    _lib.check(rc, "gdn_layer_prefill")
     return o, final_state, conv_state_out
 
 

@@ -4,9 +4,28 @@
 // before launching anything; nothing here allocates device memory.
 #include <string.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace {
+
+constexpr int kMaxDevices = 64;
+
+// One non-blocking side stream per device, created on first use and kept for the
+// process: the layer entry forks the v channels' conv onto it.
+gdn_status_t side_stream(cudaStream_t *out) {
+    static std::mutex mu;
+    static cudaStream_t streams[kMaxDevices] = {};
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!streams[dev] &&
+        cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    *out = streams[dev];
+    return GDN_OK;
+}
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -139,13 +158,19 @@ size_t gdn_chunk_prefill_workspace_size(int32_t N, int64_t T, int32_t Hk, int32_
     return gdn_host::chunk_tc_workspace(N, T, Hk, Hv);
 }
 
-gdn_status_t gdn_chunk_prefill(const gdn_tensor_t *q, const gdn_tensor_t *k,
-                               const gdn_tensor_t *v, const float *g, const float *beta,
-                               const int32_t *cu_seqlens_dev,
-                               const int32_t *cu_seqlens_host, int32_t N, int32_t chunk,
-                               float scale, uint32_t flags, const float *initial_state,
-                               const gdn_tensor_t *o, float *final_state, void *workspace,
-                               size_t workspace_bytes, int32_t *status_dev, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// gdn_chunk_prefill with one extra hook: an event that the work reading v must wait on
+// (the layer entry produces v on a second stream).
+gdn_status_t chunk_prefill_impl(const gdn_tensor_t *q, const gdn_tensor_t *k,
+                                const gdn_tensor_t *v, const float *g, const float *beta,
+                                const int32_t *cu_seqlens_dev, const int32_t *cu_seqlens_host,
+                                int32_t N, int32_t chunk, float scale, uint32_t flags,
+                                const float *initial_state, const gdn_tensor_t *o,
+                                float *final_state, void *workspace, size_t workspace_bytes,
+                                int32_t *status_dev, void *stream, cudaEvent_t v_ready) {
     View Q, K, V, O;
     gdn_status_t s;
     if ((s = view_of(q, Q)) != GDN_OK) return s;
@@ -192,9 +217,26 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t *q, const gdn_tensor_t *k,
         const size_t need = gdn_host::chunk_tc_workspace(N, Q.T, a.Hk, a.Hv);
         if (need > 0 && (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u)))
             return GDN_ERR_WORKSPACE;
-        return gdn_host::launch_chunk_tc(a, cu_seqlens_host, st);
+        return gdn_host::launch_chunk_tc(a, cu_seqlens_host, st, v_ready);
     }
+    if (v_ready && cudaStreamWaitEvent(st, v_ready, 0) != cudaSuccess) return GDN_ERR_CUDA;
     return gdn_host::launch_chunk_simt(a, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status_t gdn_chunk_prefill(const gdn_tensor_t *q, const gdn_tensor_t *k,
+                               const gdn_tensor_t *v, const float *g, const float *beta,
+                               const int32_t *cu_seqlens_dev,
+                               const int32_t *cu_seqlens_host, int32_t N, int32_t chunk,
+                               float scale, uint32_t flags, const float *initial_state,
+                               const gdn_tensor_t *o, float *final_state, void *workspace,
+                               size_t workspace_bytes, int32_t *status_dev, void *stream) {
+    return chunk_prefill_impl(q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, N, chunk,
+                              scale, flags, initial_state, o, final_state, workspace,
+                              workspace_bytes, status_dev, stream, nullptr);
 }
 
 gdn_status_t gdn_recurrent_decode(const gdn_tensor_t *q, const gdn_tensor_t *k,
@@ -252,6 +294,93 @@ gdn_status_t gdn_fused_decode(const void *x, int32_t N, int32_t Hk, int32_t Hv, 
     a.N = N; a.P = P; a.Hk = Hk; a.Hv = Hv; a.C = (int32_t)C;
     a.scale = scale; a.flags = flags; a.status = status_dev;
     return gdn_host::launch_fused_decode(a, (cudaStream_t)stream);
+}
+
+gdn_status_t gdn_layer_prefill(const void *x, int64_t T, int32_t Hk, int32_t Hv,
+                               int32_t dk, int32_t dv, const void *conv_w,
+                               const void *conv_bias, const int32_t *cu_seqlens_dev,
+                               const int32_t *cu_seqlens_host, int32_t N,
+                               const void *conv_state_in, void *conv_state_out, void *y,
+                               const float *g, const float *beta, float scale, uint32_t flags,
+                               const float *initial_state, void *o, float *final_state,
+                               void *workspace, size_t workspace_bytes, int32_t *status_dev,
+                               void *stream) {
+    if (Hk <= 0 || Hv <= 0 || dk <= 0 || dv <= 0 || T < 0 || N < 0 || N > 65535)
+        return GDN_ERR_SHAPE;
+    const int64_t qk = (int64_t)Hk * dk, C64 = 2 * qk + (int64_t)Hv * dv;
+    if (C64 > (int64_t)1 << 30) return GDN_ERR_SHAPE;
+    const int32_t C = (int32_t)C64;
+    // q, k, v: strided [T, H, D] views of the conv output y [T, C]; o: contiguous
+    gdn_tensor_t tq, tk, tv, to;
+    const gdn_tensor_t *views[4] = {&tq, &tk, &tv, &to};
+    const void *ptrs[4] = {y, y ? (const uint8_t *)y + qk * 2 : nullptr,
+                           y ? (const uint8_t *)y + 2 * qk * 2 : nullptr, o};
+    const int64_t hs[4] = {Hk, Hk, Hv, Hv}, ds[4] = {dk, dk, dv, dv};
+    for (int i = 0; i < 4; ++i) {
+        gdn_tensor_t &t = *const_cast<gdn_tensor_t *>(views[i]);
+        memset(&t, 0, sizeof(t));
+        t.ptr = const_cast<void *>(ptrs[i]);
+        t.ndim = 3;
+        t.dtype = GDN_BF16;
+        t.shape[0] = T; t.shape[1] = hs[i]; t.shape[2] = ds[i];
+        t.stride[0] = i < 3 ? C : hs[i] * ds[i];
+        t.stride[1] = ds[i];
+        t.stride[2] = 1;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T == 0) {
+        gdn_status_t s = gdn_conv1d_fwd(x, T, C, conv_w, conv_bias, cu_seqlens_dev,
+                                        cu_seqlens_host, N, conv_state_in, conv_state_out, y,
+                                        stream);
+        if (s != GDN_OK) return s;
+        return chunk_prefill_impl(&tq, &tk, &tv, g, beta, cu_seqlens_dev, cu_seqlens_host, N,
+                                  64, scale, flags, initial_state, &to, final_state, workspace,
+                                  workspace_bytes, status_dev, stream, nullptr);
+    }
+    // the conv's own checks, on the whole width, before anything is launched
+    if (!x || !conv_w || !cu_seqlens_dev || !cu_seqlens_host || !y) return GDN_ERR_NULL;
+    if (C % 8 != 0 || qk % 8 != 0) return GDN_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(conv_w) || !aligned16(conv_bias) || !aligned16(y) ||
+        !aligned16(conv_state_in) || !aligned16(conv_state_out))
+        return GDN_ERR_LAYOUT;
+    int32_t max_len = 0;
+    gdn_status_t s = check_seqlens(cu_seqlens_host, N, T, &max_len);
+    if (s != GDN_OK) return s;
+    if ((max_len + 15) / 16 > 65535) return GDN_ERR_SHAPE;
+
+    // fork: the v channels' conv on the side stream, the q/k channels' conv and the
+    // chunk preparation (which reads only q and k) on the caller's stream; the state pass
+    // waits for v.  Events live only for this call.
+    cudaStream_t side = nullptr;
+    if ((s = side_stream(&side)) != GDN_OK) return s;
+    cudaEvent_t fork = nullptr, v_ready = nullptr;
+    if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&v_ready, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventDestroy(fork);
+        return GDN_ERR_CUDA;
+    }
+    s = GDN_OK;
+    if (cudaEventRecord(fork, st) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess)
+        s = GDN_ERR_CUDA;
+    // the q/k conv is launched first so its blocks are dispatched ahead of the v conv's
+    if (s == GDN_OK)
+        s = gdn_host::launch_conv1d_fwd(x, C, conv_w, conv_bias, cu_seqlens_dev, N, max_len,
+                                        conv_state_in, conv_state_out, y, st, 0,
+                                        (int32_t)(2 * qk));
+    if (s == GDN_OK)
+        s = gdn_host::launch_conv1d_fwd(x, C, conv_w, conv_bias, cu_seqlens_dev, N, max_len,
+                                        conv_state_in, conv_state_out, y, side,
+                                        (int32_t)(2 * qk), C);
+    if (s == GDN_OK && cudaEventRecord(v_ready, side) != cudaSuccess) s = GDN_ERR_CUDA;
+    if (s == GDN_OK)
+        s = chunk_prefill_impl(&tq, &tk, &tv, g, beta, cu_seqlens_dev, cu_seqlens_host, N, 64,
+                               scale, flags, initial_state, &to, final_state, workspace,
+                               workspace_bytes, status_dev, stream, v_ready);
+    // the caller's stream joins the side stream even if a launch failed
+    if (cudaStreamWaitEvent(st, v_ready, 0) != cudaSuccess && s == GDN_OK) s = GDN_ERR_CUDA;
+    cudaEventDestroy(fork);
+    cudaEventDestroy(v_ready);
+    return s;
 }
 
 }  // extern "C"

@@ -964,7 +964,8 @@ size_t chunk_tc_workspace(int32_t N, int64_t T, int32_t Hk, int32_t Hv) {
     return slots * (size_t)Hv * gdn::kWsTile;
 }
 
-gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStream_t st) {
+gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStream_t st,
+                             cudaEvent_t before_state) {
     (void)cu_host;
     if (a.N == 0) return GDN_OK;
     if (a.out_f32) return GDN_ERR_DTYPE;
@@ -1019,6 +1020,8 @@ gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStre
                              maps, p) != cudaSuccess)
             return GDN_ERR_CUDA;
     }
+    if (before_state && cudaStreamWaitEvent(st, before_state, 0) != cudaSuccess)
+        return GDN_ERR_CUDA;
     dim3 g2(p.ntiles, a.Hv, a.N);
     if (launch_dependent(gdn::chunk_state_kernel, g2, dim3(gdn::kStateThreads), state_smem, st,
                          maps, p) != cudaSuccess)

@@ -81,9 +81,11 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size
 
 // Host-side launch helpers (defined in api.cu).
 namespace gdn_host {
+// channels [c_begin, c_end) of the C-wide rows (c_end < 0: all)
 gdn_status_t launch_conv1d_fwd(const void *x, int32_t C, const void *w, const void *bias,
                                const int32_t *cu, int32_t N, int32_t max_len,
-                               const void *s_in, void *s_out, void *y, cudaStream_t st);
+                               const void *s_in, void *s_out, void *y, cudaStream_t st,
+                               int32_t c_begin = 0, int32_t c_end = -1);
 gdn_status_t launch_conv1d_update(const void *x, int32_t N, int32_t C, const void *w,
                                   const void *bias, void *state, int32_t P,
                                   const int32_t *idx, void *y, int32_t *status,
@@ -108,7 +110,9 @@ struct ScanArgs {
     size_t ws_bytes;
 };
 gdn_status_t launch_chunk_simt(const ScanArgs &a, cudaStream_t st);
-gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStream_t st);
+// before_state: an event the state kernel's launch waits on (the producer of v), or NULL
+gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStream_t st,
+                             cudaEvent_t before_state = nullptr);
 size_t chunk_tc_workspace(int32_t N, int64_t T, int32_t Hk, int32_t Hv);
 bool chunk_tc_supported(int32_t dk, int32_t dv, int32_t chunk, int in_f32);
 

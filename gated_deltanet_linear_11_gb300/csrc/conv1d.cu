@@ -17,17 +17,19 @@ namespace gdn {
 constexpr int kConvThreads = 128;   // threads per block, 8 channels each
 constexpr int kConvTile = 16;       // tokens per thread (anchored at the sequence start)
 
-// grid: (ceil(C / (8*kConvThreads)), ceil(max_len / kConvTile) (>=1), N)
+// Channels [c_begin, c_end) of the C-wide rows.
+// grid: (ceil((c_end - c_begin) / (8*kConvThreads)), ceil(max_len / kConvTile) (>=1), N)
 __global__ void __launch_bounds__(kConvThreads, 5)
 conv1d_fwd_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
                   const bf16 *__restrict__ bias, const int32_t *__restrict__ cu,
-                  const bf16 *s_in, bf16 *s_out, bf16 *__restrict__ y, int C) {
+                  const bf16 *s_in, bf16 *s_out, bf16 *__restrict__ y, int C, int c_begin,
+                  int c_end) {
     grid_dependents_launch();
     grid_dependency_wait();
     const int n = blockIdx.z;
     const int tile = blockIdx.y;
-    const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * 8;
-    if (c0 >= C) return;
+    const int c0 = c_begin + (blockIdx.x * kConvThreads + threadIdx.x) * 8;
+    if (c0 >= c_end) return;
     const int start = cu[n];
     const int L = cu[n + 1] - start;
     const int t0 = tile * kConvTile;
@@ -179,14 +181,16 @@ namespace gdn_host {
 
 gdn_status_t launch_conv1d_fwd(const void *x, int32_t C, const void *w, const void *bias,
                                const int32_t *cu, int32_t N, int32_t max_len,
-                               const void *s_in, void *s_out, void *y, cudaStream_t st) {
-    if (N == 0) return GDN_OK;
+                               const void *s_in, void *s_out, void *y, cudaStream_t st,
+                               int32_t c_begin, int32_t c_end) {
+    if (c_end < 0) c_end = C;
+    if (N == 0 || c_end <= c_begin) return GDN_OK;
     const int tiles = max_len > 0 ? (max_len + gdn::kConvTile - 1) / gdn::kConvTile : 1;
-    dim3 grid((C / 8 + gdn::kConvThreads - 1) / gdn::kConvThreads, tiles, N);
+    dim3 grid(((c_end - c_begin) / 8 + gdn::kConvThreads - 1) / gdn::kConvThreads, tiles, N);
     const cudaError_t e = launch_dependent(
         gdn::conv1d_fwd_kernel, grid, dim3(gdn::kConvThreads), 0, st, (const gdn::bf16 *)x,
         (const gdn::bf16 *)w, (const gdn::bf16 *)bias, cu, (const gdn::bf16 *)s_in,
-        (gdn::bf16 *)s_out, (gdn::bf16 *)y, C);
+        (gdn::bf16 *)s_out, (gdn::bf16 *)y, C, c_begin, c_end);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

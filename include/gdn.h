@@ -204,6 +204,31 @@ gdn_status_t gdn_recurrent_decode(const gdn_tensor_t *q, const gdn_tensor_t *k,
                                   void *stream);
 
 /*
+ * gdn_layer_prefill -- the layer's prefill in one call: gdn_conv1d_fwd over the packed
+ * q | k | v channels, then gdn_chunk_prefill on q, k, v as strided views of its output.
+ * Sources: those of the two entries it chains.  The conv of the v channels runs on a
+ * second stream (owned by the library, one per device) while the q/k channels' conv and
+ * the chunk preparation, which reads only q and k, run on `stream`; the state pass waits
+ * for v, and `stream` waits for the second stream before the call returns, so the caller
+ * sees one ordered stream (CUDA-graph capture included).  Results are bit-identical to
+ * calling the two entries in sequence.
+ *
+ * x [T, C] bf16, C = 2*Hk*dk + Hv*dv, rows contiguous; y [T, C] bf16 receives the conv
+ * output; o [T, Hv, dv] bf16 contiguous; everything else as in gdn_conv1d_fwd and
+ * gdn_chunk_prefill with chunk = 64 (flags may hold GDN_QK_L2NORM and GDN_PREFILL_SIMT).
+ * Calls that share a device share its second stream and are ordered on it.
+ */
+gdn_status_t gdn_layer_prefill(const void *x, int64_t T, int32_t Hk, int32_t Hv,
+                               int32_t dk, int32_t dv, const void *conv_w,
+                               const void *conv_bias, const int32_t *cu_seqlens_dev,
+                               const int32_t *cu_seqlens_host, int32_t N,
+                               const void *conv_state_in, void *conv_state_out, void *y,
+                               const float *g, const float *beta, float scale, uint32_t flags,
+                               const float *initial_state, void *o, float *final_state,
+                               void *workspace, size_t workspace_bytes, int32_t *status_dev,
+                               void *stream);
+
+/*
  * gdn_fused_decode -- the whole decode step of one token per sequence in one call:
  * conv update, q/k/v split, optional q/k L2 norm, gates from raw logits, recurrent step.
  * One kernel does all of it per (sequence, v-head); a second, small one then shifts the

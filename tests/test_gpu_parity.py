@@ -279,3 +279,30 @@ def test_layer_prefill_27b_heads_sampled():
     assert_out_close(o[:, heads], o_ref)
     assert_state_close(hT[:, heads], h_ref)
     np.testing.assert_array_equal(np64(st), st_ref)
+
+
+@pytest.mark.parametrize("l2norm", [True, False])
+def test_layer_prefill_entry_equals_two_calls_bits(l2norm):
+    """gdn_layer_prefill (conv of the v channels on a second stream, overlapping the chunk
+    preparation) gives exactly the bits of gdn_conv1d_fwd followed by gdn_chunk_prefill."""
+    s = dict(Hk=2, Hv=6, dk=128, dv=128)
+    C = inputs.conv_channels(**s)
+    lens = [70, 1, 0, 129, 64]
+    cv = inputs.conv_inputs(81, lens, C, with_state=True, with_bias=True)
+    x = inputs.scan_inputs(82, lens, s["Hk"], s["Hv"], 128, 128, init_state_std=0.02)
+    args = [cv["x"].cuda(), cv["w"].cuda(), cv["bias"].cuda(), x["g"].cuda(),
+            x["beta"].cuda(), cv["cu_seqlens"].cuda()]
+    o1, h1, st1 = gdn.gdn_layer_prefill(*args, s["Hk"], s["Hv"], 128, 128,
+                                        conv_state_in=cv["conv_state"].cuda(),
+                                        initial_state=x["initial_state"].cuda(), l2norm=l2norm,
+                                        scale=0.7, cu_seqlens_host=cv["cu_seqlens"])
+    y, st2 = gdn.gdn_conv1d_fwd(args[0], args[1], args[2], args[5], cv["conv_state"].cuda(),
+                                cu_seqlens_host=cv["cu_seqlens"])
+    q, k, v = gdn.split_qkv(y, s["Hk"], s["Hv"], 128, 128)
+    o2, h2 = gdn.gdn_chunk_prefill(q, k, v, args[3], args[4], args[5], l2norm=l2norm,
+                                   scale=0.7, initial_state=x["initial_state"].cuda(),
+                                   cu_seqlens_host=cv["cu_seqlens"])
+    torch.cuda.synchronize()
+    assert_bits_equal(o1, o2, "o")
+    assert_bits_equal(h1, h2, "final state")
+    assert_bits_equal(st1, st2, "conv state")
