@@ -878,9 +878,10 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
     StateSmem &S = *reinterpret_cast<StateSmem *>(
         (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023));
     grid_dependents_launch();
-    grid_dependency_wait();
     const int tid = threadIdx.x, warp = tid >> 5;
     const int jt = blockIdx.x, hv = blockIdx.y, n = blockIdx.z;
+    // TMEM, barriers and tensor-map prefetches touch no memory of the previous kernel, so
+    // they run before the dependency wait below
     if (warp == 0) {
         tc::tmem_alloc(&S.tmem, 256);
         tc::tmem_relinquish();
@@ -899,6 +900,7 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         tc::prefetch_tmap(&maps.v);
         tc::prefetch_tmap(p.ntiles == 3 ? (jt < 2 ? &maps.o48 : &maps.o32) : &maps.o);
     }
+    grid_dependency_wait();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
