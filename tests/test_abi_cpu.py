@@ -144,3 +144,44 @@ def test_conv_rejections(lib):
                               None) == 1                        # no weights
     assert lib.gdn_conv1d_update(FAKE, 4, 16, FAKE, None, FAKE, 2, None, FAKE, None,
                                  None) == 2                     # P < N without indices
+
+
+@no_gpu
+def test_fused_decode_rejections(lib):
+    vp = None
+    args = dict(x=FAKE, N=4, Hk=2, Hv=6, dk=128, dv=128, w=FAKE, bias=vp, cs=FAKE, a=FAKE,
+                b=FAKE, state=FAKE, P=4, idx=vp, scale=1.0, flags=0, o=FAKE, status=vp,
+                stream=vp)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return lib.gdn_fused_decode(a["x"], a["N"], a["Hk"], a["Hv"], a["dk"], a["dv"],
+                                    a["w"], a["bias"], a["cs"], a["a"], a["b"], a["state"],
+                                    a["P"], a["idx"], a["scale"], a["flags"], a["o"],
+                                    a["status"], a["stream"])
+
+    assert call(Hv=5) == 2                 # Hv % Hk != 0
+    assert call(dk=64, dv=64) == 6         # only d = 128
+    assert call(a=None) == 1               # no gate logits
+    assert call(P=3) == 2                  # P < N without indices
+    assert call(o=FAKE + 8) == 3           # misaligned output
+    assert call(N=0, x=None) == 0          # nothing to do
+
+
+@no_gpu
+def test_layer_prefill_rejections(lib):
+    cu = (ctypes.c_int32 * 2)(0, 8)
+    cup = ctypes.cast(cu, ctypes.c_void_p)
+    bad = (ctypes.c_int32 * 2)(0, 9)
+    badp = ctypes.cast(bad, ctypes.c_void_p)
+
+    def call(x=FAKE, T=8, Hk=2, Hv=6, cu_h=cup, y=FAKE, w=FAKE):
+        return lib.gdn_layer_prefill(x, T, Hk, Hv, 128, 128, w, None, FAKE, cu_h, 1, None,
+                                     None, y, FAKE, FAKE, 1.0, 0, None, FAKE, None, None, 0,
+                                     None, None)
+
+    assert call(Hk=0) == 2                 # no heads
+    assert call(w=None) == 1               # no conv weights
+    assert call(y=None) == 1               # nowhere to put the conv output
+    assert call(cu_h=badp) == 5            # cu_seqlens[N] != T
+    assert call(x=FAKE + 4) == 3           # misaligned input
