@@ -19,16 +19,17 @@
 //    and stores one workspace tile: the 128x64 bf16 X = [Lo ; Mt] (already swizzled)
 //    followed by the chunk's fp32 gamma, beta, nk and nq.
 //
-//  chunk_state (one CTA per (sequence, v-head, 64-column dv tile), walks the chunks):
-//      D1 = [K;Q] h                      (h: fp32 state in TMEM, bf16 copy as operand)
+//  chunk_state (one CTA per (sequence, v-head, dv tile), walks the chunks):
+//      D1 = [K;Q] h                      (h: fp32 state in registers, bf16 copy as operand)
 //      R  = diag(beta) (V - diag(e^gamma nk) K h)              (fp32, CUDA cores)
 //      D2 = X R  = [Lo R ; Mt R]
 //      Vn = R + Lo R                     (identity part of Tinv applied exactly in fp32)
 //      O  = scale (diag(e^gamma nq) Q h + Mt R)
 //      h <- e^{gamma_L} h + K^T diag(e^{gamma_L-gamma} nk) Vn
-//    The last product takes diag(.)Vn as a bf16 hi + lo pair (one N = 128 MMA pass over
-//    [hi | lo], the halves summed in fp32) so the state keeps fp32-level accuracy; q/k L2 norms and decays are per-token fp32 scalars applied
-//    outside the MMAs, so the raw bf16 inputs are the only operands that are not split.
+//    The last product takes diag(.)Vn as a bf16 hi + lo pair (one MMA pass over [hi | lo],
+//    the halves summed in fp32) so the state keeps fp32-level accuracy; q/k L2 norms and
+//    decays are per-token fp32 scalars applied outside the MMAs, so the raw bf16 inputs
+//    are the only operands that are not split.
 //    One CTA per (sequence, v-head, dv tile of 64, 48 or 32 columns).  Eight compute
 //    warps: warps w and w+4 share TMEM lanes 32(w%4).. and take half the tile's columns
 //    each; a ninth warp issues all TMA loads and MMAs.
