@@ -168,7 +168,9 @@ constexpr int kLdY = 34;
 template <int LA, int LB>
 __device__ __forceinline__ void blk_mma(float (&acc)[2][2], const float (*A)[LA], int ar, int ac,
                                         const float (*B)[LB], int br, int bc, int tr, int tc) {
-#pragma unroll
+    // partly unrolled: nine call sites, and the prep kernel's code size shows up as
+    // instruction-fetch stalls
+#pragma unroll 4
     for (int m = 0; m < 16; ++m) {
         const float a0 = A[ar + 2 * tr][ac + m], a1 = A[ar + 2 * tr + 1][ac + m];
         const float2 bb = *reinterpret_cast<const float2 *>(&B[br + m][bc + 2 * tc]);
