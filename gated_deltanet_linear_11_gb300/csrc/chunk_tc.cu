@@ -131,7 +131,7 @@ __device__ __forceinline__ float row_sumsq(const uint8_t *tile, int row, uint32_
     float acc = 0.f;
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
-#pragma unroll
+#pragma unroll 2
         for (int c = 0; c < 8; ++c) {
             float f[8];
             unpack8(*reinterpret_cast<const uint4 *>(tile + kb * blk + tc::swz(row, c)), f);
