@@ -256,29 +256,31 @@ __device__ void tinv64_inplace(float (*AT)[kLd], float (*Y)[kLdY]) {
 
 // ================================================================ chunk_prep kernel
 
+// One region, reused by lifetime.  The [K;Q] K-major tile fills bytes 0..32767 until
+// P = [K;Q]K^T and the norms are taken.  Then the fp32 A, inverted in place into
+// T = (I + A)^{-1}, sits at byte 0, and the inverse's scratch Y at kXOff; once the
+// inverse is done, the bf16 tile X = [Lo ; M] (then [Lo ; Mt]) replaces Y at kXOff.
+constexpr uint32_t kXOff = 17 * 1024;   // 1024-aligned, past A
+static_assert(64 * kLd * 4 <= kXOff && 64 * kLdY * 4 <= kXTile, "prep region layout");
+
 struct PrepSmem {
-    // The [K;Q] K-major tile until P = [K;Q]K^T and the norms are taken; after that its
-    // first 16 KB hold the bf16 tile X = [Lo ; M] (then [Lo ; Mt]) and the rest the
-    // inverse's scratch Y.
-    union {
-        uint8_t kq[32768];
-        struct {
-            uint8_t x[kXTile];
-            float Y[64][kLdY];
-        } post;
-    };
-    float AT[64][kLd];       // A, then T = (I + A)^{-1} in place
+    uint8_t buf[kXOff + kXTile];
     float gam[64], bet[64], nk[64], nq[64];
     float c2[64];            // gamma_s log2(e) - log2(nk_s): the key-side exponent
     float carry;
     uint64_t bar_tma, bar_mma;
     uint32_t tmem;
-};
-static_assert(sizeof(PrepSmem) + 1024 <= 53 * 1024, "four prep CTAs fit on one SM");
 
-// One CTA per (chunk slot, v-head); four CTAs per SM.  TMEM (128 columns): P = [K;Q]K^T
-// in columns 0..63, whose M rows are then replaced by the fp32 M itself; M Lo in 64..127.
-__global__ void __launch_bounds__(kPrepThreads, 4)
+    __device__ uint8_t *kq() { return buf; }
+    __device__ float (*AT())[kLd] { return reinterpret_cast<float (*)[kLd]>(buf); }
+    __device__ float (*Y())[kLdY] { return reinterpret_cast<float (*)[kLdY]>(buf + kXOff); }
+    __device__ uint8_t *x() { return buf + kXOff; }
+};
+static_assert(sizeof(PrepSmem) + 1024 <= 44 * 1024, "five prep CTAs fit on one SM");
+
+// One CTA per (chunk slot, v-head); five CTAs per SM.  TMEM (64 columns): P = [K;Q]K^T,
+// whose M rows are then replaced by the fp32 M itself, onto which M Lo accumulates.
+__global__ void __launch_bounds__(kPrepThreads, 5)
 chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     PrepSmem &S = *reinterpret_cast<PrepSmem *>(
@@ -310,7 +312,7 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     }
 
     if (warp == 0) {
-        tc::tmem_alloc(&S.tmem, 128);
+        tc::tmem_alloc(&S.tmem, 64);
         tc::tmem_relinquish();
     }
     if (tid == 0) {
@@ -325,15 +327,15 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     tc::fence_after_sync();
     const uint32_t tmem = S.tmem;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t colP = 0, colM = 64;
+    const uint32_t colP = 0;
     bool ok = true;
 
     if (tid == 0) {
         tc::mbar_expect_tx(&S.bar_tma, 32768);
-        tc::tma_load_3d(S.kq + 0, &maps.k, &S.bar_tma, 0, hk, t0);
-        tc::tma_load_3d(S.kq + 16384, &maps.k, &S.bar_tma, 64, hk, t0);
-        tc::tma_load_3d(S.kq + 8192, &maps.q, &S.bar_tma, 0, hk, t0);
-        tc::tma_load_3d(S.kq + 16384 + 8192, &maps.q, &S.bar_tma, 64, hk, t0);
+        tc::tma_load_3d(S.kq() + 0, &maps.k, &S.bar_tma, 0, hk, t0);
+        tc::tma_load_3d(S.kq() + 16384, &maps.k, &S.bar_tma, 64, hk, t0);
+        tc::tma_load_3d(S.kq() + 8192, &maps.q, &S.bar_tma, 0, hk, t0);
+        tc::tma_load_3d(S.kq() + 16384 + 8192, &maps.q, &S.bar_tma, 64, hk, t0);
     }
     // inclusive scan of g by warps 0 and 1 (fixed order), while the loads fly
     float gs = gx;
@@ -347,7 +349,7 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     if (ok && tid == 0) {
         tc::fence_after_sync();
         constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 0);
-        const uint32_t base = tc::smem_u32(S.kq);
+        const uint32_t base = tc::smem_u32(S.kq());
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
@@ -359,7 +361,7 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     const int r = tid & 63;
     if (ok) {
         // L2-norm factors of this chunk's k rows (threads 0..63) and q rows (64..127)
-        const float ss = row_sumsq(S.kq, tid, 16384);
+        const float ss = row_sumsq(S.kq(), tid, 16384);
         const float f = p.l2norm ? rsqrtf(ss + 1e-6f) : 1.f;
         if (tid < 64) {
             const float nkr = r < L ? f : 0.f;
@@ -379,6 +381,7 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     uint8_t *wtile = p.ws + ((size_t)slot * p.Hv + hv) * kWsTile;
     // Rows 0..31 of A and M have no entries past column 31 (warp-uniform).
     const bool low = r < 32;
+    float (*AT)[kLd] = S.AT();
     if (ok) {
         tc::fence_after_sync();
         // A_rs = beta_r nk_r e^{gamma_r - gamma_s} nk_s P_rs (s < r); M_rs likewise with nq_r
@@ -405,11 +408,11 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
             if (arow) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 2)
-                    *reinterpret_cast<float2 *>(&S.AT[r][32 * hf + i]) = make_float2(v[i], v[i + 1]);
+                    *reinterpret_cast<float2 *>(&AT[r][32 * hf + i]) = make_float2(v[i], v[i + 1]);
             } else {
-                // fp32 M over the P half just read (for Mt = M + M Lo); bf16 M into X
-                if (!(hf == 1 && low)) tc::tmem_st32(tmem + lane_off + colP + 32 * hf, v);
-                pack_row<32>(S.post.x, tid, 4 * hf, v);
+                // fp32 M over the P half just read: M Lo accumulates onto it, giving
+                // Mt = M + M Lo (rows with no entries in this half store zeros)
+                tc::tmem_st32(tmem + lane_off + colP + 32 * hf, v);
             }
         }
         if (!arow) tc::tmem_wait_st();
@@ -424,15 +427,24 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
         }
     }
     __syncthreads();
-    if (ok) tinv64_inplace(S.AT, S.post.Y);   // ends with a barrier
+    if (ok) tinv64_inplace(AT, S.Y());   // ends with a barrier
+    // X = [Lo ; M] in bf16 over the inverse's scratch
     if (ok && tid < 64) {
         // Lo = T - I: the strictly lower part of T
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
             float lrow[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) lrow[i] = (32 * hf + i < r) ? S.AT[r][32 * hf + i] : 0.f;
-            pack_row<32>(S.post.x, tid, 4 * hf, lrow);
+            for (int i = 0; i < 32; ++i) lrow[i] = (32 * hf + i < r) ? AT[r][32 * hf + i] : 0.f;
+            pack_row<32>(S.x(), tid, 4 * hf, lrow);
+        }
+    } else if (ok) {
+        tc::fence_after_sync();
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            float m[32];
+            tmem_row32(tmem + lane_off + colP + 32 * hf, m);
+            pack_row<32>(S.x(), tid, 4 * hf, m);
         }
     }
     tc::fence_async_smem();
@@ -440,13 +452,14 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     __syncthreads();
     if (ok && tid == 0) {
         tc::fence_after_sync();
-        // D[128x64] = X[128 x 64] * Lo[64 x 64]  (B = rows 0..63 of X, MN-major)
+        // D[128x64] += X[128 x 64] * Lo[64 x 64]  (B = rows 0..63 of X, MN-major).  Rows
+        // 64..127 of D held the fp32 M, so they end as Mt; rows 0..63 are not used.
         constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
-        const uint32_t xb = tc::smem_u32(S.post.x);
+        const uint32_t xb = tc::smem_u32(S.x());
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            tc::mma_bf16(tmem + colM, tc::sdesc(xb + ks * 32, 16, 1024),
-                         tc::sdesc(xb + ks * 2048, 8192, 1024), id, ks > 0);
+            tc::mma_bf16(tmem + colP, tc::sdesc(xb + ks * 32, 16, 1024),
+                         tc::sdesc(xb + ks * 2048, 8192, 1024), id, true);
         tc::mma_commit(&S.bar_mma);
     }
     if (ok) ok = wait_all(&S.bar_mma, 1);
@@ -455,14 +468,8 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
             float mt[32];
-            tmem_row32(tmem + lane_off + colM + 32 * hf, mt);
-            if (!(hf == 1 && low)) {
-                float m[32];
-                tmem_row32(tmem + lane_off + colP + 32 * hf, m);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) mt[i] += m[i];   // Mt = M + M Lo
-            }
-            pack_row<32>(S.post.x, tid, 4 * hf, mt);          // over M, which the MMA has read
+            tmem_row32(tmem + lane_off + colP + 32 * hf, mt);
+            pack_row<32>(S.x(), tid, 4 * hf, mt);             // over M, which the MMA has read
         }
     }
     // The finished [Lo ; Mt] tile leaves in one bulk copy: 128 threads writing their own
@@ -470,14 +477,14 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     tc::fence_async_smem();
     __syncthreads();
     if (ok && tid == 0) {
-        tc::bulk_store(wtile, S.post.x, kXTile);
+        tc::bulk_store(wtile, S.x(), kXTile);
         tc::bulk_commit();
         tc::bulk_wait_all();
     }
     if (!ok && tid == 0) report(p.status, GDN_ERR_TIMEOUT);
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, 128);
+    if (warp == 0) tc::tmem_dealloc(tmem, 64);
 }
 
 // =============================================================== chunk_state kernel
