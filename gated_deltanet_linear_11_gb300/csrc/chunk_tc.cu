@@ -15,7 +15,8 @@
 //      A[r][s]  = beta_r e^{gamma_r-gamma_s} nk_r nk_s (k_r.k_s)          s < r
 //      M[r][s]  = e^{gamma_r-gamma_s} nq_r nk_s (q_r.k_s)                  s <= r
 //      Tinv     = (I + A)^{-1}   (fp32, blocked forward substitution on CUDA cores)
-//      Lo       = Tinv - I,  Mt = M Tinv = M + M Lo   (tcgen05 for M Lo)
+//      Lo       = Tinv - I,  Mt = M Tinv = M + M Lo   (tcgen05: M Lo accumulates onto
+//                                                      the fp32 M held in TMEM)
 //    and stores one workspace tile: the 128x64 bf16 X = [Lo ; Mt] (already swizzled)
 //    followed by the chunk's fp32 gamma, beta, nk and nq.
 //
@@ -1015,7 +1016,7 @@ gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStre
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
     if (!attr_set[dev].load(std::memory_order_acquire)) {
-        // four prep CTAs per SM need the largest shared-memory carveout
+        // five prep CTAs per SM need the largest shared-memory carveout
         if (cudaFuncSetAttribute(gdn::chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)prep_smem) != cudaSuccess ||
             cudaFuncSetAttribute(gdn::chunk_prep_kernel,
