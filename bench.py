@@ -41,7 +41,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 METRIC = "GDN prefill tokens/s per layer (% bf16 TC peak); decode step state GB/s vs HBM"
 SHAPE = dict(Hk=16, Hv=48, dk=128, dv=128)
 CHUNK = 64
-E2E_PARTS = 4   # pieces of the sequence in the e2e leg's copy / compute pipeline
+# Pieces of the sequence in the e2e leg's copy / compute pipeline, in sixteenths of T.
+# The host link is the bound (all inputs take ~0.41 ms to copy in), so the pieces shrink
+# toward the end: what runs after the last copy-in (the last piece's layer and copy-out)
+# is short, and there are few pieces, each of which costs host time.
+E2E_SIXTEENTHS = (6, 6, 3, 1)
 
 
 def prefill_flops_per_token(Hk, Hv, dk, dv, C=CHUNK):
@@ -404,16 +408,20 @@ def run_ours(args, world, rank, local):
         ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
         hh = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
         e2e_steps = max(3, min(args.steps, 10))
-        # The sequence is fed in E2E_PARTS pieces (multiples of the 64-token chunk): piece
-        # i+1 is copied in while piece i runs, and piece i's output is copied out while
-        # piece i+1 runs.  Each piece continues from the previous one's recurrent state and
-        # conv state, which reproduces the unsplit call bit for bit.
-        parts = E2E_PARTS if T % (64 * E2E_PARTS) == 0 else 1
-        plen = T // parts
+        # The sequence is fed in pieces (multiples of the 64-token chunk): piece i+1 is
+        # copied in while piece i runs, and piece i's output is copied out while piece i+1
+        # runs.  Each piece continues from the previous one's recurrent state and conv
+        # state, which reproduces the unsplit call bit for bit.
+        if T % (64 * 16) == 0:
+            plens = [T * k // 16 for k in E2E_SIXTEENTHS]
+        else:
+            plens = [T]
+        parts = len(plens)
+        bounds = [sum(plens[:i]) for i in range(parts + 1)]
         h2d_stream = torch.cuda.Stream(device=dev)
         d2h_stream = torch.cuda.Stream(device=dev)
-        part_cu = torch.tensor([0, plen], dtype=torch.int32)
-        part_cu_d = part_cu.to(dev)
+        part_cu = [torch.tensor([0, n], dtype=torch.int32) for n in plens]
+        part_cu_d = [c.to(dev) for c in part_cu]
         conv_states = [torch.empty_like(conv_out), torch.empty_like(conv_out)]
 
         def e2e_step():
@@ -422,7 +430,7 @@ def run_ours(args, world, rank, local):
             h2d_stream.wait_event(start)
             d2h_stream.wait_event(start)
             for i in range(parts):
-                a, b = i * plen, (i + 1) * plen
+                a, b = bounds[i], bounds[i + 1]
                 with torch.cuda.stream(h2d_stream):
                     x[a:b].copy_(hx[a:b], non_blocking=True)
                     g[a:b].copy_(hg[a:b], non_blocking=True)
@@ -430,12 +438,12 @@ def run_ours(args, world, rank, local):
                     arrived = torch.cuda.Event()
                     arrived.record(h2d_stream)
                 stream.wait_event(arrived)
-                gdn.gdn_layer_prefill(x[a:b], w, None, g[a:b], beta[a:b], part_cu_d, s["Hk"],
+                gdn.gdn_layer_prefill(x[a:b], w, None, g[a:b], beta[a:b], part_cu_d[i], s["Hk"],
                                       s["Hv"], s["dk"], s["dv"],
                                       conv_state_in=None if i == 0 else conv_states[(i - 1) & 1],
                                       conv_state_out=conv_states[i & 1],
                                       initial_state=None if i == 0 else hT, final_state=hT,
-                                      y=y[a:b], o=o[a:b], cu_seqlens_host=part_cu,
+                                      y=y[a:b], o=o[a:b], cu_seqlens_host=part_cu[i],
                                       workspace=ws)
                 computed = torch.cuda.Event()
                 computed.record(stream)
@@ -470,7 +478,8 @@ def run_ours(args, world, rank, local):
         d2h = ho.numel() * 2 + hh.numel() * 4
         e2e = {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "pipeline": "%d pieces of %d tokens: copy-in, layer and copy-out overlap" % (parts, plen)}
+               "pipeline": "%d pieces of %s tokens: copy-in, layer and copy-out overlap"
+                            % (parts, "+".join(str(n) for n in plens))}
 
     result = {
         "metric": METRIC,
