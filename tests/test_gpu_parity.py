@@ -173,6 +173,20 @@ def test_prefill_bf16_d128_parity(simt, l2norm):
     assert_state_close(hT, h_ref)
 
 
+@pytest.mark.parametrize("nseq", [6, 9])
+def test_prefill_tc_scale_parity(nseq):
+    """Tensor-core scan with scale != 1 against the oracle: the scale enters both output
+    paths (full chunks leave by tensor store, a sequence's partial last chunk by plain
+    stores).  On a 152-SM GB300, 6 sequences x 6 v-heads run the state pass in three dv
+    tiles (48 + 48 + 32 columns), 9 sequences in two (3 * Hv * N > 152)."""
+    lens = [64, 130, 1, 192, 77, 5, 128, 63, 200][:nseq]
+    x = inputs.scan_inputs(49, lens, 2, 6, 128, 128, init_state_std=0.02)
+    o, hT = run_prefill(x, scale=0.6)
+    o_ref, h_ref = ref_prefill(x, scale=0.6)
+    assert_out_close(o, o_ref)
+    assert_state_close(hT, h_ref)
+
+
 @pytest.mark.parametrize("simt", [True, False])
 def test_prefill_empty_sequences_keep_their_state(simt):
     """Zero-length sequences inside a packed batch: their final state is their initial
