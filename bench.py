@@ -524,6 +524,11 @@ def run_ours(args, world, rank, local):
         result["decode"] = decode
     if e2e is not None:
         result["e2e"] = e2e
+    if "multiseq" in legs:
+        multiseq, n = multiseq_leg(gdn, inputs, dev, flush_l2, peaks["bf16_tflops"],
+                                   args.warmup, min(args.steps, 10))
+        result["multiseq"] = multiseq
+        launches += n
     result["gpu_launches"] = launches
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(T, samples=args.cpu_samples)
@@ -556,6 +561,67 @@ def cpu_baseline(T, samples=3):
             "kind": "oracle",
             "sample": "fp64 oracle layer prefill (conv + token recurrence), the full "
                       "%d-token 27B-shaped workload, median of %d runs" % (T, samples)}
+
+
+def multiseq_leg(gdn, inputs, dev, flush_l2, peak_tf, warmup, steps):
+    """The chunk scan alone on packed multi-sequence batches (an opt-in leg).  Inputs are
+    drawn on the device from a seeded generator with the workloads' distributions: unit
+    q/k rows, v ~ N(0,1), g = -softplus(N(0,1) + 2), beta = sigmoid(N(0,1)), initial
+    states ~ N(0, 0.02) where the workload continues sequences.  Returns one record per
+    workload and the number of kernel launches."""
+    import torch
+    fresh, cont, _ = inputs.mix_lengths(5)
+    cases = [("27B shapes, 8 x 4096 tokens", [4096] * 8, 16, 48, False),
+             ("27B shapes, 8 sequences U[1, 8192], initial states",
+              inputs.varlen_lengths(3), 16, 48, True),
+             ("4B shapes, the mix's 40 prefills: 20 fresh U[12, 32768] and 20 continuations "
+              "of 2048 on initial states", fresh + cont, 16, 32, True)]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    out, launches = [], 0
+    for name, lens, Hk, Hv, init in cases:
+        T, N = sum(lens), len(lens)
+
+        def unit_rows(t):
+            return (t / t.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+        q = unit_rows(torch.randn(T, Hk, 128, device=dev, generator=gen))
+        k = unit_rows(torch.randn(T, Hk, 128, device=dev, generator=gen))
+        v = torch.randn(T, Hv, 128, device=dev, generator=gen).to(torch.bfloat16)
+        g = -torch.nn.functional.softplus(torch.randn(T, Hv, device=dev, generator=gen) + 2)
+        beta = torch.sigmoid(torch.randn(T, Hv, device=dev, generator=gen))
+        cu_h = torch.zeros(N + 1, dtype=torch.int32)
+        cu_h[1:] = torch.cumsum(torch.tensor(lens), 0)
+        cu = cu_h.to(dev)
+        h0 = torch.randn(N, Hv, 128, 128, device=dev, generator=gen) * 0.02 if init else None
+        o = torch.empty((T, Hv, 128), dtype=torch.bfloat16, device=dev)
+        hT = torch.empty((N, Hv, 128, 128), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(gdn.gdn_chunk_prefill_workspace_size(N, T, Hk, Hv, 128, 128,
+                                                                  CHUNK), 256),
+                         dtype=torch.uint8, device=dev)
+
+        def scan():
+            gdn.gdn_chunk_prefill(q, k, v, g, beta, cu, chunk=CHUNK, initial_state=h0, o=o,
+                                  final_state=hT, cu_seqlens_host=cu_h, workspace=ws)
+        for _ in range(warmup):
+            flush_l2()
+            scan()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for e0, e1 in evs:
+            flush_l2()
+            e0.record()
+            scan()
+            e1.record()
+        torch.cuda.synchronize()
+        launches += 2 * (warmup + steps)
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        tf = prefill_flops_per_token(Hk, Hv, 128, 128) * T / (ms * 1e-3) / 1e12
+        out.append({"workload": name, "tokens": T, "sequences": N, "longest": max(lens),
+                    "ms": ms, "tokens_per_s": T / (ms * 1e-3), "tflops": tf,
+                    "frac": tf / peak_tf})
+        del q, k, v, g, beta, o, hT, ws, h0
+        torch.cuda.empty_cache()
+    return out, launches
 
 
 def run_reference(args, world, rank):
@@ -597,7 +663,9 @@ def main():
     ap.add_argument("--cpu-samples", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--legs", default="prefill,decode,e2e",
-                    help="comma list of legs to run (profiling runs pick one)")
+                    help="comma list of legs to run (profiling runs pick one); "
+                         "'multiseq' (not in the default) times the chunk scan on packed "
+                         "multi-sequence batches")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
