@@ -1,0 +1,50 @@
+"""bench.py's bookkeeping, on the CPU: the algorithmic work the rooflines divide by, and
+the e2e leg's piece schedule.
+
+The figures are the ones the measurement notes state for the 27B layer (T = 4096,
+Hk = 16, Hv = 48, dk = dv = 128, 10240 conv channels) and the 256-sequence decode step.
+"""
+import pytest
+
+import bench
+
+S = dict(Hk=16, Hv=48, dk=128, dv=128)
+
+
+def gemm(m, n, k):
+    return 2.0 * m * n * k
+
+
+def test_prefill_flops_match_the_per_chunk_products():
+    """Per 64-token chunk: [K;Q]K^T per k-head; per v-head Tinv K', Tinv V' and M Vnew
+    (C x C by C x d), W S, Q S and K^T Vnew (C x d by d x d), and the triangular solve."""
+    C, d = 64, 128
+    per_chunk = (S["Hk"] * 2 * gemm(C, C, d)
+                 + S["Hv"] * (3 * gemm(C, d, C) + 3 * gemm(C, d, d))
+                 + S["Hv"] * C ** 3 / 3.0)
+    assert bench.prefill_flops_per_token(**S) == pytest.approx(per_chunk / C, rel=1e-12)
+    assert bench.prefill_flops_per_token(**S) == pytest.approx(7.67e6, rel=2e-3)
+    assert bench.prefill_flops_per_token(**S) * 4096 == pytest.approx(31.4e9, rel=2e-3)
+
+
+def test_bytes_of_each_leg():
+    # q, k (bf16, 16 heads), v, o (bf16, 48 heads), g, beta (fp32) and one fp32 state
+    T = 4096
+    act = T * (2 * 16 * 128 + 2 * 48 * 128) * 2 + T * 48 * 4 * 2
+    state = 48 * 128 * 128 * 4
+    assert bench.prefill_bytes(T, 1, **S) == act + state
+    assert bench.prefill_bytes(T, 1, **S) == pytest.approx(138.9e6, rel=1e-3)
+    # conv: x read and y written in bf16 over 10240 channels, plus the weights and tails
+    assert bench.conv_bytes(T, 10240, 1) == pytest.approx(167.8e6, rel=1e-3)
+    total, st = bench.decode_bytes(256, 16, 48, 128, 128, 10240)
+    assert st == 2 * 256 * 48 * 128 * 128 * 4          # the state read once, written once
+    assert total == pytest.approx(1.661e9, rel=1e-3)
+
+
+def test_e2e_pieces_cover_the_sequence_in_chunk_multiples():
+    T = 4096
+    assert sum(bench.E2E_SIXTEENTHS) == 16
+    pieces = [T * k // 16 for k in bench.E2E_SIXTEENTHS]
+    assert sum(pieces) == T
+    assert all(p % 64 == 0 and p > 0 for p in pieces)
+    assert pieces == sorted(pieces, reverse=True)   # the last piece is the shortest
