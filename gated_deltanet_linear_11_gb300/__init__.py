@@ -291,3 +291,16 @@ def gdn_layer_decode(x_qkv, conv_w, conv_bias, g, beta, conv_state, state, Hk, H
     q, k, v = split_qkv(y, Hk, Hv, dk, dv)
     return gdn_recurrent_decode(q, k, v, g, beta, state, state_idx, scale, l2norm, o,
                                 status)
+
+
+def gdn_selftest_bounded_wait(status=None):
+    """The failure path of the kernels' bounded waits, without a GPU fault: one CTA waits
+    on an mbarrier phase that nothing completes, gives up after about 2 s and writes
+    GDN_ERR_TIMEOUT to the status word.  Returns the status tensor (int32 [1])."""
+    lib = _lib.load()
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _need_cuda(status)
+    _lib.check(lib.gdn_selftest_bounded_wait(_vp(status), _stream()),
+               "gdn_selftest_bounded_wait")
+    return status

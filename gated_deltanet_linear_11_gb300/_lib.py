@@ -22,7 +22,7 @@ STATUS = {
 EXPORTS = ("gdn_status_string", "gdn_version", "gdn_conv1d_fwd", "gdn_conv1d_update",
            "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill",
            "gdn_chunk_prefill_noalloc", "gdn_recurrent_decode", "gdn_fused_decode",
-           "gdn_layer_prefill")
+           "gdn_layer_prefill", "gdn_selftest_bounded_wait")
 
 NOALLOC_SCRATCH_BYTES = 128 << 20
 
@@ -72,6 +72,7 @@ def load(path: str = LIB_PATH):
         "gdn_layer_prefill": ([vp, i64, i32, i32, i32, i32, vp, vp, vp, vp, i32, vp, vp, vp,
                                vp, vp, f32, u32, vp, vp, vp, vp, ctypes.c_size_t, vp, vp],
                               i32),
+        "gdn_selftest_bounded_wait": ([vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)

@@ -383,4 +383,9 @@ gdn_status_t gdn_layer_prefill(const void *x, int64_t T, int32_t Hk, int32_t Hv,
     return s;
 }
 
+gdn_status_t gdn_selftest_bounded_wait(int32_t *status_dev, void *stream) {
+    if (!status_dev) return GDN_ERR_NULL;
+    return gdn_host::launch_wait_selftest(status_dev, (cudaStream_t)stream);
+}
+
 }  // extern "C"

@@ -923,6 +923,20 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         state_cta<32>(S, maps, p, &maps.o32, 96, hv, n);
 }
 
+// Self-test of the bounded waits: one CTA waits, with the helper the kernels above use,
+// on an mbarrier phase that nothing completes.  The wait gives up after kWaitNs and the
+// CTA reports GDN_ERR_TIMEOUT, as a kernel above does when a copy or an MMA it waits on
+// never signals; then it returns, leaving the context usable.
+__global__ void __launch_bounds__(128) wait_selftest_kernel(int32_t *status) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar, 1);   // one arrival expected; none comes
+        tc::mbar_fence_init();
+    }
+    __syncthreads();
+    if (!wait_all(&bar, 0) && threadIdx.x == 0) report(status, GDN_ERR_TIMEOUT);
+}
+
 }  // namespace gdn
 
 // ======================================================================== host side
@@ -975,6 +989,11 @@ size_t chunk_tc_workspace(int32_t N, int64_t T, int32_t Hk, int32_t Hv) {
     (void)Hk;
     const size_t slots = (size_t)((T + gdn::kC - 1) / gdn::kC) + (size_t)N + 1;
     return slots * (size_t)Hv * gdn::kWsTile;
+}
+
+gdn_status_t launch_wait_selftest(int32_t *status, cudaStream_t st) {
+    gdn::wait_selftest_kernel<<<1, 128, 0, st>>>(status);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStream_t st,

@@ -257,6 +257,16 @@ gdn_status_t gdn_fused_decode(const void *x, int32_t N, int32_t Hk, int32_t Hv, 
                               float *state, int32_t P, const int32_t *state_idx, float scale,
                               uint32_t flags, void *o, int32_t *status_dev, void *stream);
 
+/* gdn_selftest_bounded_wait -- checks the failure path of the bounded waits.  Every wait
+ * of the tensor-core kernels on an mbarrier (a TMA copy or an MMA completing) gives up
+ * after 2 s; the CTA then records GDN_ERR_TIMEOUT in the status word, stops issuing work,
+ * frees its TMEM and returns, so the context stays usable.  This entry launches one CTA
+ * that waits, with the same helper, on a barrier phase that nothing completes: about 2 s
+ * later it sets *status_dev = GDN_ERR_TIMEOUT (first writer wins) and exits.
+ * status_dev: device int32, required (NULL: GDN_ERR_NULL, nothing launched).
+ */
+gdn_status_t gdn_selftest_bounded_wait(int32_t *status_dev, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

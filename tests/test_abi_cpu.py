@@ -169,6 +169,10 @@ def test_fused_decode_rejections(lib):
 
 
 @no_gpu
+def test_selftest_needs_a_status_word(lib):
+    assert lib.gdn_selftest_bounded_wait(None, None) == 1   # GDN_ERR_NULL, nothing launched
+
+
 def test_layer_prefill_rejections(lib):
     cu = (ctypes.c_int32 * 2)(0, 8)
     cup = ctypes.cast(cu, ctypes.c_void_p)
