@@ -68,6 +68,32 @@ def test_bruteforce_dense_matrix_form(l2norm):
     np.testing.assert_allclose(hT, hb, atol=1e-12, rtol=0)
 
 
+def test_empty_sequences_in_a_packed_batch():
+    """Zero-length sequences between others: each keeps its initial state and its conv
+    state exactly, and the neighbours equal the dense brute force, whose loop over an
+    empty range does nothing; the chunked form agrees."""
+    lens = [0, 5, 0, 9, 0]
+    case = rand_case(12, lens, 1, 2, 6, 4)
+    o, hT = oracle.gated_delta_rule(*case[:6], scale=0.9, initial_state=case[6])
+    ob, hb = brute_force(*case, scale=0.9, l2norm=False)
+    np.testing.assert_allclose(o, ob, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(hT, hb, atol=1e-12, rtol=0)
+    for n in (0, 2, 4):
+        np.testing.assert_array_equal(hT[n], case[6][n])
+    oc, hc = chunked_gated_delta_rule(*case[:6], chunk=16, scale=0.9,
+                                      initial_state=case[6])
+    np.testing.assert_allclose(oc, o, atol=1e-10, rtol=0)
+    np.testing.assert_allclose(hc, hT, atol=1e-10, rtol=0)
+    rng = np.random.default_rng(13)
+    C = 6
+    x = rng.standard_normal((sum(lens), C))
+    w = rng.uniform(-0.5, 0.5, (C, 4))
+    s0 = rng.standard_normal((len(lens), 3, C))
+    _, s1 = oracle.conv1d_varlen(x, w, None, case[5], s0)
+    for n in (0, 2, 4):
+        np.testing.assert_array_equal(s1[n], s0[n])
+
+
 def test_hand_worked_example():
     with open(os.path.join(GOLDEN, "hand_worked_example.json")) as f:
         ex = json.load(f)
