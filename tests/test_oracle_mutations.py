@@ -1,0 +1,83 @@
+"""The oracle's pins catch plausible mistakes: each case plants one slip in a copy of
+oracle/ (CPU only) and runs tests/test_oracle_pins.py against the copy, which must fail.
+
+The slips are the kinds a restatement of the method can make: a sign in the delta, the
+decay applied after the update or not at all, a wrong GQA head map, the conv taps in
+reverse, SiLU without its x, the conv tail not advanced, the L2 norm without its square
+root, and in the chunked form a decay exponent of the wrong sign, W h added instead of
+subtracted, M without its diagonal; in the gates, logits swapped or sigmoid mirrored.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+PINS = os.path.join(ROOT, "tests", "test_oracle_pins.py")
+
+C_SRC, CHUNKED, INIT = "gdn_oracle.c", "chunked.py", "__init__.py"
+MUTATIONS = {
+    "delta sign": [(C_SRC, "sk[j] = b * (vt[j] - sk[j]);", "sk[j] = b * (vt[j] + sk[j]);")],
+    "decay after the update": [
+        (C_SRC, "        /* S <- exp(g) S */\n        for (int i = 0; i < dk * dv; ++i) h[i] *= a;\n", ""),
+        (C_SRC, "        /* o_t = scale * S_t q_t */\n",
+         "        for (int i = 0; i < dk * dv; ++i) h[i] *= a;\n        /* o_t = scale * S_t q_t */\n")],
+    "no decay": [(C_SRC, "const double a = exp(J->g[(size_t)t * J->Hv + hv]);",
+                  "const double a = 1.0 + 0.0 * J->g[(size_t)t * J->Hv + hv];")],
+    "GQA head map": [(C_SRC, "const int hk = hv / (J->Hv / J->Hk);", "const int hk = hv % J->Hk;")],
+    "conv taps reversed": [(C_SRC, "z += w[(size_t)c * 4 + j] * xt[t + j];",
+                            "z += w[(size_t)c * 4 + j] * xt[t + 3 - j];")],
+    "SiLU without x": [(C_SRC, "= z / (1.0 + exp(-z));", "= 1.0 / (1.0 + exp(-z));")],
+    "conv tail not advanced": [(C_SRC, "state_out[((size_t)n * 3 + j) * C + c] = xt[L + j];",
+                                "state_out[((size_t)n * 3 + j) * C + c] = xt[j];")],
+    "L2 norm without sqrt": [(C_SRC, "const double inv = 1.0 / sqrt(ss + eps);",
+                              "const double inv = 1.0 / (ss + eps);")],
+    "chunked decay sign": [(CHUNKED, "np.exp(np.where(lower_incl, diff, 0.0))",
+                            "np.exp(np.where(lower_incl, -diff, 0.0))")],
+    "chunked W h sign": [(CHUNKED, "Vnew = U - W @ h0", "Vnew = U + W @ h0")],
+    "chunked M without diagonal": [(CHUNKED, "Mqk = np.where(lower_incl,", "Mqk = np.where(lower_strict,")],
+    "gate logits swapped": [(INIT, "return -softplus(a_raw), sigmoid(b_raw)",
+                             "return -softplus(b_raw), sigmoid(a_raw)")],
+    "sigmoid mirrored": [(INIT, "np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))",
+                          "np.where(x >= 0, e / (1.0 + e), 1.0 / (1.0 + e))")],
+}
+
+
+def _copy_oracle(dst, edits):
+    src = os.path.join(ROOT, "oracle")
+    shutil.copytree(src, os.path.join(dst, "oracle"),
+                    ignore=shutil.ignore_patterns("_build", "__pycache__"))
+    for name, old, new in edits:
+        path = os.path.join(dst, "oracle", name)
+        with open(path) as f:
+            text = f.read()
+        assert text.count(old) == 1, "mutation anchor not found once in %s: %r" % (name, old)
+        with open(path, "w") as f:
+            f.write(text.replace(old, new))
+
+
+def _run_pins(dst):
+    env = dict(os.environ, PYTHONPATH=os.pathsep.join([str(dst), ROOT]))
+    return subprocess.run([sys.executable, "-m", "pytest", PINS, "-x", "-q",
+                           "-p", "no:cacheprovider"], cwd=str(dst), env=env,
+                          capture_output=True, text=True, timeout=600)
+
+
+def test_unmutated_copy_passes_and_is_the_one_imported(tmp_path):
+    _copy_oracle(tmp_path, [])
+    env = dict(os.environ, PYTHONPATH=os.pathsep.join([str(tmp_path), ROOT]))
+    where = subprocess.run([sys.executable, "-c", "import oracle; print(oracle.__file__)"],
+                           cwd=str(tmp_path), env=env, capture_output=True, text=True)
+    assert where.stdout.strip().startswith(str(tmp_path)), where.stdout + where.stderr
+    r = _run_pins(tmp_path)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_fail_on_a_planted_mistake(tmp_path, name):
+    _copy_oracle(tmp_path, MUTATIONS[name])
+    r = _run_pins(tmp_path)
+    # exit code 1: tests ran and at least one failed (not a collection or usage error)
+    assert r.returncode == 1, "pins did not catch '%s':\n%s" % (name, r.stdout[-2000:])
