@@ -2,7 +2,8 @@
 oracle/ (CPU only) and runs tests/test_oracle_pins.py against the copy, which must fail.
 
 The slips are the kinds a restatement of the method can make: a sign in the delta, the
-decay applied after the update or not at all, a wrong GQA head map, the conv taps in
+decay applied after the update or not at all, the output read before the update, beta or
+the output scale dropped, a wrong GQA head map, the conv taps in
 reverse, SiLU without its x, the conv tail not advanced, the L2 norm without its square
 root, and in the chunked form a decay exponent of the wrong sign, W h added instead of
 subtracted, M without its diagonal; in the gates, logits swapped or sigmoid mirrored.
@@ -24,6 +25,24 @@ MUTATIONS = {
         (C_SRC, "        /* S <- exp(g) S */\n        for (int i = 0; i < dk * dv; ++i) h[i] *= a;\n", ""),
         (C_SRC, "        /* o_t = scale * S_t q_t */\n",
          "        for (int i = 0; i < dk * dv; ++i) h[i] *= a;\n        /* o_t = scale * S_t q_t */\n")],
+    "output before the update": [
+        (C_SRC, "        /* o_t = scale * S_t q_t */\n"
+                "        double *ot = J->o + ((size_t)t * J->Hv + hv) * dv;\n"
+                "        for (int j = 0; j < dv; ++j) {\n"
+                "            double acc = 0.0;\n"
+                "            for (int i = 0; i < dk; ++i) acc += h[(size_t)i * dv + j] * qn[i];\n"
+                "            ot[j] = J->scale * acc;\n"
+                "        }\n", ""),
+        (C_SRC, "        /* S <- exp(g) S */\n",
+         "        double *ot = J->o + ((size_t)t * J->Hv + hv) * dv;\n"
+         "        for (int j = 0; j < dv; ++j) {\n"
+         "            double acc = 0.0;\n"
+         "            for (int i = 0; i < dk; ++i) acc += h[(size_t)i * dv + j] * qn[i];\n"
+         "            ot[j] = J->scale * acc;\n"
+         "        }\n"
+         "        /* S <- exp(g) S */\n")],
+    "beta dropped": [(C_SRC, "sk[j] = b * (vt[j] - sk[j]);", "sk[j] = (vt[j] - sk[j]) + 0.0 * b;")],
+    "scale dropped": [(C_SRC, "ot[j] = J->scale * acc;", "ot[j] = acc;")],
     "no decay": [(C_SRC, "const double a = exp(J->g[(size_t)t * J->Hv + hv]);",
                   "const double a = 1.0 + 0.0 * J->g[(size_t)t * J->Hv + hv];")],
     "GQA head map": [(C_SRC, "const int hk = hv / (J->Hv / J->Hk);", "const int hk = hv % J->Hk;")],
