@@ -6,7 +6,10 @@ decay applied after the update or not at all, the output read before the update,
 the output scale dropped, a wrong GQA head map, the conv taps in
 reverse, SiLU without its x, the conv tail not advanced, the L2 norm without its square
 root, and in the chunked form a decay exponent of the wrong sign, W h added instead of
-subtracted, M without its diagonal; in the gates, logits swapped or sigmoid mirrored.
+subtracted, M without its diagonal; in the gates, logits swapped or sigmoid mirrored; in
+the layer helpers, the q and k channels swapped, the v channels shifted by one head,
+bf16 rounding toward zero instead of to nearest even, and the per-head (v_heads) branch
+reading the wrong k-head.
 """
 import os
 import shutil
@@ -61,6 +64,21 @@ MUTATIONS = {
                              "return -softplus(b_raw), sigmoid(a_raw)")],
     "sigmoid mirrored": [(INIT, "np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))",
                           "np.where(x >= 0, e / (1.0 + e), 1.0 / (1.0 + e))")],
+    "q and k channels swapped": [
+        (INIT, "q = y[:, :Hk * dk].reshape(T, Hk, dk)",
+         "q = y[:, Hk * dk:2 * Hk * dk].reshape(T, Hk, dk)"),
+        (INIT, "k = y[:, Hk * dk:2 * Hk * dk].reshape(T, Hk, dk)",
+         "k = y[:, :Hk * dk].reshape(T, Hk, dk)")],
+    "v channels one head late": [
+        (INIT, "v = y[:, 2 * Hk * dk:2 * Hk * dk + Hv * dv].reshape(T, Hv, dv)",
+         "v = np.roll(y[:, 2 * Hk * dk:2 * Hk * dk + Hv * dv], dv, axis=1).reshape(T, Hv, dv)")],
+    "bf16 rounding toward zero": [
+        (INIT, "    return torch.from_numpy(np.ascontiguousarray(a, np.float64)).float().to(\n"
+               "        torch.bfloat16).double().numpy()",
+         "    f = np.ascontiguousarray(a, np.float64).astype(np.float32)\n"
+         "    return (f.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32)"
+         ".astype(np.float64) + 0 * torch.zeros(1).numpy()")],
+    "v_heads subset with the wrong k-head": [(INIT, "        hk = hv // G\n", "        hk = hv % Hk\n")],
 }
 
 

@@ -369,3 +369,75 @@ def test_fused_decode_equals_one_token_layer_prefill():
     untouched = [s for s in range(P) if s not in set(idx.tolist())]
     np.testing.assert_array_equal(pool_new[untouched], pool[untouched])
     np.testing.assert_array_equal(conv_new[untouched], conv_pool[untouched])
+
+
+# ------------------------------------------------------------- layer helpers
+
+def test_split_qkv_channel_order_hand_example():
+    """The packed conv output is q || k || v along channels, head by head, as the
+    hand-built fixture lays out from the batch-invariance PR's mixed_qkv split; the same
+    split through torch.split + view (an independent route) agrees on a larger case."""
+    with open(os.path.join(GOLDEN, "qkv_channel_split.json")) as f:
+        ex = json.load(f)
+    q, k, v = oracle.split_qkv(np.array(ex["y"], np.float64), ex["Hk"], ex["Hv"], ex["dk"],
+                               ex["dv"])
+    np.testing.assert_array_equal(q, np.array(ex["expected_q"]))
+    np.testing.assert_array_equal(k, np.array(ex["expected_k"]))
+    np.testing.assert_array_equal(v, np.array(ex["expected_v"]))
+    Hk, Hv, dk, dv, T = 2, 6, 4, 3, 5
+    y = np.arange(T * (2 * Hk * dk + Hv * dv), dtype=np.float64).reshape(T, -1)
+    qt, kt, vt = torch.split(torch.from_numpy(y), [Hk * dk, Hk * dk, Hv * dv], dim=-1)
+    q, k, v = oracle.split_qkv(y, Hk, Hv, dk, dv)
+    np.testing.assert_array_equal(q, qt.reshape(T, Hk, dk).numpy())
+    np.testing.assert_array_equal(k, kt.reshape(T, Hk, dk).numpy())
+    np.testing.assert_array_equal(v, vt.reshape(T, Hv, dv).numpy())
+
+
+def _bf16_rne_bits(x32):
+    """Round-to-nearest-even of fp32 bit patterns to bf16 by integer arithmetic on the
+    bits (add 0x7FFF plus the lowest kept bit, then clear the 16 dropped bits)."""
+    u = x32.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def test_round_to_bf16_nearest_even():
+    """Hand-picked ties and near-ties (every input exact in fp32): a tie goes to the even
+    8-bit mantissa, anything past the tie rounds away; fp64 inputs are first rounded to
+    fp32 (the GPU conv's accumulation type), then to bf16.  A random sample agrees bit
+    for bit with the integer form of round-to-nearest-even."""
+    e = 2.0 ** -8
+    cases = [(1.0, 1.0), (1 + e, 1.0), (1 + 3 * e, 1 + 4 * e), (1 + e + 2.0 ** -23, 1 + 2 * e),
+             (1 + e - 2.0 ** -23, 1.0), (-(1 + 3 * e), -(1 + 4 * e)), (3.0, 3.0),
+             (2.0 ** -130, 2.0 ** -130), (0.0, 0.0), (1 + e + 2.0 ** -30, 1.0)]
+    got = oracle.round_to_bf16(np.array([c[0] for c in cases]))
+    np.testing.assert_array_equal(got, np.array([c[1] for c in cases]))
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal(200000) * np.exp(rng.uniform(-20, 20, 200000))).astype(np.float32)
+    np.testing.assert_array_equal(oracle.round_to_bf16(x.astype(np.float64)), _bf16_rne_bits(x))
+
+
+def test_layer_prefill_v_heads_subset_equals_full_call():
+    """The v_heads branch of the layer oracle (one call per requested v-head with its own
+    k-head) returns exactly the matching heads of the call over all heads, in the order
+    asked for, including heads of different k-head groups."""
+    rng = np.random.default_rng(31)
+    Hk, Hv, d = 2, 6, 4
+    lens = [5, 0, 9]
+    C = 2 * Hk * d + Hv * d
+    T = sum(lens)
+    x = rng.standard_normal((T, C))
+    w = rng.uniform(-0.5, 0.5, (C, 4))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    g = -np.logaddexp(0, rng.standard_normal((T, Hv)))
+    beta = 1 / (1 + np.exp(-rng.standard_normal((T, Hv))))
+    cs = rng.standard_normal((len(lens), 3, C))
+    h0 = rng.standard_normal((len(lens), Hv, d, d)) * 0.3
+    full = oracle.layer_prefill(x, w, None, g, beta, cu, Hk, Hv, d, d, conv_state=cs,
+                                initial_state=h0, scale=0.8)
+    heads = [5, 0, 3, 1, 4]   # k-heads 1, 0, 1, 0, 1 under contiguous groups
+    sub = oracle.layer_prefill(x, w, None, g, beta, cu, Hk, Hv, d, d, conv_state=cs,
+                               initial_state=h0, scale=0.8, v_heads=heads)
+    np.testing.assert_array_equal(sub[0], full[0][:, heads])
+    np.testing.assert_array_equal(sub[1], full[1][:, heads])
+    np.testing.assert_array_equal(sub[2], full[2])
