@@ -18,8 +18,9 @@
 
 namespace {
 
-// Scratch for the tensor-core prefill's per-chunk [Lo ; Mt] tiles.  Every element the
-// kernels read in a call is first written by the same call, so nothing is cleared.
+// Scratch for the tensor-core prefill's per-chunk workspace tiles ([W ; Q'], Z and the
+// per-token scalars).  Every byte the kernels read in a call is first written by the same
+// call, so nothing is cleared.
 __device__ __align__(256) uint8_t gdn_noalloc_scratch[GDN_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
@@ -49,9 +50,12 @@ extern "C" gdn_status_t gdn_chunk_prefill_noalloc(
     if (!q || !v || !cu_seqlens_host) return GDN_ERR_NULL;
     if (q->ndim < 3 || q->ndim > 4 || v->ndim != q->ndim) return GDN_ERR_SHAPE;
     const int off = q->ndim - 3;
-    const size_t need = gdn_chunk_prefill_workspace_size(
-        N, q->shape[off], (int32_t)q->shape[off + 1], (int32_t)v->shape[off + 1],
-        (int32_t)q->shape[off + 2], (int32_t)v->shape[off + 2], chunk, flags);
+    // fp32 activations always run on the CUDA-core kernel, which needs no scratch
+    const size_t need = q->dtype == GDN_F32
+        ? 0
+        : gdn_chunk_prefill_workspace_size(
+              N, q->shape[off], (int32_t)q->shape[off + 1], (int32_t)v->shape[off + 1],
+              (int32_t)q->shape[off + 2], (int32_t)v->shape[off + 2], chunk, flags);
     if (need > (size_t)GDN_NOALLOC_SCRATCH_BYTES) return GDN_ERR_WORKSPACE;
     void *scratch = nullptr;
     if (need > 0) {
