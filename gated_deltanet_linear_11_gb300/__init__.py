@@ -24,7 +24,8 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import GDN_PREFILL_SIMT, GDN_QK_L2NORM, GdnError  # noqa: F401
+from ._lib import (GDN_PREFILL_SIMT, GDN_PREFILL_TILES2, GDN_PREFILL_TILES3,  # noqa: F401
+                   GDN_QK_L2NORM, GdnError)
 
 __all__ = ["gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
            "gdn_chunk_prefill_noalloc",
@@ -125,14 +126,24 @@ def gdn_chunk_prefill_workspace_size(N, T, Hk, Hv, dk, dv, chunk=64, simt=False)
                                                     GDN_PREFILL_SIMT if simt else 0))
 
 
+def _tile_flag(tiles):
+    if tiles is None:
+        return 0
+    if tiles not in (2, 3):
+        raise ValueError("tiles must be 2, 3 or None")
+    return GDN_PREFILL_TILES2 if tiles == 2 else GDN_PREFILL_TILES3
+
+
 def gdn_chunk_prefill(q, k, v, g, beta, cu_seqlens, chunk=64, scale=1.0, l2norm=False,
                       initial_state=None, output_final_state=True, o=None,
                       final_state=None, simt=False, cu_seqlens_host=None, workspace=None,
-                      status=None):
+                      status=None, tiles=None):
     """Chunked gated delta rule over packed sequences.  Returns (o, final_state).
 
     q, k [T, Hk, dk]; v [T, Hv, dv] (token-major views; head-first is rejected);
     g, beta [T, Hv] fp32; cu_seqlens [N+1]; initial_state [N, Hv, dk, dv] fp32 or None.
+    tiles: None (chosen from N and the SM count), 2 or 3 dv tiles per head in the
+    tensor-core state pass; the bits are the same under every choice.
     """
     lib = _lib.load()
     _need_cuda(q, k, v, g, beta, initial_state, o, final_state, workspace, status)
@@ -144,7 +155,8 @@ def gdn_chunk_prefill(q, k, v, g, beta, cu_seqlens, chunk=64, scale=1.0, l2norm=
         o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
     if final_state is None and output_final_state:
         final_state = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=q.device)
-    flags = (GDN_QK_L2NORM if l2norm else 0) | (GDN_PREFILL_SIMT if simt else 0)
+    flags = ((GDN_QK_L2NORM if l2norm else 0) | (GDN_PREFILL_SIMT if simt else 0) |
+             _tile_flag(tiles))
     ws_bytes = int(lib.gdn_chunk_prefill_workspace_size(N, T, Hk, Hv, dk, dv, chunk, flags))
     if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
@@ -165,9 +177,10 @@ def gdn_chunk_prefill_noalloc(q, k, v, g, beta, cu_seqlens, chunk=64, scale=1.0,
                               o=None, final_state=None, simt=False, cu_seqlens_host=None,
                               status=None):
     """gdn_chunk_prefill for callers that cannot allocate device scratch: the library
-    uses its own fixed 128 MiB device array instead of a workspace (see include/gdn.h).
-    Output tensors are still the caller's; pass ``o``/``final_state`` to avoid any
-    allocation on the Python side as well.  Returns (o, final_state)."""
+    uses its own fixed 128 MiB device array instead of a workspace.  Output tensors are
+    still the caller's; pass ``o``/``final_state`` (and the device ``cu_seqlens``, ``g`` and
+    ``beta`` as contiguous tensors) to avoid any allocation on the Python side as well.
+    Returns (o, final_state)."""
     lib = _lib.load()
     _need_cuda(q, k, v, g, beta, initial_state, o, final_state, status)
     cu, cu_h = _seqlens(cu_seqlens, cu_seqlens_host)
@@ -241,10 +254,12 @@ def split_qkv(y, Hk, Hv, dk, dv):
 def gdn_layer_prefill(x_qkv, conv_w, conv_bias, g, beta, cu_seqlens, Hk, Hv, dk, dv,
                       conv_state_in=None, conv_state_out=None, initial_state=None,
                       final_state=None, scale=1.0, chunk=64, l2norm=True, y=None, o=None,
-                      cu_seqlens_host=None, workspace=None, status=None):
+                      cu_seqlens_host=None, workspace=None, status=None, side_stream=None):
     """conv1d + SiLU over packed q||k||v, then the chunked scan with in-kernel q/k L2 norm,
-    in one call of the C entry gdn_layer_prefill (the v channels' conv overlaps the chunk
-    preparation on a second stream; the results equal the two calls in sequence).
+    in one call of the C entry gdn_layer_prefill.  With ``side_stream`` (a second
+    torch.cuda.Stream) the v channels' conv runs on it, overlapping the chunk preparation;
+    without one everything runs on the current stream.  Either way the results equal the
+    two calls in sequence.
 
     Returns (o [T, Hv, dv], final_state [N, Hv, dk, dv], conv_state_out [N, 3, C]).
     """
@@ -279,7 +294,8 @@ def gdn_layer_prefill(x_qkv, conv_w, conv_bias, g, beta, cu_seqlens, Hk, Hv, dk,
         _vp(x_qkv), T, Hk, Hv, dk, dv, _vp(conv_w), _vp(conv_bias), _vp(cu),
         ctypes.c_void_p(cu_h.data_ptr()), N, _vp(conv_state_in), _vp(conv_state_out), _vp(y),
         _vp(g.contiguous()), _vp(beta.contiguous()), float(scale), flags, _vp(initial_state),
-        _vp(o), _vp(final_state), _vp(workspace), ws_bytes, _vp(status), _stream())
+        _vp(o), _vp(final_state), _vp(workspace), ws_bytes, _vp(status),
+        None if side_stream is None else ctypes.c_void_p(side_stream.cuda_stream), _stream())
     _lib.check(rc, "gdn_layer_prefill")
     return o, final_state, conv_state_out
 

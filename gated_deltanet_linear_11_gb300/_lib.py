@@ -12,6 +12,8 @@ LIB_PATH = os.path.join(HERE, "_build", "libgdn.so")
 GDN_BF16, GDN_F32, GDN_I32 = 0, 1, 2
 GDN_QK_L2NORM = 0x1
 GDN_PREFILL_SIMT = 0x100
+GDN_PREFILL_TILES2 = 0x200
+GDN_PREFILL_TILES3 = 0x400
 
 STATUS = {
     0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_LAYOUT",
@@ -70,8 +72,8 @@ def load(path: str = LIB_PATH):
         "gdn_fused_decode": ([vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp,
                               f32, u32, vp, vp, vp], i32),
         "gdn_layer_prefill": ([vp, i64, i32, i32, i32, i32, vp, vp, vp, vp, i32, vp, vp, vp,
-                               vp, vp, f32, u32, vp, vp, vp, vp, ctypes.c_size_t, vp, vp],
-                              i32),
+                               vp, vp, f32, u32, vp, vp, vp, vp, ctypes.c_size_t, vp, vp,
+                               vp], i32),
         "gdn_selftest_bounded_wait": ([vp, vp], i32),
     }
     for name, (args, res) in sig.items():

@@ -1225,10 +1225,18 @@ gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStre
     p.l2norm = (a.flags & GDN_QK_L2NORM) ? 1 : 0;
     p.status = a.status;
     // Three dv tiles per head (48 + 48 + 32 columns) when they still fit one wave on the
-    // SMs, else two of 64: the tiling changes how the columns are grouped, not the
-    // arithmetic of any column.
+    // SMs, else two of 64.  So the tiling follows N and the device's SM count; it changes
+    // how the columns are grouped, not the arithmetic of any column (every column's
+    // products, reductions and roundings are the same whatever tile it sits in), which
+    // keeps a sequence's bits the same alone and in a batch.  GDN_PREFILL_TILES2/3 force
+    // one tiling; the GPU tests run the same sequences under both and compare the bits.
     const int sms = sm_count();
-    p.ntiles = (sms > 0 && (int64_t)3 * a.Hv * a.N <= sms) ? 3 : 2;
+    if (a.flags & GDN_PREFILL_TILES2)
+        p.ntiles = 2;
+    else if (a.flags & GDN_PREFILL_TILES3)
+        p.ntiles = 3;
+    else
+        p.ntiles = (sms > 0 && (int64_t)3 * a.Hv * a.N <= sms) ? 3 : 2;
 
     const size_t prep_smem = sizeof(gdn::PrepSmem) + 1024;
     const size_t state_smem = sizeof(gdn::StateSmem) + 1024;

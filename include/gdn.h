@@ -22,9 +22,9 @@
  *  * The conv state is the three conv inputs that precede the next token, [.., 3, C],
  *    oldest first, in the activation dtype (bf16).
  *  * v-head h reads q/k head h / (Hv / Hk).  g and beta are per v-head, fp32 [T, Hv].
- *  * Every device pointer is owned by the caller.  The library allocates no device or
- *    pinned memory and keeps no global state beyond per-device cached properties and
- *    driver entry points.  Inputs are read-only; only the documented outputs are
+ *  * Every device pointer and stream is owned by the caller.  The library allocates no
+ *    device or pinned memory and keeps no global state beyond per-device cached properties
+ *    (SM count, kernel attributes set once) and driver entry points.  Inputs are read-only; only the documented outputs are
  *    written.  All calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream) and may be issued from several host threads.
  *  * Validation failures return before anything is launched.  Launch failures return
@@ -140,6 +140,12 @@ gdn_status_t gdn_conv1d_update(const void *x, int32_t N, int32_t C, const void *
  * aligned (may be NULL when that size is 0).
  */
 #define GDN_PREFILL_SIMT 0x100u /* force the CUDA-core kernel */
+/* Tensor-core kernel only: the state pass splits each head's 128 dv columns into tiles,
+ * three (48 + 48 + 32) when 3 * Hv * N CTAs fit the device's SMs in one wave, else two of
+ * 64.  These flags force one tiling (tests and tuning); results are bit-identical under
+ * either, since no column's arithmetic depends on its tile. */
+#define GDN_PREFILL_TILES2 0x200u
+#define GDN_PREFILL_TILES3 0x400u
 
 size_t gdn_chunk_prefill_workspace_size(int32_t N, int64_t T, int32_t Hk, int32_t Hv,
                                         int32_t dk, int32_t dv, int32_t chunk,
@@ -162,9 +168,12 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t *q, const gdn_tensor_t *k,
  * Arguments, results, kernels and errors are those of gdn_chunk_prefill, except that the
  * scratch comes from a fixed array of GDN_NOALLOC_SCRATCH_BYTES inside the library's
  * device image, which every GPU that loads the library holds until the process exits.
- * A call whose gdn_chunk_prefill_workspace_size() exceeds that size returns
- * GDN_ERR_WORKSPACE before launching anything.  The call allocates nothing (no cudaMalloc
- * or cudaFree, no allocating library routine).
+ * A tensor-core call needs (ceil(T / 64) + N + 1) * Hv * 49680 bytes (one 49680-byte tile
+ * per chunk slot and v-head); one whose size exceeds the array returns GDN_ERR_WORKSPACE
+ * before launching anything.  With 48 v-heads that admits up to 56 slots, e.g. one
+ * 3456-token sequence or 8 sequences totalling 3008 tokens; fp32 activations (CUDA-core
+ * kernel) need no scratch at any size.  The call allocates nothing (no cudaMalloc or
+ * cudaFree, no allocating library routine).
  * The first call on a device (with that device current) looks up the array's device
  * address once and caches it; make that first call before any stream capture.
  * Every call shares the one array: calls that overlap on the GPU (on different streams,
@@ -206,17 +215,21 @@ gdn_status_t gdn_recurrent_decode(const gdn_tensor_t *q, const gdn_tensor_t *k,
 /*
  * gdn_layer_prefill -- the layer's prefill in one call: gdn_conv1d_fwd over the packed
  * q | k | v channels, then gdn_chunk_prefill on q, k, v as strided views of its output.
- * Sources: those of the two entries it chains.  The conv of the v channels runs on a
- * second stream (owned by the library, one per device) while the q/k channels' conv and
- * the chunk preparation, which reads only q and k, run on `stream`; the state pass waits
- * for v, and `stream` waits for the second stream before the call returns, so the caller
- * sees one ordered stream (CUDA-graph capture included).  Results are bit-identical to
- * calling the two entries in sequence.
+ * Sources: those of the two entries it chains.
+ * side_stream: NULL, or a second cudaStream_t of the caller's (it must differ from
+ * `stream`).  With NULL everything runs on `stream` in order.  With a side stream the conv
+ * of the v channels runs on it while the q/k channels' conv and the chunk preparation,
+ * which reads only q and k, run on `stream`; the state pass waits for v, and `stream`
+ * waits for the side stream before the call returns, so the caller sees one ordered
+ * stream (CUDA-graph capture included).  The library owns no stream: the fork and join
+ * use two events that this call creates and destroys.  Calls that share a side stream are
+ * ordered on it.  Results are bit-identical to calling the two entries in sequence, with
+ * or without a side stream.
  *
  * x [T, C] bf16, C = 2*Hk*dk + Hv*dv, rows contiguous; y [T, C] bf16 receives the conv
  * output; o [T, Hv, dv] bf16 contiguous; everything else as in gdn_conv1d_fwd and
- * gdn_chunk_prefill with chunk = 64 (flags may hold GDN_QK_L2NORM and GDN_PREFILL_SIMT).
- * Calls that share a device share its second stream and are ordered on it.
+ * gdn_chunk_prefill with chunk = 64 (flags may hold GDN_QK_L2NORM, GDN_PREFILL_SIMT and
+ * the tiling flags).
  */
 gdn_status_t gdn_layer_prefill(const void *x, int64_t T, int32_t Hk, int32_t Hv,
                                int32_t dk, int32_t dv, const void *conv_w,
@@ -226,7 +239,7 @@ gdn_status_t gdn_layer_prefill(const void *x, int64_t T, int32_t Hk, int32_t Hv,
                                const float *g, const float *beta, float scale, uint32_t flags,
                                const float *initial_state, void *o, float *final_state,
                                void *workspace, size_t workspace_bytes, int32_t *status_dev,
-                               void *stream);
+                               void *side_stream, void *stream);
 
 /*
  * gdn_fused_decode -- the whole decode step of one token per sequence in one call:

@@ -295,10 +295,11 @@ def test_layer_prefill_27b_heads_sampled():
     np.testing.assert_array_equal(np64(st), st_ref)
 
 
-@pytest.mark.parametrize("l2norm", [True, False])
-def test_layer_prefill_entry_equals_two_calls_bits(l2norm):
-    """gdn_layer_prefill (conv of the v channels on a second stream, overlapping the chunk
-    preparation) gives exactly the bits of gdn_conv1d_fwd followed by gdn_chunk_prefill."""
+@pytest.mark.parametrize("l2norm,side", [(True, True), (False, True), (True, False)])
+def test_layer_prefill_entry_equals_two_calls_bits(l2norm, side):
+    """gdn_layer_prefill (with a caller's side stream, the conv of the v channels runs on
+    it, overlapping the chunk preparation; without one, everything runs on the current
+    stream) gives exactly the bits of gdn_conv1d_fwd followed by gdn_chunk_prefill."""
     s = dict(Hk=2, Hv=6, dk=128, dv=128)
     C = inputs.conv_channels(**s)
     lens = [70, 1, 0, 129, 64]
@@ -309,7 +310,8 @@ def test_layer_prefill_entry_equals_two_calls_bits(l2norm):
     o1, h1, st1 = gdn.gdn_layer_prefill(*args, s["Hk"], s["Hv"], 128, 128,
                                         conv_state_in=cv["conv_state"].cuda(),
                                         initial_state=x["initial_state"].cuda(), l2norm=l2norm,
-                                        scale=0.7, cu_seqlens_host=cv["cu_seqlens"])
+                                        scale=0.7, cu_seqlens_host=cv["cu_seqlens"],
+                                        side_stream=torch.cuda.Stream() if side else None)
     y, st2 = gdn.gdn_conv1d_fwd(args[0], args[1], args[2], args[5], cv["conv_state"].cuda(),
                                 cu_seqlens_host=cv["cu_seqlens"])
     q, k, v = gdn.split_qkv(y, s["Hk"], s["Hv"], 128, 128)
@@ -320,3 +322,27 @@ def test_layer_prefill_entry_equals_two_calls_bits(l2norm):
     assert_bits_equal(o1, o2, "o")
     assert_bits_equal(h1, h2, "final state")
     assert_bits_equal(st1, st2, "conv state")
+
+
+@pytest.mark.parametrize("l2norm", [False, True])
+def test_prefill_dv_tilings_give_identical_bits(l2norm):
+    """The state pass groups each head's 128 dv columns into two tiles of 64 or three of
+    48 + 48 + 32 (chosen from N and the SM count).  The same batch run under both tilings,
+    forced by flag, gives the same bits for o and the final states, and the oracle
+    agrees with both."""
+    lens = [130, 1, 64, 300, 17, 65]
+    x = inputs.scan_inputs(51, lens, 2, 6, 128, 128, normalise_qk=not l2norm,
+                           init_state_std=0.02)
+    xg = cuda(x)
+    outs = []
+    for tiles in (2, 3):
+        o, hT = gdn.gdn_chunk_prefill(xg["q"], xg["k"], xg["v"], xg["g"], xg["beta"],
+                                      xg["cu_seqlens"], l2norm=l2norm,
+                                      initial_state=xg["initial_state"],
+                                      cu_seqlens_host=x["cu_seqlens"], tiles=tiles)
+        outs.append((o, hT))
+    assert_bits_equal(outs[0][0], outs[1][0], "o, two vs three dv tiles")
+    assert_bits_equal(outs[0][1], outs[1][1], "final state, two vs three dv tiles")
+    o_ref, h_ref = ref_prefill(x, l2norm=l2norm)
+    assert_out_close(outs[0][0], o_ref)
+    assert_state_close(outs[0][1], h_ref)
