@@ -244,6 +244,9 @@ def run_ours(args, world, rank, local):
         flush.zero_()
         flush_rd.max()
     q_v, k_v, v_v = gdn.split_qkv(y, s["Hk"], s["Hv"], s["dk"], s["dv"])
+    # the layer entry runs the v channels' conv on this second stream, under the chunk
+    # preparation
+    side = torch.cuda.Stream(device=dev)
 
     scan_launches = 2 if ws_bytes else 1   # tensor-core path: prep + state kernels
     legs = set(args.legs.split(","))
@@ -255,12 +258,12 @@ def run_ours(args, world, rank, local):
 
     if "prefill" in legs:
         # (1) the step: one gdn_layer_prefill call (conv over q|k|v, then the chunk scan;
-        #     the v channels' conv runs on the library's second stream under the chunk
+        #     the v channels' conv runs on the caller's side stream under the chunk
         #     preparation), timed as a whole
         def layer_step():
             gdn.gdn_layer_prefill(x, w, None, g, beta, cu, s["Hk"], s["Hv"], s["dk"], s["dv"],
                                   conv_state_out=conv_out, o=o, final_state=hT, y=y,
-                                  cu_seqlens_host=cu_h, workspace=ws)
+                                  cu_seqlens_host=cu_h, workspace=ws, side_stream=side)
 
         # (2) the same work as two calls, each bracketed, for the per-kernel roofline
         def component_step(evs):
@@ -444,7 +447,7 @@ def run_ours(args, world, rank, local):
                                       conv_state_out=conv_states[i & 1],
                                       initial_state=None if i == 0 else hT, final_state=hT,
                                       y=y[a:b], o=o[a:b], cu_seqlens_host=part_cu[i],
-                                      workspace=ws)
+                                      workspace=ws, side_stream=side)
                 computed = torch.cuda.Event()
                 computed.record(stream)
                 d2h_stream.wait_event(computed)

@@ -4,28 +4,9 @@
 // before launching anything; nothing here allocates device memory.
 #include <string.h>
 
-#include <mutex>
-
 #include "common.cuh"
 
 namespace {
-
-constexpr int kMaxDevices = 64;
-
-// One non-blocking side stream per device, created on first use and kept for the
-// process: the layer entry forks the v channels' conv onto it.
-gdn_status_t side_stream(cudaStream_t *out) {
-    static std::mutex mu;
-    static cudaStream_t streams[kMaxDevices] = {};
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!streams[dev] &&
-        cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess)
-        return GDN_ERR_CUDA;
-    *out = streams[dev];
-    return GDN_OK;
-}
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -304,7 +285,7 @@ gdn_status_t gdn_layer_prefill(const void *x, int64_t T, int32_t Hk, int32_t Hv,
                                const float *g, const float *beta, float scale, uint32_t flags,
                                const float *initial_state, void *o, float *final_state,
                                void *workspace, size_t workspace_bytes, int32_t *status_dev,
-                               void *stream) {
+                               void *side_stream, void *stream) {
     if (Hk <= 0 || Hv <= 0 || dk <= 0 || dv <= 0 || T < 0 || N < 0 || N > 65535)
         return GDN_ERR_SHAPE;
     const int64_t qk = (int64_t)Hk * dk, C64 = 2 * qk + (int64_t)Hv * dv;
@@ -348,11 +329,19 @@ gdn_status_t gdn_layer_prefill(const void *x, int64_t T, int32_t Hk, int32_t Hv,
     if (s != GDN_OK) return s;
     if ((max_len + 15) / 16 > 65535) return GDN_ERR_SHAPE;
 
-    // fork: the v channels' conv on the side stream, the q/k channels' conv and the
-    // chunk preparation (which reads only q and k) on the caller's stream; the state pass
-    // waits for v.  Events live only for this call.
-    cudaStream_t side = nullptr;
-    if ((s = side_stream(&side)) != GDN_OK) return s;
+    if (!side_stream) {
+        // one stream: the conv over every channel, then the chunk scan
+        s = gdn_host::launch_conv1d_fwd(x, C, conv_w, conv_bias, cu_seqlens_dev, N, max_len,
+                                        conv_state_in, conv_state_out, y, st);
+        if (s != GDN_OK) return s;
+        return chunk_prefill_impl(&tq, &tk, &tv, g, beta, cu_seqlens_dev, cu_seqlens_host, N,
+                                  64, scale, flags, initial_state, &to, final_state, workspace,
+                                  workspace_bytes, status_dev, stream, nullptr);
+    }
+    // fork: the v channels' conv on the caller's side stream, the q/k channels' conv and
+    // the chunk preparation (which reads only q and k) on `stream`; the state pass waits
+    // for v.  Events live only for this call.
+    cudaStream_t side = (cudaStream_t)side_stream;
     cudaEvent_t fork = nullptr, v_ready = nullptr;
     if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess) return GDN_ERR_CUDA;
     if (cudaEventCreateWithFlags(&v_ready, cudaEventDisableTiming) != cudaSuccess) {

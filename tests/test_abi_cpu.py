@@ -196,7 +196,7 @@ def test_layer_prefill_rejections(lib):
     def call(x=FAKE, T=8, Hk=2, Hv=6, cu_h=cup, y=FAKE, w=FAKE):
         return lib.gdn_layer_prefill(x, T, Hk, Hv, 128, 128, w, None, FAKE, cu_h, 1, None,
                                      None, y, FAKE, FAKE, 1.0, 0, None, FAKE, None, None, 0,
-                                     None, None)
+                                     None, None, None)
 
     assert call(Hk=0) == 2                 # no heads
     assert call(w=None) == 1               # no conv weights
