@@ -153,6 +153,15 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     return d;
 }
 
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("add.rn.f32x2 %0, %1, %2;"
+        : "=l"(*reinterpret_cast<unsigned long long *>(&d))
+        : "l"(*reinterpret_cast<const unsigned long long *>(&a)),
+          "l"(*reinterpret_cast<const unsigned long long *>(&b)));
+    return d;
+}
+
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
     float2 d;
     asm("mul.rn.f32x2 %0, %1, %2;"
@@ -403,17 +412,17 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     }
     if (tid == 31) S.carry = gs;
     ok = wait_all(&S.bar_tma, 0);
-    if (ok && tid == 0) {
+    if (ok && warp == 0) {
         tc::fence_after_sync();
         constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 0);
         const uint32_t base = tc::smem_u32(S.kq());
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            tc::mma_bf16(tmem, tc::sdesc(base + off, 16, 1024), tc::sdesc(base + off, 16, 1024),
-                         id, ks > 0);
+            tc::mma_bf16_warp(tmem, tc::sdesc(base + off, 16, 1024),
+                              tc::sdesc(base + off, 16, 1024), id, ks > 0);
         }
-        tc::mma_commit(&S.bar_mma);
+        tc::mma_commit_warp(&S.bar_mma);
     }
     const int r = tid & 63;
     if (ok) {
@@ -513,7 +522,7 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
-    if (ok && tid == 0) {
+    if (ok && warp == 0) {
         tc::fence_after_sync();
         // D[128x64] += X[128 x 64] * Lo[64 x 64]  (B = rows 0..63 of X, MN-major).  Rows
         // 64..127 of D held the fp32 M, so they end as Mt; rows 0..63 are not used.
@@ -521,9 +530,9 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
         const uint32_t xb = tc::smem_u32(S.x());
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            tc::mma_bf16(tmem, tc::sdesc(xb + ks * 32, 16, 1024),
-                         tc::sdesc(xb + ks * 2048, 8192, 1024), id, true);
-        tc::mma_commit(&S.bar_mma);
+            tc::mma_bf16_warp(tmem, tc::sdesc(xb + ks * 32, 16, 1024),
+                              tc::sdesc(xb + ks * 2048, 8192, 1024), id, true);
+        tc::mma_commit_warp(&S.bar_mma);
     }
     if (ok) ok = wait_all(&S.bar_mma, 1);
 
@@ -606,15 +615,15 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     uint32_t wq[2][32];                      // this thread's [W ; Q'] row, packed bf16
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-        if (ok && tid == 0) {
+        if (ok && warp == 0) {
             tc::fence_after_sync();
             constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
             const uint32_t yb = tc::smem_u32(S.x()), kb = tc::smem_u32(S.buf + half * 8192);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tmem, tc::sdesc(yb + ks * 32, 16, 1024),
-                             tc::sdesc(kb + ks * 2048, 8192, 1024), id, ks > 0);
-            tc::mma_commit(&S.bar_mma);
+                tc::mma_bf16_warp(tmem, tc::sdesc(yb + ks * 32, 16, 1024),
+                                  tc::sdesc(kb + ks * 2048, 8192, 1024), id, ks > 0);
+            tc::mma_commit_warp(&S.bar_mma);
         }
         if (ok) ok = wait_all(&S.bar_mma, half & 1);
         if (ok) {
@@ -757,8 +766,14 @@ __device__ __forceinline__ void fold_update(float (&h)[NC], float a, uint32_t ta
     float u[NC], w[NC];
     tmem_cols<NC>(taddr, u);
     tmem_cols<NC>(taddr + 2 * NC, w);
+    const float2 a2 = make_float2(a, a);
 #pragma unroll
-    for (int i = 0; i < NC; ++i) h[i] = fmaf(a, h[i], u[i] + w[i]);
+    for (int i = 0; i < NC; i += 2) {
+        const float2 s = add2(make_float2(u[i], u[i + 1]), make_float2(w[i], w[i + 1]));
+        const float2 r = fma2(a2, make_float2(h[i], h[i + 1]), s);
+        h[i] = r.x;
+        h[i + 1] = r.y;
+    }
 }
 
 // Named barrier between the four warps that own TMEM lanes 0..63 (warps 0, 1, 4, 5: the
@@ -808,8 +823,10 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
 
     if (warp == kIssuerWarp) {
         // ------------------------------------------------------------ issuer warp
-        // Shared-memory descriptors, built once; a byte offset o is added as o >> 4.
-        // Stage b of a double buffer sits b * (buffer bytes) after stage 0.
+        // Lane 0 does the bounded waits; the whole warp then issues each MMA group in
+        // converged code (one elected lane issues), which keeps the descriptors in uniform
+        // registers.  Shared-memory descriptors are built once; a byte offset o is added as
+        // o >> 4.  Stage b of a double buffer sits b * (buffer bytes) after stage 0.
         const uint64_t dWQ0 = tc::sdesc(tc::smem_u32(S.ws[0]), 16, 1024);          // K-major
         const uint64_t dZ0 = tc::sdesc(tc::smem_u32(S.ws[0] + kZOff), 16, 1024);   // K-major
         const uint64_t dKt0 = tc::sdesc(tc::smem_u32(S.k[0]), 8192, 1024);         // K^T, MN-major
@@ -819,57 +836,62 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
         constexpr uint32_t id1 = tc::idesc_bf16(128, NT, 0, 1);
         constexpr uint32_t id3 = tc::idesc_bf16(128, 2 * NT, 1, 1);
         const bool leader = lane == 0;
-        bool ok = true;
-        for (int c = 0; c < nch; ++c) {
+        bool ok = true;   // meaningful in lane 0
+        // lane 0's verdict, broadcast: go on issuing unless a wait ran out
+        auto go = [&]() { return __shfl_sync(0xffffffffu, (ok && !*abort) ? 1 : 0, 0) != 0; };
+        // D = Z V of chunk c into its stage's accumulator, once the chunk's tiles landed.
+        // It needs nothing of the chain: chunk c's is issued right after chunk c-1's state
+        // update, so it runs while the compute warps fold that update.
+        auto issue_zv = [&](int c) {
             const int st = c & 1;
-            const uint32_t colD = 64 * st;
             if (leader) {
                 if (ok) ok = wait_one(&S.bar_ws[st], (c >> 1) & 1, abort);
                 if (ok) ok = wait_one(&S.bar_kv[st], (c >> 1) & 1, abort);
-                if (ok && !*abort) {
-                    // D = Z V: needs nothing of the chain, so it runs while the compute
-                    // warps fold the previous update.  D's buffer was last read in chunk
-                    // c-2, whose readers all passed the previous chunk's barrier.
-                    tc::fence_after_sync();
+            }
+            if (go()) {
+                tc::fence_after_sync();
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        tc::mma_bf16(tmem + colD, dZ0 + ((st * kWsStage + ks * 32) >> 4),
-                                     dV0 + ((st * 8192 + ks * 2048) >> 4), id1, ks > 0);
-                }
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16_warp(tmem + 64 * st, dZ0 + ((st * kWsStage + ks * 32) >> 4),
+                                      dV0 + ((st * 8192 + ks * 2048) >> 4), id1, ks > 0);
             }
             __syncwarp();
+        };
+        if (nch > 0) issue_zv(0);
+        for (int c = 0; c < nch; ++c) {
+            const int st = c & 1;
+            const uint32_t colD = 64 * st;
             __syncthreads();                                   // h published as bf16
-            if (leader) {
-                if (ok && !*abort) {
-                    tc::fence_after_sync();
-                    // D += [W ; Q'] h
+            if (go()) {
+                tc::fence_after_sync();
+                // D += [W ; Q'] h
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        tc::mma_bf16(tmem + colD,
-                                     dWQ0 + ((st * kWsStage + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                                     dH + ((ks * 2048) >> 4), id1, 1);
-                    tc::mma_commit(&S.bar_d1);
-                }
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_bf16_warp(tmem + colD,
+                                      dWQ0 + ((st * kWsStage + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                                      dH + ((ks * 2048) >> 4), id1, 1);
+                tc::mma_commit_warp(&S.bar_d1);
             }
             __syncwarp();
             chain_barrier();                                   // hi | lo of d Vn ready
-            if (leader && ok && !*abort) {
+            if (go()) {
                 // K^T [hi | lo]: both halves of the update in one pass, summed in fp32 later
                 tc::fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(tmem + colS, dKt0 + ((st * 16384 + ks * 2048) >> 4),
-                                 dVhl + ((ks * 2048) >> 4), id3, ks > 0);
-                tc::mma_commit(&S.bar_d3);
+                    tc::mma_bf16_warp(tmem + colS, dKt0 + ((st * 16384 + ks * 2048) >> 4),
+                                      dVhl + ((ks * 2048) >> 4), id3, ks > 0);
+                tc::mma_commit_warp(&S.bar_d3);
             }
             __syncwarp();
+            // The next chunk's accumulator (stage st^1) was last read in chunk c-1, whose
+            // readers all passed this chunk's first barrier.
+            if (c + 1 < nch) issue_zv(c + 1);
         }
-        if (leader) {
-            // Nothing this warp started may still run when the CTA exits: wait (bounded) for
-            // every MMA it issued.
-            tc::mma_commit(&S.bar_fin);
-            wait_bounded(&S.bar_fin, 0);
-        }
+        // Nothing this warp started may still run when the CTA exits: wait (bounded) for
+        // every MMA it issued.
+        tc::mma_commit_warp(&S.bar_fin);
+        if (leader) wait_bounded(&S.bar_fin, 0);
         __syncwarp();
         tc::fence_before_sync();
         __syncthreads();
@@ -955,7 +977,10 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
         const int L = min(kC, len - c * kC);
         const uint32_t colD = 64 * st;
 
-        // --- A: fold the previous chunk's update into h, publish the bf16 copy
+        // --- A: fold the previous chunk's update into h, publish the bf16 copy.  This
+        // chunk's tiles were requested a chunk ago: waiting for them here overlaps the
+        // barrier query with the previous update's MMAs instead of following the barrier.
+        if (ok) ok = wait_one(&S.bar_kv[st], (c >> 1) & 1, abort);
         if (c > 0 && ok) {
             ok = wait_one(&S.bar_d3, ph ^ 1, abort);
             if (ok) {
@@ -967,7 +992,6 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
-        if (ok) ok = wait_one(&S.bar_kv[st], (c >> 1) & 1, abort);
         const float *sc = reinterpret_cast<const float *>(S.ws[st] + kScalOff);
         const float aL = sc[128];
 
@@ -983,28 +1007,46 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
         }
         if (chain) {
             // Vn = beta V - D on the chain rows, then d Vn as bf16 hi + lo
+            // x = d (beta V - D), formed as (-d) (D - beta V) two columns at a time: the
+            // same roundings as d * fma(beta, v, -D) (negation is exact)
             const bool live = r < L;
-            const float br = sc[r];
-            const float dc = live ? sc[64 + r] : 0.f;
+            const float2 nb = make_float2(-sc[r], -sc[r]);
+            const float2 nd = make_float2(-sc[64 + r], -sc[64 + r]);
             float x[NC];
+            if (live) {
 #pragma unroll
-            for (int cc = 0; cc < NCH; ++cc) {
-                float vv[8];
-                unpack8(*reinterpret_cast<const uint4 *>(S.v[st] + tc::swz(r, c0 + cc)), vv);
+                for (int cc = 0; cc < NCH; ++cc) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(S.v[st] + tc::swz(r, c0 + cc));
+                    const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    x[8 * cc + e] = live ? dc * fmaf(br, vv[e], -d1[8 * cc + e]) : 0.f;
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = 8 * cc + 2 * e;
+                        const float2 v2 = make_float2(__uint_as_float(uw[e] << 16),
+                                                      __uint_as_float(uw[e] & 0xffff0000u));
+                        const float2 t = fma2(nb, v2, make_float2(d1[i], d1[i + 1]));
+                        const float2 xx = mul2(nd, t);
+                        x[i] = xx.x;
+                        x[i + 1] = xx.y;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < NC; ++i) x[i] = 0.f;
             }
             // hi = bf16(x) two at a time (the paired conversion issues at several times
             // the rate of the single one); lo = x - hi is exact in fp32
             uint32_t hp[NC / 2];
             float lo[NC];
+            const float2 m1 = make_float2(-1.f, -1.f);
 #pragma unroll
             for (int jj = 0; jj < NC / 2; ++jj) {
                 const __nv_bfloat162 hb2 = __floats2bfloat162_rn(x[2 * jj], x[2 * jj + 1]);
                 hp[jj] = *reinterpret_cast<const uint32_t *>(&hb2);
-                lo[2 * jj] = x[2 * jj] - __uint_as_float(hp[jj] << 16);
-                lo[2 * jj + 1] = x[2 * jj + 1] - __uint_as_float(hp[jj] & 0xffff0000u);
+                const float2 l2 = fma2(m1, make_float2(__uint_as_float(hp[jj] << 16),
+                                                       __uint_as_float(hp[jj] & 0xffff0000u)),
+                                       make_float2(x[2 * jj], x[2 * jj + 1]));
+                lo[2 * jj] = l2.x;
+                lo[2 * jj + 1] = l2.y;
             }
 #pragma unroll
             for (int cc = 0; cc < NCH; ++cc) {
