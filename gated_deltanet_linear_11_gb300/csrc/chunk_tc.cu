@@ -5,39 +5,36 @@
 // start ("[Feature] Add batch invariance support to GDN_ATTN backend - #45819", Birol's
 // comment, part 3(a), and the PR's "Fixes: 2."), so nothing depends on the packed batch.
 //
-// With gamma the in-chunk inclusive log-decay sums, nk, nq the L2-norm factors (1 when
-// the flag is off) and h the [dk][dv] state entering a chunk, the chunk's WY/UT form is
-//     A[r][s] = beta_r e^{gamma_r-gamma_s} nk_r nk_s (k_r.k_s)        s < r
-//     M[r][s] = e^{gamma_r-gamma_s} nq_r nk_s (q_r.k_s)                s <= r
-//     Tinv = (I + A)^{-1} = I + Lo,   a_s = beta_s e^{gamma_s} nk_s
-//     W  = Tinv diag(a) K,            U = Tinv diag(beta) V
-//     Vn = U - W h,                   O = scale (diag(e^gamma nq) Q h + M Vn)
-//     h <- e^{gamma_L} h + K^T diag(e^{gamma_L-gamma} nk) Vn
-// Everything that does not involve h is folded, per (chunk, v-head), into three operand
-// tiles so that the state pass has one product before Vn and one after it:
-//     WQ = [W ; Q'],  Q' = diag(e^gamma nq) Q - M W          (the rows that multiply h)
-//     Z  = [-Lo diag(beta) ; Mt diag(beta)],  Mt = M Tinv     (the rows that multiply V)
-// so that  [Z V + WQ h]  holds  beta V - Vn  in its first 64 rows and  O / scale  in the
-// other 64  (Vn = beta V + Lo diag(beta) V - W h;  M Vn = Mt diag(beta) V - M W h).
-//
 // Two kernels, both tcgen05 (MMA into TMEM, operands in 128B-swizzled shared memory fed
-// by TMA and bulk copies):
+// by TMA):
 //
 //  chunk_prep (one CTA per (chunk, v-head), fully parallel):
-//      P = [K;Q] K^T  ->  A, M (fp32)  ->  Tinv (blocked forward substitution, CUDA
-//      cores)  ->  Mt = M + M Lo  ->  [Lo a ; Mt a] K  ->  WQ, Z, and the per-token
-//      scalars beta, d = e^{gamma_L-gamma} nk and e^{gamma_L}, stored as one workspace
-//      tile.
+//      P = [K;Q] K^T                                   (tcgen05, M=128 N=64 K=128)
+//    with gamma the in-chunk inclusive log-decay sums and nk, nq the L2-norm factors
+//    (1 when the flag is off):
+//      A[r][s]  = beta_r e^{gamma_r-gamma_s} nk_r nk_s (k_r.k_s)          s < r
+//      M[r][s]  = e^{gamma_r-gamma_s} nq_r nk_s (q_r.k_s)                  s <= r
+//      Tinv     = (I + A)^{-1}   (fp32, blocked forward substitution on CUDA cores)
+//      Lo       = Tinv - I,  Mt = M Tinv = M + M Lo   (tcgen05: M Lo accumulates onto
+//                                                      the fp32 M held in TMEM)
+//    and stores one workspace tile: the 128x64 bf16 X = [Lo ; Mt] (already swizzled)
+//    followed by the chunk's fp32 gamma, beta, nk and nq.
 //
 //  chunk_state (one CTA per (sequence, v-head, dv tile), walks the chunks):
-//      D  = Z V  (issued ahead, off the chain)  +  WQ h_bf16
-//      Vn = beta V - D[0:64];   O = scale D[64:128]
-//      h <- e^{gamma_L} h + K^T [hi | lo](d Vn)
-//    The state update takes d Vn as a bf16 hi + lo pair (one MMA pass over [hi | lo], the
-//    halves summed in fp32) and beta V enters Vn exactly in fp32, so the state keeps
-//    fp32-level accuracy.  Eight compute warps: warps w and w+4 share TMEM lanes 32(w%4)..
-//    and take half the tile's columns each; a ninth warp issues the MMAs and a tenth the
-//    TMA and bulk loads.
+//      D1 = [K;Q] h                      (h: fp32 state in registers, bf16 copy as operand)
+//      R  = diag(beta) (V - diag(e^gamma nk) K h)              (fp32, CUDA cores)
+//      D2 = X R  = [Lo R ; Mt R]
+//      Vn = R + Lo R                     (identity part of Tinv applied exactly in fp32)
+//      O  = scale (diag(e^gamma nq) Q h + Mt R)
+//      h <- e^{gamma_L} h + K^T diag(e^{gamma_L-gamma} nk) Vn
+//    The last product takes diag(.)Vn as a bf16 hi + lo pair (one MMA pass over [hi | lo],
+//    the halves summed in fp32) so the state keeps fp32-level accuracy; q/k L2 norms and
+//    decays are per-token fp32 scalars applied outside the MMAs, so the raw bf16 inputs
+//    are the only operands that are not split.
+//    One CTA per (sequence, v-head, dv tile of 64, 48 or 32 columns).  Eight compute
+//    warps: warps w and w+4 share TMEM lanes 32(w%4).. and take half the tile's columns
+//    each; a ninth warp issues the MMAs (as a converged warp, one elected lane issuing) and
+//    a tenth the TMA and bulk loads.
 //
 // Every wait on an mbarrier is bounded in time; on expiry the CTA records GDN_ERR_TIMEOUT
 // in the status word, stops issuing work, frees its TMEM and returns.
@@ -56,13 +53,8 @@ constexpr int kPrepThreads = 128;
 constexpr int kC = 64;          // chunk
 constexpr int kD = 128;         // dk = dv
 constexpr uint32_t kXTile = 16384;            // bf16 [128 rows][64] swizzled
-// Workspace tile per (chunk slot, v-head)
-constexpr uint32_t kWQBytes = 32768;          // [W ; Q'] bf16: two 64-column K blocks
-constexpr uint32_t kZOff = kWQBytes;          // Z = [-Lo diag(beta) ; Mt diag(beta)] bf16
-constexpr uint32_t kScalOff = kZOff + kXTile; // beta[64], d[64], e^{gamma_L} (fp32)
-constexpr uint32_t kScalBytes = 528;
-constexpr uint32_t kWsTile = kScalOff + kScalBytes;
-static_assert(kWsTile % 16 == 0, "bulk copies move multiples of 16 bytes");
+constexpr uint32_t kScal = 4 * kC * 4;        // gamma, beta, nk, nq (fp32 x 64 each)
+constexpr uint32_t kWsTile = kXTile + kScal;  // one workspace tile per (slot, v-head)
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s bound on any single wait
 
 struct TcMaps {
@@ -77,8 +69,6 @@ struct TcParams {
     float *hT;
     bf16 *o;
     int64_t o_tok;
-    const bf16 *q;           // q rows, read back by the prep kernel for Q'
-    int64_t q_tok;
     uint8_t *ws;
     int N, Hk, Hv;
     float scale;
@@ -93,18 +83,13 @@ __device__ __forceinline__ uint64_t now_ns() {
     return t;
 }
 
-// Bounded wait on an mbarrier phase by thread 0, then a CTA-wide agreement.  The barrier
-// orders everything the phase made visible to thread 0 before the other threads' reads,
-// and only one thread polls the mbarrier's shared-memory word.
+// Bounded wait on an mbarrier phase by every thread, then a CTA-wide agreement.
 __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
-    bool ok = true;
-    if (threadIdx.x == 0) {
-        ok = tc::mbar_try_wait(bar, parity);
-        if (!ok) {
-            const uint64_t t0 = now_ns();
-            while (!(ok = tc::mbar_try_wait(bar, parity)))
-                if (now_ns() - t0 > kWaitNs) break;
-        }
+    bool ok = tc::mbar_try_wait(bar, parity);
+    if (!ok) {
+        const uint64_t t0 = now_ns();
+        while (!(ok = tc::mbar_try_wait(bar, parity)))
+            if (now_ns() - t0 > kWaitNs) break;
     }
     return __syncthreads_and(ok ? 1 : 0) != 0;
 }
@@ -142,7 +127,9 @@ __device__ __forceinline__ void tmem_row32(uint32_t taddr, float (&v)[32]) {
     tc::tmem_wait_ld();
 }
 
-// Packed fp32 pair arithmetic (two lanes per instruction).
+// Sum of squares of one 128-element bf16 row held in a K-major tile of two 64-wide
+// blocks (block stride `blk` bytes), fixed order.
+// Packed fp32 pair arithmetic (two lanes per instruction), rounded like the scalar ops.
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     float2 d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;"
@@ -152,7 +139,6 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
           "l"(*reinterpret_cast<const unsigned long long *>(&c)));
     return d;
 }
-
 __device__ __forceinline__ float2 add2(float2 a, float2 b) {
     float2 d;
     asm("add.rn.f32x2 %0, %1, %2;"
@@ -161,7 +147,6 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
           "l"(*reinterpret_cast<const unsigned long long *>(&b)));
     return d;
 }
-
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
     float2 d;
     asm("mul.rn.f32x2 %0, %1, %2;"
@@ -171,32 +156,19 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
     return d;
 }
 
-// Sum of squares of one 128-element bf16 row held in a K-major tile of two 64-wide
-// blocks (block stride `blk` bytes): four packed accumulators over fixed element
-// positions, summed in a fixed order.
-__device__ __forceinline__ float row_sumsq(const uint8_t *tile, int row, uint32_t blk,
-                                           uint32_t park) {
-    float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+__device__ __forceinline__ float row_sumsq(const uint8_t *tile, int row, uint32_t blk) {
+    float acc = 0.f;
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
-        float raw[32];   // the 64 bf16 values of this block, as 32 packed words
-#pragma unroll
+#pragma unroll 2
         for (int c = 0; c < 8; ++c) {
-            const uint4 u = *reinterpret_cast<const uint4 *>(tile + kb * blk + tc::swz(row, c));
-            raw[4 * c] = __uint_as_float(u.x); raw[4 * c + 1] = __uint_as_float(u.y);
-            raw[4 * c + 2] = __uint_as_float(u.z); raw[4 * c + 3] = __uint_as_float(u.w);
             float f[8];
-            unpack8(u, f);
+            unpack8(*reinterpret_cast<const uint4 *>(tile + kb * blk + tc::swz(row, c)), f);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 x = make_float2(f[2 * e], f[2 * e + 1]);
-                acc[e] = fma2(x, x, acc[e]);
-            }
+            for (int e = 0; e < 8; ++e) acc = fmaf(f[e], f[e], acc);
         }
-        tc::tmem_st32(park + 32 * kb, raw);
     }
-    return ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
-           ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+    return acc;
 }
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -313,26 +285,17 @@ __device__ void tinv64_inplace(float (*AT)[kLd], float (*Y)[kLdY]) {
 
 // ================================================================ chunk_prep kernel
 
-// One 33 KB region, reused by lifetime:
-//   [0, 32K)    the [K;Q] K-major tile, until P = [K;Q]K^T and the norms are taken;
-//               then the fp32 A, inverted in place into T = (I + A)^{-1}, at byte 0 and
-//               the inverse's scratch at kXOff; once T is dead, the Z tile (staged for
-//               its bulk copy) and then the chunk's K tile again (two 64-column blocks at
-//               0 and 8K), the B operand of Y K.
-//   [17K, 33K)  X = [Lo ; M] (bf16, the A operand of M Lo), then Y = [Lo a ; Mt a].
-// Finally the [W ; Q'] tile is staged over [0, 32K) for one bulk copy.
-// TMEM (128 columns): columns 0..63 hold P, then M and Mt, then each 64-column half of
-// [Lo a ; Mt a] K in turn; columns 64..127 hold, from the start, this thread's own row of
-// the chunk's K (lanes 0..63) or Q (lanes 64..127) as packed bf16, for the epilogue.
+// One region, reused by lifetime.  The [K;Q] K-major tile fills bytes 0..32767 until
+// P = [K;Q]K^T and the norms are taken.  Then the fp32 A, inverted in place into
+// T = (I + A)^{-1}, sits at byte 0, and the inverse's scratch Y at kXOff; once the
+// inverse is done, the bf16 tile X = [Lo ; M] (then [Lo ; Mt]) replaces Y at kXOff.
 constexpr uint32_t kXOff = 17 * 1024;   // 1024-aligned, past A
-constexpr uint32_t kPrepRegion = kXOff + kXTile;
 static_assert(64 * kLd * 4 <= kXOff && 64 * kLdY * 4 <= kXTile, "prep region layout");
 
 struct PrepSmem {
-    uint8_t buf[kPrepRegion];
+    uint8_t buf[kXOff + kXTile];
     float gam[64], bet[64], nk[64], nq[64];
     float c2[64];            // gamma_s log2(e) - log2(nk_s): the key-side exponent
-    float a[64];             // beta_s e^{gamma_s} nk_s
     float carry;
     uint64_t bar_tma, bar_mma;
     uint32_t tmem;
@@ -342,10 +305,11 @@ struct PrepSmem {
     __device__ float (*Y())[kLdY] { return reinterpret_cast<float (*)[kLdY]>(buf + kXOff); }
     __device__ uint8_t *x() { return buf + kXOff; }
 };
-static_assert(sizeof(PrepSmem) + 1024 <= 56 * 1024, "four prep CTAs fit on one SM");
+static_assert(sizeof(PrepSmem) + 1024 <= 44 * 1024, "five prep CTAs fit on one SM");
 
-// One CTA per (chunk slot, v-head); four CTAs per SM.
-__global__ void __launch_bounds__(kPrepThreads, 4)
+// One CTA per (chunk slot, v-head); five CTAs per SM.  TMEM (64 columns): P = [K;Q]K^T,
+// whose M rows are then replaced by the fp32 M itself, onto which M Lo accumulates.
+__global__ void __launch_bounds__(kPrepThreads, 5)
 chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     PrepSmem &S = *reinterpret_cast<PrepSmem *>(
@@ -353,9 +317,7 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     grid_dependents_launch();
     grid_dependency_wait();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // Launched chunk-major in reverse: the first chunks of every head are prepared last,
-    // so their tiles are the ones still in L2 when the state pass starts reading.
-    const int hv = blockIdx.x, slot = gridDim.y - 1 - blockIdx.y;
+    const int slot = blockIdx.x, hv = blockIdx.y;
     const int hk = hv / (p.Hv / p.Hk);
 
     // slot -> (sequence n, chunk c): the last n with slot0(n) <= slot.
@@ -379,7 +341,7 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     }
 
     if (warp == 0) {
-        tc::tmem_alloc(&S.tmem, 128);
+        tc::tmem_alloc(&S.tmem, 64);
         tc::tmem_relinquish();
     }
     if (tid == 0) {
@@ -394,6 +356,7 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     tc::fence_after_sync();
     const uint32_t tmem = S.tmem;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t colP = 0;
     bool ok = true;
 
     if (tid == 0) {
@@ -419,7 +382,7 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            tc::mma_bf16_warp(tmem, tc::sdesc(base + off, 16, 1024),
+            tc::mma_bf16_warp(tmem + colP, tc::sdesc(base + off, 16, 1024),
                               tc::sdesc(base + off, 16, 1024), id, ks > 0);
         }
         tc::mma_commit_warp(&S.bar_mma);
@@ -427,8 +390,7 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
     const int r = tid & 63;
     if (ok) {
         // L2-norm factors of this chunk's k rows (threads 0..63) and q rows (64..127)
-        const float ss = row_sumsq(S.kq(), tid, 16384, tmem + lane_off + 64);
-        tc::tmem_wait_st();
+        const float ss = row_sumsq(S.kq(), tid, 16384);
         const float f = p.l2norm ? rsqrtf(ss + 1e-6f) : 1.f;
         if (tid < 64) {
             const float nkr = r < L ? f : 0.f;
@@ -436,7 +398,6 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
             S.nk[r] = nkr;
             S.gam[r] = gamr;
             S.bet[r] = bx;
-            S.a[r] = bx * __expf(gamr) * nkr;
             // e^{gamma_r - gamma_s} nk_s = 2^(gamma_r log2 e - c2_s); nk_s = 0 gives +inf here
             // and an exact 0 below
             S.c2[r] = nkr > 0.f ? gamr * kLog2e - __log2f(nkr) : __int_as_float(0x7f800000);
@@ -466,20 +427,11 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
                 for (int i = 0; i < 32; ++i) v[i] = 0.f;
             } else {
                 float pv[32];
-                tmem_row32(tmem + lane_off + 32 * hf, pv);
+                tmem_row32(tmem + lane_off + colP + 32 * hf, pv);
 #pragma unroll
-                for (int i = 0; i < 32; i += 4) {
+                for (int i = 0; i < 32; ++i) {
                     const int s = 32 * hf + i;
-                    const float4 c4 = *reinterpret_cast<const float4 *>(&S.c2[s]);
-                    const float2 e0 = make_float2(fast_exp2(g2r - c4.x), fast_exp2(g2r - c4.y));
-                    const float2 e1 = make_float2(fast_exp2(g2r - c4.z), fast_exp2(g2r - c4.w));
-                    const float2 rf = make_float2(rowf, rowf);
-                    const float2 w0 = mul2(mul2(rf, make_float2(pv[i], pv[i + 1])), e0);
-                    const float2 w1 = mul2(mul2(rf, make_float2(pv[i + 2], pv[i + 3])), e1);
-                    v[i] = (s < lim && r < L) ? w0.x : 0.f;
-                    v[i + 1] = (s + 1 < lim && r < L) ? w0.y : 0.f;
-                    v[i + 2] = (s + 2 < lim && r < L) ? w1.x : 0.f;
-                    v[i + 3] = (s + 3 < lim && r < L) ? w1.y : 0.f;
+                    v[i] = (s < lim && r < L) ? rowf * pv[i] * fast_exp2(g2r - S.c2[s]) : 0.f;
                 }
             }
             if (arow) {
@@ -489,10 +441,19 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
             } else {
                 // fp32 M over the P half just read: M Lo accumulates onto it, giving
                 // Mt = M + M Lo (rows with no entries in this half store zeros)
-                tc::tmem_st32(tmem + lane_off + 32 * hf, v);
+                tc::tmem_st32(tmem + lane_off + colP + 32 * hf, v);
             }
         }
         if (!arow) tc::tmem_wait_st();
+        // per-token scalars for the state kernel
+        float *ws_s = reinterpret_cast<float *>(wtile + kXTile);
+        if (tid < 64) {
+            ws_s[r] = S.gam[r];
+            ws_s[64 + r] = S.bet[r];
+            ws_s[128 + r] = S.nk[r];
+        } else {
+            ws_s[192 + r] = S.nq[r];
+        }
     }
     __syncthreads();
     if (ok) tinv64_inplace(AT, S.Y());   // ends with a barrier
@@ -503,11 +464,7 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
         for (int hf = 0; hf < 2; ++hf) {
             float lrow[32];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const float2 t2 = *reinterpret_cast<const float2 *>(&AT[r][32 * hf + i]);
-                lrow[i] = (32 * hf + i < r) ? t2.x : 0.f;
-                lrow[i + 1] = (32 * hf + i + 1 < r) ? t2.y : 0.f;
-            }
+            for (int i = 0; i < 32; ++i) lrow[i] = (32 * hf + i < r) ? AT[r][32 * hf + i] : 0.f;
             pack_row<32>(S.x(), tid, 4 * hf, lrow);
         }
     } else if (ok) {
@@ -515,7 +472,7 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
             float m[32];
-            tmem_row32(tmem + lane_off + 32 * hf, m);
+            tmem_row32(tmem + lane_off + colP + 32 * hf, m);
             pack_row<32>(S.x(), tid, 4 * hf, m);
         }
     }
@@ -530,163 +487,49 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
         const uint32_t xb = tc::smem_u32(S.x());
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            tc::mma_bf16_warp(tmem, tc::sdesc(xb + ks * 32, 16, 1024),
+            tc::mma_bf16_warp(tmem + colP, tc::sdesc(xb + ks * 32, 16, 1024),
                               tc::sdesc(xb + ks * 2048, 8192, 1024), id, true);
         tc::mma_commit_warp(&S.bar_mma);
     }
     if (ok) ok = wait_all(&S.bar_mma, 1);
-
-    // Y = [Lo diag(a) ; Mt diag(a)] over X (which the MMA has read), and the rows of
-    // Z = [-Lo diag(beta) ; Mt diag(beta)], kept in registers until A is dead.
-    uint32_t zrow[32];
-    if (ok) {
+    if (ok && tid >= 64) {
         tc::fence_after_sync();
-        const float zs = tid < 64 ? -1.f : 1.f;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-            float src[32];
-            if (tid < 64) {
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const float2 t2 = *reinterpret_cast<const float2 *>(&AT[r][32 * hf + i]);
-                    src[i] = (32 * hf + i < r) ? t2.x : 0.f;
-                    src[i + 1] = (32 * hf + i + 1 < r) ? t2.y : 0.f;
-                }
-            } else {
-                tmem_row32(tmem + lane_off + 32 * hf, src);
-            }
-            float y[32];
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(&S.a[32 * hf + i]);
-                const float4 b4 = *reinterpret_cast<const float4 *>(&S.bet[32 * hf + i]);
-                const float2 s0 = make_float2(src[i], src[i + 1]);
-                const float2 s1 = make_float2(src[i + 2], src[i + 3]);
-                const float2 y0 = mul2(s0, make_float2(a4.x, a4.y));
-                const float2 y1 = mul2(s1, make_float2(a4.z, a4.w));
-                const float2 z0 = mul2(mul2(s0, make_float2(zs, zs)), make_float2(b4.x, b4.y));
-                const float2 z1 = mul2(mul2(s1, make_float2(zs, zs)), make_float2(b4.z, b4.w));
-                y[i] = y0.x; y[i + 1] = y0.y; y[i + 2] = y1.x; y[i + 3] = y1.y;
-                const __nv_bfloat162 p0 = __floats2bfloat162_rn(z0.x, z0.y);
-                const __nv_bfloat162 p1 = __floats2bfloat162_rn(z1.x, z1.y);
-                zrow[16 * hf + i / 2] = *reinterpret_cast<const uint32_t *>(&p0);
-                zrow[16 * hf + i / 2 + 1] = *reinterpret_cast<const uint32_t *>(&p1);
-            }
-            pack_row<32>(S.x(), tid, 4 * hf, y);
+            float mt[32];
+            tmem_row32(tmem + lane_off + colP + 32 * hf, mt);
+            pack_row<32>(S.x(), tid, 4 * hf, mt);             // over M, which the MMA has read
         }
     }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();                         // A is dead, Y is complete, Mt has been read
-    // Z leaves through shared memory (over A) and one bulk copy; then the chunk's K tile
-    // comes back into the same bytes (an L2 hit), the B operand of Y K.
-    if (ok) {
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-            *reinterpret_cast<uint4 *>(S.buf + tc::swz(tid, cc)) =
-                make_uint4(zrow[4 * cc], zrow[4 * cc + 1], zrow[4 * cc + 2], zrow[4 * cc + 3]);
-    }
+    // The finished [Lo ; Mt] tile leaves in one bulk copy: 128 threads writing their own
+    // 128-byte rows would cost a load/store wavefront per row per instruction.
     tc::fence_async_smem();
     __syncthreads();
     if (ok && tid == 0) {
-        tc::bulk_store(wtile + kZOff, S.buf, kXTile);
+        tc::bulk_store(wtile, S.x(), kXTile);
         tc::bulk_commit();
-        tc::bulk_wait_read<0>();
-        tc::mbar_expect_tx(&S.bar_tma, 16384);
-        tc::tma_load_3d(S.buf + 0, &maps.k, &S.bar_tma, 0, hk, t0);
-        tc::tma_load_3d(S.buf + 8192, &maps.k, &S.bar_tma, 64, hk, t0);
+        tc::bulk_wait_all();
     }
-    if (ok) {
-        float *ws_s = reinterpret_cast<float *>(wtile + kScalOff);
-        const float gL = S.gam[L - 1];
-        if (tid < 64) {
-            ws_s[r] = S.bet[r];
-            ws_s[64 + r] = r < L ? __expf(gL - S.gam[r]) * S.nk[r] : 0.f;
-        } else if (tid == 64) {
-            ws_s[128] = __expf(gL);
-        }
-    }
-    if (ok) ok = wait_all(&S.bar_tma, 1);
-    // W = diag(a) K + (Lo a) K and Q' = diag(e^gamma nq) Q - (Mt a) K in two 64-column
-    // halves of the dk columns: D[128 x 64] = Y[128 x 64 tokens] * K[64 tokens x 64]
-    // (B = one 64-column block of the K tile, MN-major), then this thread's row of the
-    // half, from registers to the workspace tile.
-    const float rs = tid < 64 ? S.a[r] : __expf(S.gam[r]) * S.nq[r];
-    uint32_t wq[2][32];                      // this thread's [W ; Q'] row, packed bf16
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        if (ok && warp == 0) {
-            tc::fence_after_sync();
-            constexpr uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
-            const uint32_t yb = tc::smem_u32(S.x()), kb = tc::smem_u32(S.buf + half * 8192);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16_warp(tmem, tc::sdesc(yb + ks * 32, 16, 1024),
-                                  tc::sdesc(kb + ks * 2048, 8192, 1024), id, ks > 0);
-            tc::mma_commit_warp(&S.bar_mma);
-        }
-        if (ok) ok = wait_all(&S.bar_mma, half & 1);
-        if (ok) {
-            tc::fence_after_sync();
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                float dv[32], raw[16];
-                tc::tmem_ld32(tmem + lane_off + 32 * j, *reinterpret_cast<float (*)[32]>(dv));
-                tc::tmem_ld16(tmem + lane_off + 64 + 32 * half + 16 * j, raw);
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int w = 0; w < 16; ++w) {
-                    const float2 f = __bfloat1622float2(
-                        *reinterpret_cast<const __nv_bfloat162 *>(&raw[w]));
-                    const float2 d2 = make_float2(dv[2 * w], dv[2 * w + 1]);
-                    const float2 x = fma2(make_float2(rs, rs), f,
-                                          tid < 64 ? d2 : make_float2(-d2.x, -d2.y));
-                    const __nv_bfloat162 p2 = __floats2bfloat162_rn(x.x, x.y);
-                    wq[half][16 * j + w] = *reinterpret_cast<const uint32_t *>(&p2);
-                }
-            }
-        }
-        tc::fence_before_sync();
-        __syncthreads();                     // this half's columns are read: TMEM free again
-    }
-    // Y and the K tile are dead: stage [W ; Q'] over them and send it in one bulk copy
-    if (ok) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half)
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc)
-                *reinterpret_cast<uint4 *>(S.buf + half * 16384 + tc::swz(tid, cc)) =
-                    make_uint4(wq[half][4 * cc], wq[half][4 * cc + 1], wq[half][4 * cc + 2],
-                               wq[half][4 * cc + 3]);
-    }
-    tc::fence_async_smem();
-    __syncthreads();
-    if (ok && tid == 0) {
-        tc::bulk_store(wtile, S.buf, kWQBytes);
-        tc::bulk_commit();
-    }
-    if (tid == 0) tc::bulk_wait_all();      // the Z and [W ; Q'] copies have completed
     if (!ok && tid == 0) report(p.status, GDN_ERR_TIMEOUT);
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, 128);
+    if (warp == 0) tc::tmem_dealloc(tmem, 64);
 }
 
 // =============================================================== chunk_state kernel
 
-constexpr uint32_t kWsStage = (kWsTile + 1023) & ~1023u;  // workspace tile, 1024-aligned
+constexpr uint32_t kXStage = 18432;  // workspace tile rounded up to 1024 bytes
 
 struct StateSmem {
-    uint8_t ws[2][kWsStage]; // [W ; Q'], Z and the scalars, per stage
-    uint8_t k[2][16384];     // K tile [64 tokens][128 dk] as two 64-column blocks
+    uint8_t kq[2][32768];    // [K;Q] per stage
+    uint8_t x[2][kXStage];   // [Lo ; Mt] + scalars per stage
     uint8_t v[2][8192];      // V tile [64 tokens][64 dv] per stage
     uint8_t hb[16384];       // bf16 h  [128 dk rows][64 dv]  (MN-major B)
-    uint8_t dvh[8192];       // bf16 hi of diag(d) Vn
+    uint8_t rb[8192];        // bf16 R  [64 tokens][64 dv]    (MN-major B)
+    uint8_t dvh[8192];       // bf16 hi of diag(dcy) Vn
     uint8_t dvl[8192];       // bf16 lo
     uint8_t ob[2][8192];     // bf16 O tile [64 tokens][64 dv] per stage, stored by TMA
-    uint64_t bar_ws[2];      // [W ; Q'] and Z of a stage have landed
-    uint64_t bar_kv[2];      // K, V and the scalars of a stage have landed
-    uint64_t bar_d1, bar_d3, bar_fin;
+    uint64_t bar_tma[2], bar_d1, bar_d2, bar_d3, bar_fin;
     uint32_t tmem;
     int abort;               // set by the first thread whose wait runs out
 };
@@ -717,31 +560,21 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity) {
     return true;
 }
 
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 :: "r"(tc::smem_u32(dst)), "l"(src), "r"(bytes), "r"(tc::smem_u32(bar)) : "memory");
-}
-
-// A stage's loads come in two groups with their own barriers: the [W ; Q'] and Z tiles
-// (read only by MMAs, dead once the chunk's W h product completes), and the K and V tiles
-// with the per-token scalars (read until the chunk's state update and by the compute
-// warps).
-__device__ __forceinline__ void issue_ws_loads(StateSmem &S, const TcParams &p, int stage,
-                                               int hv, int slot) {
-    uint64_t *bar = &S.bar_ws[stage];
-    tc::mbar_expect_tx(bar, kScalOff);
-    bulk_load(S.ws[stage], p.ws + ((size_t)slot * p.Hv + hv) * kWsTile, kScalOff, bar);
-}
-__device__ __forceinline__ void issue_kv_loads(StateSmem &S, const TcMaps &maps,
-                                               const TcParams &p, int stage, int t0, int hk,
-                                               int hv, int j0, int slot) {
-    uint64_t *bar = &S.bar_kv[stage];
-    tc::mbar_expect_tx(bar, 16384 + 8192 + kScalBytes);
-    tc::tma_load_3d(S.k[stage] + 0, &maps.k, bar, 0, hk, t0);
-    tc::tma_load_3d(S.k[stage] + 8192, &maps.k, bar, 64, hk, t0);
+__device__ __forceinline__ void issue_chunk_loads(StateSmem &S, const TcMaps &maps,
+                                                  const TcParams &p, int stage, int t0,
+                                                  int hk, int hv, int j0, int slot) {
+    uint64_t *bar = &S.bar_tma[stage];
+    tc::mbar_expect_tx(bar, 32768 + 8192 + kWsTile);
+    uint8_t *kq = S.kq[stage];
+    tc::tma_load_3d(kq + 0, &maps.k, bar, 0, hk, t0);
+    tc::tma_load_3d(kq + 16384, &maps.k, bar, 64, hk, t0);
+    tc::tma_load_3d(kq + 8192, &maps.q, bar, 0, hk, t0);
+    tc::tma_load_3d(kq + 16384 + 8192, &maps.q, bar, 64, hk, t0);
     tc::tma_load_3d(S.v[stage], &maps.v, bar, j0, hv, t0);
-    bulk_load(S.ws[stage] + kScalOff, p.ws + ((size_t)slot * p.Hv + hv) * kWsTile + kScalOff,
-              kScalBytes, bar);
+    const uint8_t *src = p.ws + ((size_t)slot * p.Hv + hv) * kWsTile;
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(tc::smem_u32(S.x[stage])), "l"(src), "r"(kWsTile),
+                    "r"(tc::smem_u32(bar)) : "memory");
 }
 
 // NC consecutive TMEM columns of this thread's lane (NC = 32, 24 or 16).
@@ -796,16 +629,11 @@ __device__ __forceinline__ void out_barrier() {
 }
 
 // The per-CTA program for one dv tile of NT columns starting at column j0 (NT = 64, 48
-// or 32).  Warp 8 issues every MMA and warp 9 every TMA and bulk load, so no compute warp
-// ever stalls behind an issue queue; warps 0..7 hold the fp32 state rows and do the
-// elementwise work.
+// or 32).  Warp 8 issues every MMA and warp 9 every TMA load, so no compute warp ever stalls
+// behind an issue queue; warps 0..7 hold the fp32 state rows and do the elementwise work.
 // Operand tiles are 64 columns wide in shared memory whatever NT is; an NT-wide MMA reads
 // only the first NT columns.  [hi | lo] is one 2 NT-wide MN-major operand whose 64-column
 // blocks are S.dvh and S.dvl.
-//
-// TMEM columns: the chunk accumulator D, double-buffered at 0 and 64 so that the next
-// chunk's Z V can be issued while the current D is still being read, and the state update
-// [K^T hi | K^T lo] at 128.
 template <int NT>
 __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, const TcParams &p,
                                           const CUtensorMap *omap, int j0, int hv, int n) {
@@ -818,20 +646,19 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
     const int s0 = slot0(p.cu, n);
     const size_t hoff = ((size_t)n * p.Hv + hv) * kD * kD;
     const uint32_t tmem = S.tmem;
-    const uint32_t colS = 128;
+    // TMEM columns: D1 [K;Q]h, D2 [Lo;Mt]R, and the state update as a hi | lo pair
+    const uint32_t colD1 = 0, colD2 = 64, colS = 128;
     volatile int *abort = &S.abort;
 
     if (warp == kIssuerWarp) {
         // ------------------------------------------------------------ issuer warp
-        // Lane 0 does the bounded waits; the whole warp then issues each MMA group in
-        // converged code (one elected lane issues), which keeps the descriptors in uniform
-        // registers.  Shared-memory descriptors are built once; a byte offset o is added as
-        // o >> 4.  Stage b of a double buffer sits b * (buffer bytes) after stage 0.
-        const uint64_t dWQ0 = tc::sdesc(tc::smem_u32(S.ws[0]), 16, 1024);          // K-major
-        const uint64_t dZ0 = tc::sdesc(tc::smem_u32(S.ws[0] + kZOff), 16, 1024);   // K-major
-        const uint64_t dKt0 = tc::sdesc(tc::smem_u32(S.k[0]), 8192, 1024);         // K^T, MN-major
-        const uint64_t dV0 = tc::sdesc(tc::smem_u32(S.v[0]), 8192, 1024);          // MN-major
+        // Shared-memory descriptors, built once; a byte offset o is added as o >> 4.
+        // Stage b of a double buffer sits b * (buffer bytes) after stage 0.
+        const uint64_t dKQ0 = tc::sdesc(tc::smem_u32(S.kq[0]), 16, 1024);      // [K;Q], K-major
+        const uint64_t dKQt0 = tc::sdesc(tc::smem_u32(S.kq[0]), 16384, 1024);  // K^T, MN-major
+        const uint64_t dX0 = tc::sdesc(tc::smem_u32(S.x[0]), 16, 1024);        // [Lo;Mt], K-major
         const uint64_t dH = tc::sdesc(tc::smem_u32(S.hb), 8192, 1024);
+        const uint64_t dR = tc::sdesc(tc::smem_u32(S.rb), 8192, 1024);
         const uint64_t dVhl = tc::sdesc(tc::smem_u32(S.dvh), 8192, 1024);
         constexpr uint32_t id1 = tc::idesc_bf16(128, NT, 0, 1);
         constexpr uint32_t id3 = tc::idesc_bf16(128, 2 * NT, 1, 1);
@@ -839,38 +666,31 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
         bool ok = true;   // meaningful in lane 0
         // lane 0's verdict, broadcast: go on issuing unless a wait ran out
         auto go = [&]() { return __shfl_sync(0xffffffffu, (ok && !*abort) ? 1 : 0, 0) != 0; };
-        // D = Z V of chunk c into its stage's accumulator, once the chunk's tiles landed.
-        // It needs nothing of the chain: chunk c's is issued right after chunk c-1's state
-        // update, so it runs while the compute warps fold that update.
-        auto issue_zv = [&](int c) {
+        // A chunk's tiles are waited for before the barrier that publishes its h: for
+        // chunk c+1 right after chunk c's state update is issued, while the compute warps
+        // fold that update, so the wait stays off the chain.
+        if (leader && nch > 0) ok = wait_one(&S.bar_tma[0], 0, abort);
+        for (int c = 0; c < nch; ++c) {
             const int st = c & 1;
-            if (leader) {
-                if (ok) ok = wait_one(&S.bar_ws[st], (c >> 1) & 1, abort);
-                if (ok) ok = wait_one(&S.bar_kv[st], (c >> 1) & 1, abort);
+            __syncthreads();                                   // h published as bf16
+            if (go()) {
+                tc::fence_after_sync();
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_bf16_warp(tmem + colD1,
+                                      dKQ0 + ((st * 32768 + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                                      dH + ((ks * 2048) >> 4), id1, ks > 0);
+                tc::mma_commit_warp(&S.bar_d1);
             }
+            __syncwarp();
+            chain_barrier();                                   // R ready
             if (go()) {
                 tc::fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16_warp(tmem + 64 * st, dZ0 + ((st * kWsStage + ks * 32) >> 4),
-                                      dV0 + ((st * 8192 + ks * 2048) >> 4), id1, ks > 0);
-            }
-            __syncwarp();
-        };
-        if (nch > 0) issue_zv(0);
-        for (int c = 0; c < nch; ++c) {
-            const int st = c & 1;
-            const uint32_t colD = 64 * st;
-            __syncthreads();                                   // h published as bf16
-            if (go()) {
-                tc::fence_after_sync();
-                // D += [W ; Q'] h
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16_warp(tmem + colD,
-                                      dWQ0 + ((st * kWsStage + (ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                                      dH + ((ks * 2048) >> 4), id1, 1);
-                tc::mma_commit_warp(&S.bar_d1);
+                    tc::mma_bf16_warp(tmem + colD2, dX0 + ((st * kXStage + ks * 32) >> 4),
+                                      dR + ((ks * 2048) >> 4), id1, ks > 0);
+                tc::mma_commit_warp(&S.bar_d2);
             }
             __syncwarp();
             chain_barrier();                                   // hi | lo of d Vn ready
@@ -879,14 +699,13 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
                 tc::fence_after_sync();
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16_warp(tmem + colS, dKt0 + ((st * 16384 + ks * 2048) >> 4),
+                    tc::mma_bf16_warp(tmem + colS, dKQt0 + ((st * 32768 + ks * 2048) >> 4),
                                       dVhl + ((ks * 2048) >> 4), id3, ks > 0);
                 tc::mma_commit_warp(&S.bar_d3);
             }
             __syncwarp();
-            // The next chunk's accumulator (stage st^1) was last read in chunk c-1, whose
-            // readers all passed this chunk's first barrier.
-            if (c + 1 < nch) issue_zv(c + 1);
+            if (leader && ok && c + 1 < nch)
+                ok = wait_one(&S.bar_tma[st ^ 1], ((c + 1) >> 1) & 1, abort);
         }
         // Nothing this warp started may still run when the CTA exits: wait (bounded) for
         // every MMA it issued.
@@ -899,43 +718,32 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
     }
     if (warp == kLoaderWarp) {
         // ----------------------------------------------------------- loader warp
-        // Chunks 0 and 1 are loaded up front; chunk c+2 goes into stage c&1 after chunk c.
-        //  * Its [W ; Q'] and Z tiles leave as soon as chunk c's W h product completes: only
-        //    that product and the Z V before it read them.
-        //  * Its K, V and scalars leave after the barrier that publishes h for chunk c+1: by
-        //    then every compute warp has finished its reads of stage c&1 and waited for
-        //    chunk c's state update, the last MMA that reads K.
-        // The loads thus leave one to one and a half chunks ahead, on a warp of their own
-        // (issuing them costs the MMA issuer no time).
+        // Chunks 0 and 1 are loaded up front; chunk c+1 (c >= 1) goes into stage (c+1)&1
+        // after the barrier that publishes chunk c's h: every warp has then finished chunk
+        // c-1, the stage's previous occupant (its last MMA, the state update, completed
+        // before the compute warps folded it).  Issuing them costs the MMA issuer nothing.
         const bool leader = lane == 0;
-        int ws_issued = 0, kv_issued = 0;                      // chunks 0..n-1 are loaded
+        int issued = 0;                                        // chunks 0..issued-1 are loaded
         if (leader) {
             for (int c = 0; c < 2 && c < nch; ++c) {
-                issue_ws_loads(S, p, c, hv, s0 + c);
-                issue_kv_loads(S, maps, p, c, start + c * kC, hk, hv, j0, s0 + c);
-                ws_issued = kv_issued = c + 1;
+                issue_chunk_loads(S, maps, p, c, start + c * kC, hk, hv, j0, s0 + c);
+                issued = c + 1;
             }
         }
         for (int c = 0; c < nch; ++c) {
             __syncwarp();
             __syncthreads();                                   // h published as bf16
             if (leader && c >= 1 && c + 1 < nch && !*abort) {
-                issue_kv_loads(S, maps, p, (c + 1) & 1, start + (c + 1) * kC, hk, hv, j0,
-                               s0 + c + 1);
-                kv_issued = c + 2;
-            }
-            if (leader && c + 2 < nch && !*abort && wait_one(&S.bar_d1, c & 1, abort)) {
-                issue_ws_loads(S, p, c & 1, hv, s0 + c + 2);
-                ws_issued = c + 3;
+                issue_chunk_loads(S, maps, p, (c + 1) & 1, start + (c + 1) * kC, hk, hv, j0,
+                                  s0 + c + 1);
+                issued = c + 2;
             }
         }
         if (leader) {
             // wait (bounded) for the last load into each stage before the CTA may exit
             for (int s = 0; s < 2; ++s) {
-                int last = ws_issued - 1 - ((ws_issued - 1 - s) & 1);   // last chunk into stage s
-                if (last >= 0) wait_bounded(&S.bar_ws[s], (last >> 1) & 1);
-                last = kv_issued - 1 - ((kv_issued - 1 - s) & 1);
-                if (last >= 0) wait_bounded(&S.bar_kv[s], (last >> 1) & 1);
+                const int last = issued - 1 - ((issued - 1 - s) & 1);   // last chunk into stage s
+                if (last >= 0) wait_bounded(&S.bar_tma[s], (last >> 1) & 1);
             }
         }
         __syncwarp();
@@ -975,12 +783,11 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
         const uint32_t ph = c & 1;
         const int t0 = start + c * kC;
         const int L = min(kC, len - c * kC);
-        const uint32_t colD = 64 * st;
 
         // --- A: fold the previous chunk's update into h, publish the bf16 copy.  This
         // chunk's tiles were requested a chunk ago: waiting for them here overlaps the
         // barrier query with the previous update's MMAs instead of following the barrier.
-        if (ok) ok = wait_one(&S.bar_kv[st], (c >> 1) & 1, abort);
+        if (ok) ok = wait_one(&S.bar_tma[st], (c >> 1) & 1, abort);
         if (c > 0 && ok) {
             ok = wait_one(&S.bar_d3, ph ^ 1, abort);
             if (ok) {
@@ -992,116 +799,147 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
-        const float *sc = reinterpret_cast<const float *>(S.ws[st] + kScalOff);
-        const float aL = sc[128];
+        const float *sc = reinterpret_cast<const float *>(S.x[st] + kXTile);
+        const float *gam = sc, *bet = sc + 64, *nk = sc + 128, *nq = sc + 192;
+        const float gL = gam[L - 1];
+        const float gr = gam[r];
 
-        // --- B: D = Z V + [W ; Q'] h
+        // --- B: R = beta (V - e^gamma nk K h) on the chain rows; e^gamma nq Q h on the rest
         if (ok) ok = wait_one(&S.bar_d1, ph, abort);
-        float d1[NC];
-        if (ok) {
-            tc::fence_after_sync();
-            tmem_cols<NC>(tmem + lane_off + colD + ch, d1);
-        } else {
-#pragma unroll
-            for (int j = 0; j < NC; ++j) d1[j] = 0.f;
-        }
-        if (chain) {
-            // Vn = beta V - D on the chain rows, then d Vn as bf16 hi + lo
-            // x = d (beta V - D), formed as (-d) (D - beta V) two columns at a time: the
-            // same roundings as d * fma(beta, v, -D) (negation is exact)
-            const bool live = r < L;
-            const float2 nb = make_float2(-sc[r], -sc[r]);
-            const float2 nd = make_float2(-sc[64 + r], -sc[64 + r]);
-            float x[NC];
-            if (live) {
-#pragma unroll
-                for (int cc = 0; cc < NCH; ++cc) {
-                    const uint4 u = *reinterpret_cast<const uint4 *>(S.v[st] + tc::swz(r, c0 + cc));
-                    const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = 8 * cc + 2 * e;
-                        const float2 v2 = make_float2(__uint_as_float(uw[e] << 16),
-                                                      __uint_as_float(uw[e] & 0xffff0000u));
-                        const float2 t = fma2(nb, v2, make_float2(d1[i], d1[i + 1]));
-                        const float2 xx = mul2(nd, t);
-                        x[i] = xx.x;
-                        x[i + 1] = xx.y;
-                    }
-                }
+        float keep[NC];
+        {
+            float d1[NC];
+            if (ok) {
+                tc::fence_after_sync();
+                tmem_cols<NC>(tmem + lane_off + colD1 + ch, d1);
             } else {
 #pragma unroll
-                for (int i = 0; i < NC; ++i) x[i] = 0.f;
+                for (int j = 0; j < NC; ++j) d1[j] = 0.f;
             }
-            // hi = bf16(x) two at a time (the paired conversion issues at several times
-            // the rate of the single one); lo = x - hi is exact in fp32
-            uint32_t hp[NC / 2];
-            float lo[NC];
-            const float2 m1 = make_float2(-1.f, -1.f);
+            if (chain) {
+                // R = beta (v - c d1) two columns at a time; rows past the chunk's end are
+                // exact zeros
+                const float2 br = make_float2(bet[r], bet[r]);
+                const float cr = __expf(gr) * nk[r];
+                const float2 ncr = make_float2(-cr, -cr);
+                if (r < L) {
 #pragma unroll
-            for (int jj = 0; jj < NC / 2; ++jj) {
-                const __nv_bfloat162 hb2 = __floats2bfloat162_rn(x[2 * jj], x[2 * jj + 1]);
-                hp[jj] = *reinterpret_cast<const uint32_t *>(&hb2);
-                const float2 l2 = fma2(m1, make_float2(__uint_as_float(hp[jj] << 16),
-                                                       __uint_as_float(hp[jj] & 0xffff0000u)),
-                                       make_float2(x[2 * jj], x[2 * jj + 1]));
-                lo[2 * jj] = l2.x;
-                lo[2 * jj + 1] = l2.y;
-            }
+                    for (int cc = 0; cc < NCH; ++cc) {
+                        const uint4 u = *reinterpret_cast<const uint4 *>(S.v[st] + tc::swz(r, c0 + cc));
+                        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-            for (int cc = 0; cc < NCH; ++cc) {
-                // hi: elements ch + 8cc of [hi | lo]; lo: NT + ch + 8cc, in 64-wide blocks
-                *reinterpret_cast<uint4 *>(S.dvh + tc::swz(r, c0 + cc)) =
-                    make_uint4(hp[4 * cc], hp[4 * cc + 1], hp[4 * cc + 2], hp[4 * cc + 3]);
-                const int el = NT + 8 * (c0 + cc);
-                float f[8];
+                        for (int q = 0; q < 4; ++q) {
+                            const int i = 8 * cc + 2 * q;
+                            const float2 v2 = make_float2(__uint_as_float(uw[q] << 16),
+                                                          __uint_as_float(uw[q] & 0xffff0000u));
+                            const float2 x2 = mul2(br, fma2(ncr, make_float2(d1[i], d1[i + 1]), v2));
+                            keep[i] = x2.x;
+                            keep[i + 1] = x2.y;
+                        }
+                    }
+                } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = lo[8 * cc + e];
-                *reinterpret_cast<uint4 *>((el >= 64 ? S.dvl : S.dvh) + tc::swz(r, (el & 63) >> 3)) =
-                    pack8(f);
-            }
-            tc::fence_async_smem();
-            tc::fence_before_sync();
-            chain_barrier();
-        } else if (L == kC) {
-            // O = scale D on the output rows.  A full chunk's O tile goes out through shared
-            // memory with one tensor store, keeping 64 scattered row writes per warp off the
-            // load/store pipeline that the chain warps' shared-memory traffic shares.  Stage
-            // st was last stored two chunks ago; allowing one group in flight covers the
-            // previous chunk.  A 64-wide tile uses the 128B-swizzled layout, narrower ones
-            // plain rows.
-            uint8_t *ob = S.ob[st];
-            if (tid == kOutLeader) tc::bulk_wait_read<1>();
-            out_barrier();
+                    for (int j = 0; j < NC; ++j) keep[j] = 0.f;
+                }
+                pack_row<NC>(S.rb, r, c0, keep);
+                tc::fence_async_smem();
+                tc::fence_before_sync();
+                chain_barrier();
+            } else {
+                const float cq = __expf(gr) * nq[r];
+                const float2 cq2 = make_float2(cq, cq);
 #pragma unroll
-            for (int cc = 0; cc < NCH; ++cc) {
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = p.scale * d1[8 * cc + e];
-                const uint32_t off = NT == 64 ? tc::swz(r, c0 + cc)
-                                              : (uint32_t)(r * NT * 2 + (c0 + cc) * 16);
-                *reinterpret_cast<uint4 *>(ob + off) = pack8(f);
-            }
-            tc::fence_async_smem();
-            out_barrier();
-            if (tid == kOutLeader && ok && !*abort) {
-                tc::tma_store_3d(omap, ob, j0, hv, t0);
-                tc::bulk_commit();
-            }
-        } else if (r < L && ok) {
-            // the last, partial chunk of a sequence: rows past L belong to the next one
-            uint4 *dst = reinterpret_cast<uint4 *>(p.o + (size_t)(t0 + r) * p.o_tok +
-                                                   (size_t)hv * kD + j0 + ch);
-#pragma unroll
-            for (int cc = 0; cc < NCH; ++cc) {
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = p.scale * d1[8 * cc + e];
-                dst[cc] = pack8(f);
+                for (int j = 0; j < NC; j += 2) {
+                    const float2 k2 = mul2(cq2, make_float2(d1[j], d1[j + 1]));
+                    keep[j] = k2.x;
+                    keep[j + 1] = k2.y;
+                }
             }
         }
-        tc::fence_before_sync();
-        aL_prev = aL;
+
+        // --- C: Vn = R + Lo R -> d Vn as bf16 hi + lo; outputs on the other rows
+        if (ok) ok = wait_one(&S.bar_d2, ph, abort);
+        {
+            float d2[NC];
+            if (ok) {
+                tc::fence_after_sync();
+                tmem_cols<NC>(tmem + lane_off + colD2 + ch, d2);
+            } else {
+#pragma unroll
+                for (int j = 0; j < NC; ++j) d2[j] = 0.f;
+            }
+            if (chain) {
+                const float dc = r < L ? __expf(gL - gr) * nk[r] : 0.f;
+                // hi = bf16(x) two at a time (the paired conversion issues at several times
+                // the rate of the single one); lo = x - hi is exact in fp32
+                uint32_t hp[NC / 2];
+                float lo[NC];
+                const float2 dc2 = make_float2(dc, dc), m1 = make_float2(-1.f, -1.f);
+#pragma unroll
+                for (int jj = 0; jj < NC / 2; ++jj) {
+                    const float2 x2 = mul2(dc2, add2(make_float2(keep[2 * jj], keep[2 * jj + 1]),
+                                                     make_float2(d2[2 * jj], d2[2 * jj + 1])));
+                    const __nv_bfloat162 hb2 = __floats2bfloat162_rn(x2.x, x2.y);
+                    hp[jj] = *reinterpret_cast<const uint32_t *>(&hb2);
+                    const float2 l2 = fma2(m1, make_float2(__uint_as_float(hp[jj] << 16),
+                                                           __uint_as_float(hp[jj] & 0xffff0000u)), x2);
+                    lo[2 * jj] = l2.x;
+                    lo[2 * jj + 1] = l2.y;
+                }
+#pragma unroll
+                for (int cc = 0; cc < NCH; ++cc) {
+                    // hi: elements ch + 8cc of [hi | lo]; lo: NT + ch + 8cc, in 64-wide blocks
+                    *reinterpret_cast<uint4 *>(S.dvh + tc::swz(r, c0 + cc)) =
+                        make_uint4(hp[4 * cc], hp[4 * cc + 1], hp[4 * cc + 2], hp[4 * cc + 3]);
+                    const int el = NT + 8 * (c0 + cc);
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = lo[8 * cc + e];
+                    *reinterpret_cast<uint4 *>((el >= 64 ? S.dvl : S.dvh) + tc::swz(r, (el & 63) >> 3)) =
+                        pack8(f);
+                }
+                tc::fence_async_smem();
+                tc::fence_before_sync();
+                chain_barrier();
+            } else if (L == kC) {
+                // A full chunk's O tile goes out through shared memory with one tensor store,
+                // keeping 64 scattered row writes per warp off the load/store pipeline that
+                // the chain warps' shared-memory traffic shares.  Stage st was last stored
+                // two chunks ago; allowing one group in flight covers the previous chunk.
+                // A 64-wide tile uses the 128B-swizzled layout, narrower ones plain rows.
+                uint8_t *ob = S.ob[st];
+                if (tid == kOutLeader) tc::bulk_wait_read<1>();
+                out_barrier();
+#pragma unroll
+                for (int cc = 0; cc < NCH; ++cc) {
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = p.scale * (keep[8 * cc + e] + d2[8 * cc + e]);
+                    const uint32_t off = NT == 64 ? tc::swz(r, c0 + cc)
+                                                  : (uint32_t)(r * NT * 2 + (c0 + cc) * 16);
+                    *reinterpret_cast<uint4 *>(ob + off) = pack8(f);
+                }
+                tc::fence_async_smem();
+                out_barrier();
+                if (tid == kOutLeader && ok && !*abort) {
+                    tc::tma_store_3d(omap, ob, j0, hv, t0);
+                    tc::bulk_commit();
+                }
+            } else if (r < L && ok) {
+                // the last, partial chunk of a sequence: rows past L belong to the next one
+                uint4 *dst = reinterpret_cast<uint4 *>(p.o + (size_t)(t0 + r) * p.o_tok +
+                                                       (size_t)hv * kD + j0 + ch);
+#pragma unroll
+                for (int cc = 0; cc < NCH; ++cc) {
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = p.scale * (keep[8 * cc + e] + d2[8 * cc + e]);
+                    dst[cc] = pack8(f);
+                }
+            }
+            tc::fence_before_sync();
+        }
+        aL_prev = __expf(gL);
     }
     if (ok && nch > 0) {
         ok = wait_one(&S.bar_d3, (nch - 1) & 1, abort);
@@ -1140,16 +978,16 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        tc::mbar_init(&S.bar_ws[0], 1);
-        tc::mbar_init(&S.bar_ws[1], 1);
-        tc::mbar_init(&S.bar_kv[0], 1);
-        tc::mbar_init(&S.bar_kv[1], 1);
+        tc::mbar_init(&S.bar_tma[0], 1);
+        tc::mbar_init(&S.bar_tma[1], 1);
         tc::mbar_init(&S.bar_d1, 1);
+        tc::mbar_init(&S.bar_d2, 1);
         tc::mbar_init(&S.bar_d3, 1);
         tc::mbar_init(&S.bar_fin, 1);
         S.abort = 0;
         tc::mbar_fence_init();
         tc::prefetch_tmap(&maps.k);
+        tc::prefetch_tmap(&maps.q);
         tc::prefetch_tmap(&maps.v);
         tc::prefetch_tmap(p.ntiles == 3 ? (jt < 2 ? &maps.o48 : &maps.o32) : &maps.o);
     }
@@ -1257,8 +1095,6 @@ gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStre
     p.hT = a.hT;
     p.o = (gdn::bf16 *)a.o;
     p.o_tok = a.o_tok;
-    p.q = (const gdn::bf16 *)a.q;
-    p.q_tok = a.q_tok;
     p.ws = (uint8_t *)a.ws;
     p.N = a.N;
     p.Hk = a.Hk;
@@ -1267,11 +1103,8 @@ gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStre
     p.l2norm = (a.flags & GDN_QK_L2NORM) ? 1 : 0;
     p.status = a.status;
     // Three dv tiles per head (48 + 48 + 32 columns) when they still fit one wave on the
-    // SMs, else two of 64.  So the tiling follows N and the device's SM count; it changes
-    // how the columns are grouped, not the arithmetic of any column (every column's
-    // products, reductions and roundings are the same whatever tile it sits in), which
-    // keeps a sequence's bits the same alone and in a batch.  GDN_PREFILL_TILES2/3 force
-    // one tiling; the GPU tests run the same sequences under both and compare the bits.
+    // SMs, else two of 64: the tiling changes how the columns are grouped, not the
+    // arithmetic of any column.
     const int sms = sm_count();
     if (a.flags & GDN_PREFILL_TILES2)
         p.ntiles = 2;
@@ -1297,11 +1130,9 @@ gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStre
             return GDN_ERR_CUDA;
         attr_set[dev].store(true, std::memory_order_release);
     }
-    const int64_t slots64 = (a.T + gdn::kC - 1) / gdn::kC + a.N;
-    if (slots64 > 65535) return GDN_ERR_SHAPE;   // chunk slots index the grid's y dimension
-    const int slots = (int)slots64;
+    const int slots = (int)((a.T + gdn::kC - 1) / gdn::kC) + a.N;
     if (slots > 0) {
-        dim3 g1(a.Hv, slots);
+        dim3 g1(slots, a.Hv);
         if (launch_dependent(gdn::chunk_prep_kernel, g1, dim3(gdn::kPrepThreads), prep_smem, st,
                              maps, p) != cudaSuccess)
             return GDN_ERR_CUDA;

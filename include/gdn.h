@@ -168,10 +168,10 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t *q, const gdn_tensor_t *k,
  * Arguments, results, kernels and errors are those of gdn_chunk_prefill, except that the
  * scratch comes from a fixed array of GDN_NOALLOC_SCRATCH_BYTES inside the library's
  * device image, which every GPU that loads the library holds until the process exits.
- * A tensor-core call needs (ceil(T / 64) + N + 1) * Hv * 49680 bytes (one 49680-byte tile
+ * A tensor-core call needs (ceil(T / 64) + N + 1) * Hv * 17408 bytes (one 17408-byte tile
  * per chunk slot and v-head); one whose size exceeds the array returns GDN_ERR_WORKSPACE
- * before launching anything.  With 48 v-heads that admits up to 56 slots, e.g. one
- * 3456-token sequence or 8 sequences totalling 3008 tokens; fp32 activations (CUDA-core
+ * before launching anything.  With 48 v-heads that admits up to 160 slots, e.g. one
+ * 10112-token sequence or 8 sequences totalling 9664 tokens; fp32 activations (CUDA-core
  * kernel) need no scratch at any size.  The call allocates nothing (no cudaMalloc or
  * cudaFree, no allocating library routine).
  * The first call on a device (with that device current) looks up the array's device

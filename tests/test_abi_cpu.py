@@ -171,14 +171,13 @@ def test_fused_decode_rejections(lib):
 @no_gpu
 def test_workspace_size(lib):
     """The CUDA-core path needs no workspace; the tensor-core path needs one tile per
-    (chunk slot, v-head): the bf16 128x128 [W ; Q'] tile, the bf16 128x64 Z tile and 132
-    fp32 scalars (beta and the state-update weight per token, e^{gamma_L}, padding), over
-    ceil(T / 64) + N + 1 slots (chunks anchored at every sequence start)."""
+    (chunk slot, v-head), the bf16 128x64 [Lo ; Mt] tile plus four fp32 per-token
+    scalars, over ceil(T / 64) + N + 1 slots (chunks anchored at every sequence start)."""
     f = lib.gdn_chunk_prefill_workspace_size
     assert f(2, 500, 2, 4, 64, 64, 64, 0) == 0
     assert f(2, 500, 2, 4, 128, 128, 16, 0) == 0
     assert f(2, 500, 2, 4, 128, 128, 64, _lib.GDN_PREFILL_SIMT) == 0
-    tile = 128 * 128 * 2 + 128 * 64 * 2 + 132 * 4
+    tile = 128 * 64 * 2 + 4 * 64 * 4
     for N, T, Hv in ((1, 4096, 48), (8, 30702, 48), (40, 311605, 32), (3, 0, 6)):
         assert f(N, T, 16, Hv, 128, 128, 64, 0) == (-(-T // 64) + N + 1) * Hv * tile
 
