@@ -788,6 +788,17 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
         // chunk's tiles were requested a chunk ago: waiting for them here overlaps the
         // barrier query with the previous update's MMAs instead of following the barrier.
         if (ok) ok = wait_one(&S.bar_tma[st], (c >> 1) & 1, abort);
+        // this row's per-token factors, formed while the previous update's MMAs run
+        const float *sc = reinterpret_cast<const float *>(S.x[st] + kXTile);
+        const float *gam = sc, *bet = sc + 64, *nk = sc + 128, *nq = sc + 192;
+        const float gL = gam[L - 1];
+        const float gr = gam[r];
+        const float egr = __expf(gr);
+        const float cr = egr * nk[r];                          // e^gamma nk   (chain rows)
+        const float cq = egr * nq[r];                          // e^gamma nq   (output rows)
+        const float dc = r < L ? __expf(gL - gr) * nk[r] : 0.f;   // e^{gamma_L-gamma} nk
+        const float br = bet[r];
+        const float aL = __expf(gL);
         if (c > 0 && ok) {
             ok = wait_one(&S.bar_d3, ph ^ 1, abort);
             if (ok) {
@@ -799,10 +810,13 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
         tc::fence_async_smem();
         tc::fence_before_sync();
         __syncthreads();
-        const float *sc = reinterpret_cast<const float *>(S.x[st] + kXTile);
-        const float *gam = sc, *bet = sc + 64, *nk = sc + 128, *nq = sc + 192;
-        const float gL = gam[L - 1];
-        const float gr = gam[r];
+        // this row's V columns, read ahead of the D1 wait (the chain rows' R needs them)
+        uint4 vraw[NCH];
+        if (chain) {
+#pragma unroll
+            for (int cc = 0; cc < NCH; ++cc)
+                vraw[cc] = *reinterpret_cast<const uint4 *>(S.v[st] + tc::swz(r, c0 + cc));
+        }
 
         // --- B: R = beta (V - e^gamma nk K h) on the chain rows; e^gamma nq Q h on the rest
         if (ok) ok = wait_one(&S.bar_d1, ph, abort);
@@ -819,20 +833,19 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
             if (chain) {
                 // R = beta (v - c d1) two columns at a time; rows past the chunk's end are
                 // exact zeros
-                const float2 br = make_float2(bet[r], bet[r]);
-                const float cr = __expf(gr) * nk[r];
+                const float2 br2 = make_float2(br, br);
                 const float2 ncr = make_float2(-cr, -cr);
                 if (r < L) {
 #pragma unroll
                     for (int cc = 0; cc < NCH; ++cc) {
-                        const uint4 u = *reinterpret_cast<const uint4 *>(S.v[st] + tc::swz(r, c0 + cc));
+                        const uint4 u = vraw[cc];
                         const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const int i = 8 * cc + 2 * q;
                             const float2 v2 = make_float2(__uint_as_float(uw[q] << 16),
                                                           __uint_as_float(uw[q] & 0xffff0000u));
-                            const float2 x2 = mul2(br, fma2(ncr, make_float2(d1[i], d1[i + 1]), v2));
+                            const float2 x2 = mul2(br2, fma2(ncr, make_float2(d1[i], d1[i + 1]), v2));
                             keep[i] = x2.x;
                             keep[i + 1] = x2.y;
                         }
@@ -846,7 +859,6 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
                 tc::fence_before_sync();
                 chain_barrier();
             } else {
-                const float cq = __expf(gr) * nq[r];
                 const float2 cq2 = make_float2(cq, cq);
 #pragma unroll
                 for (int j = 0; j < NC; j += 2) {
@@ -869,7 +881,6 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
                 for (int j = 0; j < NC; ++j) d2[j] = 0.f;
             }
             if (chain) {
-                const float dc = r < L ? __expf(gL - gr) * nk[r] : 0.f;
                 // hi = bf16(x) two at a time (the paired conversion issues at several times
                 // the rate of the single one); lo = x - hi is exact in fp32
                 uint32_t hp[NC / 2];
@@ -939,7 +950,7 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
             }
             tc::fence_before_sync();
         }
-        aL_prev = __expf(gL);
+        aL_prev = aL;
     }
     if (ok && nch > 0) {
         ok = wait_one(&S.bar_d3, (nch - 1) & 1, abort);
