@@ -579,10 +579,19 @@ def multiseq_leg(gdn, inputs, dev, flush_l2, peak_tf, warmup, steps):
               inputs.varlen_lengths(3), 16, 48, True),
              ("4B shapes, the mix's 40 prefills: 20 fresh U[12, 32768] and 20 continuations "
               "of 2048 on initial states", fresh + cont, 16, 32, True)]
+    # a head-sharded layer (the 27B heads over 8 GPUs of tensor parallelism: Hk=2, Hv=6)
+    # on one long sequence: its 18 chains leave most SMs idle, so the scan also runs
+    # context-parallel, in ranges of 32 and of 64 chunks (range_chunks, last field)
+    cases += [("27B heads / 8 (Hk=2, Hv=6), 1 x 32768 tokens", [32768], 2, 6, True, 0),
+              ("27B heads / 8 (Hk=2, Hv=6), 1 x 32768 tokens, context-parallel in ranges "
+               "of 64 chunks", [32768], 2, 6, True, 64),
+              ("27B heads / 8 (Hk=2, Hv=6), 1 x 32768 tokens, context-parallel in ranges "
+               "of 32 chunks", [32768], 2, 6, True, 32)]
+    cases = [c if len(c) == 6 else c + (0,) for c in cases]
     gen = torch.Generator(device=dev)
     gen.manual_seed(7)
     out, launches = [], 0
-    for name, lens, Hk, Hv, init in cases:
+    for name, lens, Hk, Hv, init, range_chunks in cases:
         T, N = sum(lens), len(lens)
 
         def unit_rows(t):
@@ -598,13 +607,22 @@ def multiseq_leg(gdn, inputs, dev, flush_l2, peak_tf, warmup, steps):
         h0 = torch.randn(N, Hv, 128, 128, device=dev, generator=gen) * 0.02 if init else None
         o = torch.empty((T, Hv, 128), dtype=torch.bfloat16, device=dev)
         hT = torch.empty((N, Hv, 128, 128), dtype=torch.float32, device=dev)
-        ws = torch.empty(max(gdn.gdn_chunk_prefill_workspace_size(N, T, Hk, Hv, 128, 128,
-                                                                  CHUNK), 256),
-                         dtype=torch.uint8, device=dev)
+        if range_chunks:
+            ws_bytes = gdn.gdn_chunk_prefill_cp_workspace_size(cu_h, T, Hk, Hv, 128, 128,
+                                                               range_chunks, CHUNK)
+        else:
+            ws_bytes = gdn.gdn_chunk_prefill_workspace_size(N, T, Hk, Hv, 128, 128, CHUNK)
+        ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
 
         def scan():
-            gdn.gdn_chunk_prefill(q, k, v, g, beta, cu, chunk=CHUNK, initial_state=h0, o=o,
-                                  final_state=hT, cu_seqlens_host=cu_h, workspace=ws)
+            if range_chunks:
+                gdn.gdn_chunk_prefill_cp(q, k, v, g, beta, cu, range_chunks, chunk=CHUNK,
+                                         initial_state=h0, o=o, final_state=hT,
+                                         cu_seqlens_host=cu_h, workspace=ws)
+            else:
+                gdn.gdn_chunk_prefill(q, k, v, g, beta, cu, chunk=CHUNK, initial_state=h0,
+                                      o=o, final_state=hT, cu_seqlens_host=cu_h,
+                                      workspace=ws)
         for _ in range(warmup):
             flush_l2()
             scan()
@@ -616,10 +634,11 @@ def multiseq_leg(gdn, inputs, dev, flush_l2, peak_tf, warmup, steps):
             scan()
             e1.record()
         torch.cuda.synchronize()
-        launches += 2 * steps
+        launches += (5 if range_chunks else 2) * steps
         ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
         tf = prefill_flops_per_token(Hk, Hv, 128, 128) * T / (ms * 1e-3) / 1e12
         out.append({"workload": name, "tokens": T, "sequences": N, "longest": max(lens),
+                    "range_chunks": range_chunks or None,
                     "ms": ms, "tokens_per_s": T / (ms * 1e-3), "tflops": tf,
                     "frac": tf / peak_tf,
                     "roofline": {"kernel": "chunk_prefill", "bound": "tensor", "achieved": tf,

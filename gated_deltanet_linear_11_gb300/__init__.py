@@ -28,7 +28,8 @@ from ._lib import (GDN_PREFILL_SIMT, GDN_PREFILL_TILES2, GDN_PREFILL_TILES3,  # 
                    GDN_QK_L2NORM, GdnError)
 
 __all__ = ["gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
-           "gdn_chunk_prefill_noalloc",
+           "gdn_chunk_prefill_noalloc", "gdn_chunk_prefill_cp",
+           "gdn_chunk_prefill_cp_workspace_size",
            "gdn_recurrent_decode", "gdn_fused_decode", "gdn_chunk_prefill_workspace_size",
            "gdn_layer_prefill", "gdn_layer_decode", "GdnError", "load"]
 
@@ -169,6 +170,48 @@ def gdn_chunk_prefill(q, k, v, g, beta, cu_seqlens, chunk=64, scale=1.0, l2norm=
         _vp(initial_state), ctypes.byref(do), _vp(final_state), _vp(workspace),
         ws_bytes, _vp(status), _stream())
     _lib.check(rc, "gdn_chunk_prefill")
+    return o, final_state
+
+
+def gdn_chunk_prefill_cp_workspace_size(cu_seqlens_host, T, Hk, Hv, dk, dv, range_chunks,
+                                        chunk=64):
+    """Workspace bytes of gdn_chunk_prefill_cp (0 for a shape it does not take)."""
+    lib = _lib.load()
+    cu_h = cu_seqlens_host.to(torch.int32).contiguous()
+    return int(lib.gdn_chunk_prefill_cp_workspace_size(
+        ctypes.c_void_p(cu_h.data_ptr()), cu_h.numel() - 1, T, Hk, Hv, dk, dv, chunk,
+        range_chunks))
+
+
+def gdn_chunk_prefill_cp(q, k, v, g, beta, cu_seqlens, range_chunks, chunk=64, scale=1.0,
+                         l2norm=False, initial_state=None, output_final_state=True, o=None,
+                         final_state=None, cu_seqlens_host=None, workspace=None, status=None,
+                         tiles=None):
+    """gdn_chunk_prefill with every sequence split into ranges of ``range_chunks`` chunks
+    run side by side (the context-parallel scan; tensor-core path only).  Returns
+    (o, final_state)."""
+    lib = _lib.load()
+    _need_cuda(q, k, v, g, beta, initial_state, o, final_state, workspace, status)
+    cu, cu_h = _seqlens(cu_seqlens, cu_seqlens_host)
+    N = cu_h.numel() - 1
+    T, Hk, dk = q.shape[-3:]
+    Hv, dv = v.shape[-2:]
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=q.device)
+    flags = (GDN_QK_L2NORM if l2norm else 0) | _tile_flag(tiles)
+    ws_bytes = int(lib.gdn_chunk_prefill_cp_workspace_size(
+        ctypes.c_void_p(cu_h.data_ptr()), N, T, Hk, Hv, dk, dv, chunk, range_chunks))
+    if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    dq, dk_, dv_, do = _desc(q), _desc(k), _desc(v), _desc(o)
+    rc = lib.gdn_chunk_prefill_cp(
+        ctypes.byref(dq), ctypes.byref(dk_), ctypes.byref(dv_), _vp(g.contiguous()),
+        _vp(beta.contiguous()), _vp(cu), ctypes.c_void_p(cu_h.data_ptr()), N, chunk,
+        float(scale), flags, int(range_chunks), _vp(initial_state), ctypes.byref(do),
+        _vp(final_state), _vp(workspace), ws_bytes, _vp(status), _stream())
+    _lib.check(rc, "gdn_chunk_prefill_cp")
     return o, final_state
 
 

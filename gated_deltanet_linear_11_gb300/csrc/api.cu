@@ -151,7 +151,8 @@ gdn_status_t chunk_prefill_impl(const gdn_tensor_t *q, const gdn_tensor_t *k,
                                 int32_t N, int32_t chunk, float scale, uint32_t flags,
                                 const float *initial_state, const gdn_tensor_t *o,
                                 float *final_state, void *workspace, size_t workspace_bytes,
-                                int32_t *status_dev, void *stream, cudaEvent_t v_ready) {
+                                int32_t *status_dev, void *stream, cudaEvent_t v_ready,
+                                int32_t range_chunks = 0) {
     View Q, K, V, O;
     gdn_status_t s;
     if ((s = view_of(q, Q)) != GDN_OK) return s;
@@ -194,7 +195,20 @@ gdn_status_t chunk_prefill_impl(const gdn_tensor_t *q, const gdn_tensor_t *k,
     a.in_f32 = Q.dtype == GDN_F32; a.out_f32 = O.dtype == GDN_F32;
     a.status = status_dev; a.ws = workspace; a.ws_bytes = workspace_bytes;
 
-    if (!(flags & GDN_PREFILL_SIMT) && gdn_host::chunk_tc_supported(a.dk, a.dv, chunk, a.in_f32)) {
+    const bool tc = !(flags & GDN_PREFILL_SIMT) &&
+                    gdn_host::chunk_tc_supported(a.dk, a.dv, chunk, a.in_f32);
+    if (range_chunks != 0) {
+        // the context-parallel scan exists on the tensor-core path only
+        if (!tc || a.out_f32) return GDN_ERR_UNSUPPORTED;
+        if (range_chunks < 0) return GDN_ERR_SHAPE;
+        const size_t need = gdn_host::chunk_tc_cp_workspace(cu_seqlens_host, N, Q.T, a.Hk, a.Hv,
+                                                            range_chunks);
+        if (N > 0 && need == 0) return GDN_ERR_SHAPE;
+        if (need > 0 && (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u)))
+            return GDN_ERR_WORKSPACE;
+        return gdn_host::launch_chunk_tc_cp(a, cu_seqlens_host, range_chunks, st);
+    }
+    if (tc) {
         const size_t need = gdn_host::chunk_tc_workspace(N, Q.T, a.Hk, a.Hv);
         if (need > 0 && (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u)))
             return GDN_ERR_WORKSPACE;
@@ -218,6 +232,27 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t *q, const gdn_tensor_t *k,
     return chunk_prefill_impl(q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, N, chunk,
                               scale, flags, initial_state, o, final_state, workspace,
                               workspace_bytes, status_dev, stream, nullptr);
+}
+
+size_t gdn_chunk_prefill_cp_workspace_size(const int32_t *cu_seqlens_host, int32_t N,
+                                           int64_t T, int32_t Hk, int32_t Hv, int32_t dk,
+                                           int32_t dv, int32_t chunk, int32_t range_chunks) {
+    if (!gdn_host::chunk_tc_supported(dk, dv, chunk, 0)) return 0;
+    return gdn_host::chunk_tc_cp_workspace(cu_seqlens_host, N, T, Hk, Hv, range_chunks);
+}
+
+gdn_status_t gdn_chunk_prefill_cp(const gdn_tensor_t *q, const gdn_tensor_t *k,
+                                  const gdn_tensor_t *v, const float *g, const float *beta,
+                                  const int32_t *cu_seqlens_dev,
+                                  const int32_t *cu_seqlens_host, int32_t N, int32_t chunk,
+                                  float scale, uint32_t flags, int32_t range_chunks,
+                                  const float *initial_state, const gdn_tensor_t *o,
+                                  float *final_state, void *workspace, size_t workspace_bytes,
+                                  int32_t *status_dev, void *stream) {
+    if (range_chunks <= 0) return GDN_ERR_SHAPE;
+    return chunk_prefill_impl(q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, N, chunk,
+                              scale, flags, initial_state, o, final_state, workspace,
+                              workspace_bytes, status_dev, stream, nullptr, range_chunks);
 }
 
 gdn_status_t gdn_recurrent_decode(const gdn_tensor_t *q, const gdn_tensor_t *k,

@@ -41,7 +41,9 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
+#include <cstring>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -75,7 +77,23 @@ struct TcParams {
     int l2norm;
     int ntiles;              // dv tiles per head in the state kernel: 2 or 3
     int32_t *status;
+    // Context-parallel passes over a batch split into chunk-aligned ranges (cp = 0: the
+    // plain scan, cu and h0/hT indexed by sequence).  cu then holds the ranges' bounds.
+    //   cp = 1: grid z = 2 n_ranges.  z < n_ranges: range z from its first state (the
+    //           sequence's initial state for a sequence's first range, else zero), end
+    //           state to sA (to hT when the range is the whole sequence), O only for first
+    //           ranges.  z >= n_ranges: the transition map of range z - n_ranges (V taken
+    //           as zero, start = I), to sP; first and last ranges need none.
+    //   cp = 2: grid z = n_ranges.  Every range but a first from its start state in sS,
+    //           O stored, a last range's end state to hT.
+    int cp;
+    int n_ranges;
+    const int32_t *rtab;     // per range: its sequence | first << 30 | last << 29
+    float *sA, *sP;
+    const float *sS;
 };
+
+constexpr int32_t kRangeFirst = 1 << 30, kRangeLast = 1 << 29, kRangeSeq = (1 << 29) - 1;
 
 __device__ __forceinline__ uint64_t now_ns() {
     uint64_t t;
@@ -562,15 +580,16 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity) {
 
 __device__ __forceinline__ void issue_chunk_loads(StateSmem &S, const TcMaps &maps,
                                                   const TcParams &p, int stage, int t0,
-                                                  int hk, int hv, int j0, int slot) {
+                                                  int hk, int hv, int j0, int slot,
+                                                  bool with_v) {
     uint64_t *bar = &S.bar_tma[stage];
-    tc::mbar_expect_tx(bar, 32768 + 8192 + kWsTile);
+    tc::mbar_expect_tx(bar, 32768 + (with_v ? 8192 : 0) + kWsTile);
     uint8_t *kq = S.kq[stage];
     tc::tma_load_3d(kq + 0, &maps.k, bar, 0, hk, t0);
     tc::tma_load_3d(kq + 16384, &maps.k, bar, 64, hk, t0);
     tc::tma_load_3d(kq + 8192, &maps.q, bar, 0, hk, t0);
     tc::tma_load_3d(kq + 16384 + 8192, &maps.q, bar, 64, hk, t0);
-    tc::tma_load_3d(S.v[stage], &maps.v, bar, j0, hv, t0);
+    if (with_v) tc::tma_load_3d(S.v[stage], &maps.v, bar, j0, hv, t0);
     const uint8_t *src = p.ws + ((size_t)slot * p.Hv + hv) * kWsTile;
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  :: "r"(tc::smem_u32(S.x[stage])), "l"(src), "r"(kWsTile),
@@ -634,17 +653,31 @@ __device__ __forceinline__ void out_barrier() {
 // Operand tiles are 64 columns wide in shared memory whatever NT is; an NT-wide MMA reads
 // only the first NT columns.  [hi | lo] is one 2 NT-wide MN-major operand whose 64-column
 // blocks are S.dvh and S.dvl.
+// What one state CTA computes: the chunks of entry n of p.cu (a sequence, or a range of
+// one) for one v-head, from a start state, optionally without V, storing O and/or the
+// end state.
+struct StateJob {
+    int n;
+    bool active;             // false: nothing to do (no chunks, no stores)
+    bool identity;           // start from I (dk = dv) instead of h0
+    bool with_v;             // false: V is taken as zero and its tiles are not loaded
+    bool write_o;            // store the chunk outputs
+    const float *h0;         // this head's start state [dk][dv], or null for zero
+    float *hT;               // this head's end state [dk][dv], or null
+};
+
 template <int NT>
 __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, const TcParams &p,
-                                          const CUtensorMap *omap, int j0, int hv, int n) {
+                                          const CUtensorMap *omap, int j0, int hv,
+                                          const StateJob &job) {
+    const int n = job.n;
     constexpr int NC = NT / 2;               // columns per thread
     constexpr int NCH = NC / 8;              // 16-byte chunks per thread row
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hk = hv / (p.Hv / p.Hk);
-    const int start = p.cu[n], len = p.cu[n + 1] - start;
+    const int start = p.cu[n], len = job.active ? p.cu[n + 1] - start : 0;
     const int nch = (len + kC - 1) / kC;
     const int s0 = slot0(p.cu, n);
-    const size_t hoff = ((size_t)n * p.Hv + hv) * kD * kD;
     const uint32_t tmem = S.tmem;
     // TMEM columns: D1 [K;Q]h, D2 [Lo;Mt]R, and the state update as a hi | lo pair
     const uint32_t colD1 = 0, colD2 = 64, colS = 128;
@@ -726,7 +759,7 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
         int issued = 0;                                        // chunks 0..issued-1 are loaded
         if (leader) {
             for (int c = 0; c < 2 && c < nch; ++c) {
-                issue_chunk_loads(S, maps, p, c, start + c * kC, hk, hv, j0, s0 + c);
+                issue_chunk_loads(S, maps, p, c, start + c * kC, hk, hv, j0, s0 + c, job.with_v);
                 issued = c + 1;
             }
         }
@@ -735,7 +768,7 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
             __syncthreads();                                   // h published as bf16
             if (leader && c >= 1 && c + 1 < nch && !*abort) {
                 issue_chunk_loads(S, maps, p, (c + 1) & 1, start + (c + 1) * kC, hk, hv, j0,
-                                  s0 + c + 1);
+                                  s0 + c + 1, job.with_v);
                 issued = c + 2;
             }
         }
@@ -763,8 +796,11 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
 
     // fp32 master state in registers: dk row `row`, dv columns j0+ch .. +NC-1.
     float h[NC];
-    if (p.h0) {
-        const float4 *src = reinterpret_cast<const float4 *>(p.h0 + hoff + (size_t)row * kD + j0 + ch);
+    if (job.identity) {
+#pragma unroll
+        for (int i = 0; i < NC; ++i) h[i] = row == j0 + (int)ch + i ? 1.f : 0.f;
+    } else if (job.h0) {
+        const float4 *src = reinterpret_cast<const float4 *>(job.h0 + (size_t)row * kD + j0 + ch);
 #pragma unroll
         for (int i = 0; i < NC / 4; ++i) {
             const float4 f = src[i];
@@ -815,7 +851,8 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
         if (chain) {
 #pragma unroll
             for (int cc = 0; cc < NCH; ++cc)
-                vraw[cc] = *reinterpret_cast<const uint4 *>(S.v[st] + tc::swz(r, c0 + cc));
+                vraw[cc] = job.with_v ? *reinterpret_cast<const uint4 *>(S.v[st] + tc::swz(r, c0 + cc))
+                                      : make_uint4(0u, 0u, 0u, 0u);
         }
 
         // --- B: R = beta (V - e^gamma nk K h) on the chain rows; e^gamma nq Q h on the rest
@@ -912,6 +949,8 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
                 tc::fence_async_smem();
                 tc::fence_before_sync();
                 chain_barrier();
+            } else if (!job.write_o) {
+                // no outputs from this CTA
             } else if (L == kC) {
                 // A full chunk's O tile goes out through shared memory with one tensor store,
                 // keeping 64 scattered row writes per warp off the load/store pipeline that
@@ -962,8 +1001,8 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
     if (tid == kOutLeader) tc::bulk_wait_all();   // O tiles written before the CTA exits
     tc::fence_before_sync();
     __syncthreads();
-    if (!*abort && p.hT) {
-        float4 *dst = reinterpret_cast<float4 *>(p.hT + hoff + (size_t)row * kD + j0 + ch);
+    if (!*abort && job.hT) {
+        float4 *dst = reinterpret_cast<float4 *>(job.hT + (size_t)row * kD + j0 + ch);
 #pragma unroll
         for (int i = 0; i < NC / 4; ++i)
             dst[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
@@ -1006,12 +1045,133 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    const size_t hd = (size_t)kD * kD;                  // one head's state
+    StateJob job;
+    job.identity = false;
+    job.with_v = true;
+    job.write_o = true;
+    job.active = true;
+    if (p.cp == 0) {
+        job.n = n;
+        job.h0 = p.h0 ? p.h0 + ((size_t)n * p.Hv + hv) * hd : nullptr;
+        job.hT = p.hT ? p.hT + ((size_t)n * p.Hv + hv) * hd : nullptr;
+    } else {
+        const bool trans = p.cp == 1 && n >= p.n_ranges;
+        const int rr = trans ? n - p.n_ranges : n;
+        const int32_t t = p.rtab[rr];
+        const int seq = t & kRangeSeq;
+        const bool first = (t & kRangeFirst) != 0, last = (t & kRangeLast) != 0;
+        float *hT_seq = p.hT ? p.hT + ((size_t)seq * p.Hv + hv) * hd : nullptr;
+        const size_t roff = ((size_t)rr * p.Hv + hv) * hd;
+        job.n = rr;
+        job.h0 = nullptr;
+        job.hT = nullptr;
+        if (p.cp == 1 && !trans) {
+            job.h0 = first && p.h0 ? p.h0 + ((size_t)seq * p.Hv + hv) * hd : nullptr;
+            job.hT = first && last ? hT_seq : p.sA + roff;
+            job.write_o = first;
+        } else if (p.cp == 1) {
+            job.active = !first && !last;
+            job.identity = true;
+            job.with_v = false;
+            job.write_o = false;
+            job.hT = job.active ? p.sP + roff : nullptr;
+        } else {
+            job.active = !first;
+            job.h0 = job.active ? p.sS + roff : nullptr;
+            job.hT = job.active && last ? hT_seq : nullptr;
+        }
+    }
     if (p.ntiles != 3)
-        state_cta<64>(S, maps, p, &maps.o, 64 * jt, hv, n);
+        state_cta<64>(S, maps, p, &maps.o, 64 * jt, hv, job);
     else if (jt < 2)
-        state_cta<48>(S, maps, p, &maps.o48, 48 * jt, hv, n);
+        state_cta<48>(S, maps, p, &maps.o48, 48 * jt, hv, job);
     else
-        state_cta<32>(S, maps, p, &maps.o32, 96, hv, n);
+        state_cta<32>(S, maps, p, &maps.o32, 96, hv, job);
+}
+
+// ====================================================== context-parallel composition
+// A sequence split into chunk-aligned ranges: each range's end state is an affine map of
+// its start state, h_end = P h_start + R (h in the [dk][dv] layout, P dk x dk), since
+// every token's update h <- e^g (I - beta k k^T) h + beta k v^T is affine in h.  The
+// first state pass gives R (start 0) and P (start I, V = 0) for every range; the start
+// states follow in order, S_{r+1} = P_r S_r + R_r; the second pass reruns each range from
+// its start.
+
+// The split batch's tables, from the device copy of cu: range bounds, per range its
+// sequence and first / last flags, and each sequence's first range.  One thread, in
+// order; a range count that disagrees with the host's (a device cu that differs from the
+// host copy) stops the tables and reports GDN_ERR_SEQLENS.
+__global__ void cp_tables_kernel(const int32_t *cu, int N, int range_chunks, int n_ranges,
+                                 int32_t *cu_split, int32_t *rtab, int32_t *seq_first,
+                                 int32_t *status) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    int idx = 0;
+    for (int n = 0; n < N; ++n) {
+        const int start = cu[n], len = cu[n + 1] - start;
+        const int nch = (len + kC - 1) / kC;
+        const int R = max(1, (nch + range_chunks - 1) / range_chunks);
+        seq_first[n] = idx;
+        for (int r = 0; r < R; ++r) {
+            if (idx >= n_ranges) {
+                report(status, GDN_ERR_SEQLENS);
+                return;
+            }
+            cu_split[idx] = start + (int)min((int64_t)r * range_chunks * kC, (int64_t)len);
+            rtab[idx] = n | (r == 0 ? kRangeFirst : 0) | (r == R - 1 ? kRangeLast : 0);
+            ++idx;
+        }
+    }
+    if (idx != n_ranges) report(status, GDN_ERR_SEQLENS);
+    cu_split[n_ranges] = cu[N];
+}
+
+// Start states of a sequence's ranges, in order: one CTA per (16 dv columns, v-head,
+// sequence), one thread per dk row.  S = the first range's end state; for each later
+// range r: its start is S, then S <- P_r S + R_r (fp32, k in increasing order).
+constexpr int kComposeCols = 16;
+constexpr int kComposeLd = kD + 1;          // padded P rows: thread i reads row i
+constexpr size_t kComposeSmem = (size_t)kD * kComposeLd * 4 + (size_t)kD * kComposeCols * 4;
+__global__ void __launch_bounds__(kD)
+cp_compose_kernel(const float *sA, const float *sP, float *sS, const int32_t *seq_first,
+                  int N, int Hv, int n_ranges) {
+    extern __shared__ float csm[];
+    float (*Psm)[kComposeLd] = reinterpret_cast<float (*)[kComposeLd]>(csm);
+    float (*Ssm)[kComposeCols] = reinterpret_cast<float (*)[kComposeCols]>(csm + kD * kComposeLd);
+    grid_dependents_launch();
+    grid_dependency_wait();
+    const int j0 = blockIdx.x * kComposeCols, hv = blockIdx.y, n = blockIdx.z;
+    const int i = threadIdx.x;
+    const int first = seq_first[n];
+    const int R = (n + 1 < N ? seq_first[n + 1] : n_ranges) - first;
+    if (R <= 1) return;
+    const size_t hd = (size_t)kD * kD;
+    auto head = [&](const float *base, int range) { return base + ((size_t)range * Hv + hv) * hd; };
+#pragma unroll
+    for (int j = 0; j < kComposeCols; ++j) Ssm[i][j] = head(sA, first)[(size_t)i * kD + j0 + j];
+    for (int r = 1; r < R; ++r) {
+        const int idx = first + r;
+        float *dst = const_cast<float *>(head(sS, idx)) + (size_t)i * kD + j0;
+#pragma unroll
+        for (int j = 0; j < kComposeCols; ++j) dst[j] = Ssm[i][j];
+        if (r == R - 1) break;
+        const float *P = head(sP, idx);
+        for (int e = i; e < kD * kD; e += kD) Psm[e / kD][e % kD] = P[e];
+        float acc[kComposeCols];
+        const float *Rr = head(sA, idx) + (size_t)i * kD + j0;
+#pragma unroll
+        for (int j = 0; j < kComposeCols; ++j) acc[j] = Rr[j];
+        __syncthreads();
+        for (int k = 0; k < kD; ++k) {
+            const float pk = Psm[i][k];
+#pragma unroll
+            for (int j = 0; j < kComposeCols; ++j) acc[j] = fmaf(pk, Ssm[k][j], acc[j]);
+        }
+        __syncthreads();                       // every read of S and P is done
+#pragma unroll
+        for (int j = 0; j < kComposeCols; ++j) Ssm[i][j] = acc[j];
+        __syncthreads();
+    }
 }
 
 // Self-test of the bounded waits: one CTA waits, with the helper the kernels above use,
@@ -1087,18 +1247,19 @@ gdn_status_t launch_wait_selftest(int32_t *status, cudaStream_t st) {
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStream_t st,
-                             cudaEvent_t before_state) {
-    (void)cu_host;
-    if (a.N == 0) return GDN_OK;
-    if (a.out_f32) return GDN_ERR_DTYPE;
-    gdn::TcMaps maps;
+namespace {
+
+// Tensor maps, kernel parameters and the one-time per-device kernel attributes shared by
+// the plain and the context-parallel scans.  n_chains: CTAs per (head, dv tile) of the
+// state pass, for the tiling choice.
+gdn_status_t setup_scan(const ScanArgs &a, int64_t n_chains, gdn::TcMaps &maps,
+                        gdn::TcParams &p, size_t &prep_smem, size_t &state_smem) {
     if (!make_map(&maps.q, a.q, a.T, a.Hk, a.q_tok) || !make_map(&maps.k, a.k, a.T, a.Hk, a.k_tok) ||
         !make_map(&maps.v, a.v, a.T, a.Hv, a.v_tok) || !make_map(&maps.o, a.o, a.T, a.Hv, a.o_tok) ||
         !make_map(&maps.o48, a.o, a.T, a.Hv, a.o_tok, 48) ||
         !make_map(&maps.o32, a.o, a.T, a.Hv, a.o_tok, 32))
         return GDN_ERR_CUDA;
-    gdn::TcParams p;
+    memset(&p, 0, sizeof(p));
     p.g = a.g;
     p.beta = a.beta;
     p.cu = a.cu;
@@ -1114,18 +1275,21 @@ gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStre
     p.l2norm = (a.flags & GDN_QK_L2NORM) ? 1 : 0;
     p.status = a.status;
     // Three dv tiles per head (48 + 48 + 32 columns) when they still fit one wave on the
-    // SMs, else two of 64: the tiling changes how the columns are grouped, not the
-    // arithmetic of any column.
+    // SMs, else two of 64.  So the tiling follows N and the device's SM count; it changes
+    // how the columns are grouped, not the arithmetic of any column (every column's
+    // products, reductions and roundings are the same whatever tile it sits in), which
+    // keeps a sequence's bits the same alone and in a batch.  GDN_PREFILL_TILES2/3 force
+    // one tiling; the GPU tests run the same sequences under both and compare the bits.
     const int sms = sm_count();
     if (a.flags & GDN_PREFILL_TILES2)
         p.ntiles = 2;
     else if (a.flags & GDN_PREFILL_TILES3)
         p.ntiles = 3;
     else
-        p.ntiles = (sms > 0 && (int64_t)3 * a.Hv * a.N <= sms) ? 3 : 2;
+        p.ntiles = (sms > 0 && (int64_t)3 * a.Hv * n_chains <= sms) ? 3 : 2;
 
-    const size_t prep_smem = sizeof(gdn::PrepSmem) + 1024;
-    const size_t state_smem = sizeof(gdn::StateSmem) + 1024;
+    prep_smem = sizeof(gdn::PrepSmem) + 1024;
+    state_smem = sizeof(gdn::StateSmem) + 1024;
     // the shared-memory opt-in is a per-device attribute: set it once on each device
     static std::atomic<bool> attr_set[kMaxDevices];
     int dev = 0;
@@ -1137,24 +1301,131 @@ gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStre
             cudaFuncSetAttribute(gdn::chunk_prep_kernel,
                                  cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess ||
             cudaFuncSetAttribute(gdn::chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)state_smem) != cudaSuccess)
+                                 (int)state_smem) != cudaSuccess ||
+            cudaFuncSetAttribute(gdn::cp_compose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)gdn::kComposeSmem) != cudaSuccess)
             return GDN_ERR_CUDA;
         attr_set[dev].store(true, std::memory_order_release);
     }
-    const int slots = (int)((a.T + gdn::kC - 1) / gdn::kC) + a.N;
-    if (slots > 0) {
-        dim3 g1(slots, a.Hv);
-        if (launch_dependent(gdn::chunk_prep_kernel, g1, dim3(gdn::kPrepThreads), prep_smem, st,
-                             maps, p) != cudaSuccess)
-            return GDN_ERR_CUDA;
+    return GDN_OK;
+}
+
+gdn_status_t launch_prep(const gdn::TcMaps &maps, const gdn::TcParams &p, int64_t T,
+                         size_t prep_smem, cudaStream_t st) {
+    const int slots = (int)((T + gdn::kC - 1) / gdn::kC) + p.N;
+    if (slots <= 0) return GDN_OK;
+    dim3 g1(slots, p.Hv);
+    return launch_dependent(gdn::chunk_prep_kernel, g1, dim3(gdn::kPrepThreads), prep_smem, st,
+                            maps, p) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status_t launch_state(const gdn::TcMaps &maps, const gdn::TcParams &p, int grid_z,
+                          size_t state_smem, cudaStream_t st) {
+    dim3 g2(p.ntiles, p.Hv, grid_z);
+    return launch_dependent(gdn::chunk_state_kernel, g2, dim3(gdn::kStateThreads), state_smem,
+                            st, maps, p) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+// Ranges of the context-parallel split: ceil(chunks / range_chunks) per sequence, at
+// least one (an empty sequence is one empty range).  -1 when the count exceeds the
+// launch limits.
+int64_t cp_range_count(const int32_t *cu_host, int32_t N, int32_t range_chunks) {
+    int64_t nr = 0;
+    for (int32_t n = 0; n < N; ++n) {
+        const int64_t len = (int64_t)cu_host[n + 1] - cu_host[n];
+        const int64_t nch = (len + gdn::kC - 1) / gdn::kC;
+        nr += std::max<int64_t>(1, (nch + range_chunks - 1) / range_chunks);
     }
+    return 2 * nr > 65535 ? -1 : nr;
+}
+
+constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct CpLayout {
+    size_t tiles, sA, sP, sS, cu_split, rtab, seq_first, total;
+};
+
+CpLayout cp_layout(int64_t nr, int32_t N, int64_t T, int32_t Hk, int32_t Hv) {
+    CpLayout L;
+    const size_t states = (size_t)nr * Hv * gdn::kD * gdn::kD * sizeof(float);
+    L.tiles = 0;
+    L.sA = align256(chunk_tc_workspace((int32_t)nr, T, Hk, Hv));
+    L.sP = L.sA + align256(states);
+    L.sS = L.sP + align256(states);
+    L.cu_split = L.sS + align256(states);
+    L.rtab = L.cu_split + align256((size_t)(nr + 1) * sizeof(int32_t));
+    L.seq_first = L.rtab + align256((size_t)nr * sizeof(int32_t));
+    L.total = L.seq_first + align256((size_t)N * sizeof(int32_t));
+    return L;
+}
+
+}  // namespace
+
+size_t chunk_tc_cp_workspace(const int32_t *cu_host, int32_t N, int64_t T, int32_t Hk,
+                             int32_t Hv, int32_t range_chunks) {
+    if (!cu_host || N <= 0 || range_chunks <= 0) return 0;
+    const int64_t nr = cp_range_count(cu_host, N, range_chunks);
+    if (nr < 0) return 0;
+    return cp_layout(nr, N, T, Hk, Hv).total;
+}
+
+gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStream_t st,
+                             cudaEvent_t before_state) {
+    (void)cu_host;
+    if (a.N == 0) return GDN_OK;
+    if (a.out_f32) return GDN_ERR_DTYPE;
+    gdn::TcMaps maps;
+    gdn::TcParams p;
+    size_t prep_smem = 0, state_smem = 0;
+    gdn_status_t s = setup_scan(a, a.N, maps, p, prep_smem, state_smem);
+    if (s != GDN_OK) return s;
+    if ((s = launch_prep(maps, p, a.T, prep_smem, st)) != GDN_OK) return s;
     if (before_state && cudaStreamWaitEvent(st, before_state, 0) != cudaSuccess)
         return GDN_ERR_CUDA;
-    dim3 g2(p.ntiles, a.Hv, a.N);
-    if (launch_dependent(gdn::chunk_state_kernel, g2, dim3(gdn::kStateThreads), state_smem, st,
-                         maps, p) != cudaSuccess)
+    return launch_state(maps, p, a.N, state_smem, st);
+}
+
+gdn_status_t launch_chunk_tc_cp(const ScanArgs &a, const int32_t *cu_host, int32_t range_chunks,
+                                cudaStream_t st) {
+    if (a.N == 0) return GDN_OK;
+    if (a.out_f32) return GDN_ERR_DTYPE;
+    if (range_chunks <= 0) return GDN_ERR_SHAPE;
+    const int64_t nr = cp_range_count(cu_host, a.N, range_chunks);
+    if (nr < 0) return GDN_ERR_SHAPE;
+    const CpLayout L = cp_layout(nr, a.N, a.T, a.Hk, a.Hv);
+    uint8_t *ws = (uint8_t *)a.ws;
+    float *sA = (float *)(ws + L.sA), *sP = (float *)(ws + L.sP), *sS = (float *)(ws + L.sS);
+    int32_t *cu_split = (int32_t *)(ws + L.cu_split), *rtab = (int32_t *)(ws + L.rtab);
+    int32_t *seq_first = (int32_t *)(ws + L.seq_first);
+
+    gdn::cp_tables_kernel<<<1, 32, 0, st>>>(a.cu, a.N, range_chunks, (int)nr, cu_split, rtab,
+                                            seq_first, a.status);
+    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+
+    ScanArgs split = a;
+    split.cu = cu_split;
+    split.N = (int32_t)nr;
+    gdn::TcMaps maps;
+    gdn::TcParams p;
+    size_t prep_smem = 0, state_smem = 0;
+    gdn_status_t s = setup_scan(split, 2 * nr, maps, p, prep_smem, state_smem);
+    if (s != GDN_OK) return s;
+    p.rtab = rtab;
+    p.n_ranges = (int)nr;
+    p.sA = sA;
+    p.sP = sP;
+    p.sS = sS;
+    // the workspace tiles depend only on q, k, g and beta: one prep pass serves both passes
+    if ((s = launch_prep(maps, p, a.T, prep_smem, st)) != GDN_OK) return s;
+    p.cp = 1;
+    if ((s = launch_state(maps, p, (int)(2 * nr), state_smem, st)) != GDN_OK) return s;
+    if (launch_dependent(gdn::cp_compose_kernel, dim3(gdn::kD / gdn::kComposeCols, a.Hv, a.N),
+                         dim3(gdn::kD), gdn::kComposeSmem, st, (const float *)sA,
+                         (const float *)sP, sS, (const int32_t *)seq_first, (int)a.N, (int)a.Hv,
+                         (int)nr) != cudaSuccess)
         return GDN_ERR_CUDA;
-    return GDN_OK;
+    p.cp = 2;
+    return launch_state(maps, p, (int)nr, state_smem, st);
 }
 
 }  // namespace gdn_host

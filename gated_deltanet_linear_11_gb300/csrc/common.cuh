@@ -114,6 +114,12 @@ gdn_status_t launch_chunk_simt(const ScanArgs &a, cudaStream_t st);
 gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStream_t st,
                              cudaEvent_t before_state = nullptr);
 size_t chunk_tc_workspace(int32_t N, int64_t T, int32_t Hk, int32_t Hv);
+// The context-parallel scan: each sequence in ranges of range_chunks chunks (cu_host: the
+// host copy of cu).  Workspace bytes (0 when the arguments are invalid) and the launch.
+size_t chunk_tc_cp_workspace(const int32_t *cu_host, int32_t N, int64_t T, int32_t Hk,
+                             int32_t Hv, int32_t range_chunks);
+gdn_status_t launch_chunk_tc_cp(const ScanArgs &a, const int32_t *cu_host, int32_t range_chunks,
+                                cudaStream_t st);
 // one CTA whose bounded mbarrier wait runs out (GDN_ERR_TIMEOUT into *status)
 gdn_status_t launch_wait_selftest(int32_t *status, cudaStream_t st);
 bool chunk_tc_supported(int32_t dk, int32_t dv, int32_t chunk, int in_f32);

@@ -160,6 +160,45 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t *q, const gdn_tensor_t *k,
                                size_t workspace_bytes, int32_t *status_dev, void *stream);
 
 /*
+ * gdn_chunk_prefill_cp -- gdn_chunk_prefill with each sequence split into ranges of
+ * range_chunks chunks (64 tokens each) that run side by side: a context-parallel scan
+ * for long sequences whose heads alone leave SMs idle.
+ * Sources: the recurrence of gdn_chunk_prefill ("Qwen3.5-27B GPTQ Garbage Inference --
+ * Root Cause Analysis", "Why abliteration failed on Qwen3.5", item 3).  The per-token
+ * update h <- e^g (I - beta k k^T) h + beta k v^T is affine in the state, so a range's end
+ * state is P h_start + R; "[Feature] Add batch invariance support to GDN_ATTN backend -
+ * #45819" (its commit adding use_cp=False) records that a context-parallel variant chosen
+ * by batch composition breaks batch invariance, so here the split is the caller's
+ * explicit choice and depends only on each sequence's own length.
+ * Method: one prep pass over the ranges; a state pass that gives every range's end state
+ * from its first state (the sequence's initial state for a first range, zero otherwise)
+ * and every middle range's P (V taken as zero, start = identity); the start states in
+ * order (S_{r+1} = P_r S_r + R_r, fp32); a second state pass from those starts, which
+ * writes o and the final states.  A sequence of at most range_chunks chunks is one range
+ * and gives exactly the bits of gdn_chunk_prefill.  Longer ones match the oracle within
+ * the same tolerances but are not bit-identical to gdn_chunk_prefill (the starts come
+ * from composed maps); they are bit-identical alone and in any batch, for a given
+ * range_chunks.
+ * Arguments are those of gdn_chunk_prefill plus range_chunks >= 1; the tensor-core path
+ * only (bf16, dk = dv = 128, chunk 64), else GDN_ERR_UNSUPPORTED.  workspace: device
+ * scratch of gdn_chunk_prefill_cp_workspace_size() bytes, 256-byte aligned.  A device
+ * cu_seqlens that disagrees with the host copy is reported in *status_dev as
+ * GDN_ERR_SEQLENS.
+ */
+size_t gdn_chunk_prefill_cp_workspace_size(const int32_t *cu_seqlens_host, int32_t N,
+                                           int64_t T, int32_t Hk, int32_t Hv, int32_t dk,
+                                           int32_t dv, int32_t chunk, int32_t range_chunks);
+
+gdn_status_t gdn_chunk_prefill_cp(const gdn_tensor_t *q, const gdn_tensor_t *k,
+                                  const gdn_tensor_t *v, const float *g, const float *beta,
+                                  const int32_t *cu_seqlens_dev,
+                                  const int32_t *cu_seqlens_host, int32_t N, int32_t chunk,
+                                  float scale, uint32_t flags, int32_t range_chunks,
+                                  const float *initial_state, const gdn_tensor_t *o,
+                                  float *final_state, void *workspace, size_t workspace_bytes,
+                                  int32_t *status_dev, void *stream);
+
+/*
  * gdn_chunk_prefill_noalloc -- gdn_chunk_prefill without a caller-provided workspace.
  * The pages have no counterpart to this entry point; it exists for callers that cannot
  * call cudaMalloc (an engine whose allocator owns all device memory, a latency-critical

@@ -182,6 +182,52 @@ def test_workspace_size(lib):
         assert f(N, T, 16, Hv, 128, 128, 64, 0) == (-(-T // 64) + N + 1) * Hv * tile
 
 
+def cp_prefill(lib, q, k, v, o, cu, N, range_chunks, ws=None, ws_bytes=0):
+    cu_arr = (ctypes.c_int32 * len(cu))(*cu)
+    return lib.gdn_chunk_prefill_cp(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v),
+                                    FAKE, FAKE, FAKE, ctypes.cast(cu_arr, ctypes.c_void_p),
+                                    N, 64, 1.0, 0, range_chunks, None, ctypes.byref(o), None,
+                                    ws, ws_bytes, None, None)
+
+
+@no_gpu
+def test_cp_workspace_size(lib):
+    """The context-parallel scan's scratch: the workspace tiles of the split batch (one
+    range per range_chunks chunks of each sequence, at least one), then three
+    [ranges, Hv, dk, dv] fp32 state arrays (end states from the first pass, transition
+    maps, composed start states) and three int32 tables, each 256-byte aligned."""
+    f = lib.gdn_chunk_prefill_cp_workspace_size
+    lens = [700, 64, 1, 300, 129, 0]
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    cu_arr = (ctypes.c_int32 * len(cu))(*cu)
+    cup = ctypes.cast(cu_arr, ctypes.c_void_p)
+    T, N, Hv = cu[-1], len(lens), 6
+
+    def a256(x):
+        return (x + 255) // 256 * 256
+    for rc in (1, 2, 5, 100):
+        nr = sum(max(1, -(-(-(-n // 64)) // rc)) for n in lens)
+        tiles = (-(-T // 64) + nr + 1) * Hv * (128 * 64 * 2 + 4 * 64 * 4)
+        want = (a256(tiles) + 3 * a256(nr * Hv * 128 * 128 * 4) + a256((nr + 1) * 4) +
+                a256(nr * 4) + a256(N * 4))
+        assert f(cup, N, T, 2, Hv, 128, 128, 64, rc) == want, rc
+    assert f(cup, N, T, 2, Hv, 128, 128, 64, 0) == 0       # no range length
+    assert f(cup, N, T, 2, Hv, 64, 64, 64, 2) == 0         # not a tensor-core shape
+
+
+@no_gpu
+def test_cp_rejections(lib):
+    q, k, v, o = desc(8, 2, 128), desc(8, 2, 128), desc(8, 2, 128), desc(8, 2, 128)
+    assert cp_prefill(lib, q, k, v, o, [0, 8], 1, 0) == 2     # range_chunks < 1
+    assert cp_prefill(lib, q, k, v, o, [0, 8], 1, 2) == 9     # no workspace
+    f32 = [desc(8, 2, 128, dtype=_lib.GDN_F32) for _ in range(4)]
+    assert cp_prefill(lib, *f32, [0, 8], 1, 2) == 6           # CUDA-core shapes only
+    qh = desc(8, 2, 128, stride=(128, 8 * 128, 1))            # head-first
+    assert cp_prefill(lib, qh, k, v, o, [0, 8], 1, 2) == 3
+
+
 def test_selftest_needs_a_status_word(lib):
     assert lib.gdn_selftest_bounded_wait(None, None) == 1   # GDN_ERR_NULL, nothing launched
 

@@ -218,6 +218,37 @@ def test_split_and_carry_invariance():
     np.testing.assert_allclose(he, hT, atol=1e-12)
 
 
+def test_range_end_state_is_affine_in_start_state():
+    """The context-parallel scan's composition: each token's update
+    h <- e^g (I - beta k k^T) h + beta k v^T is affine in the [dk][dv] state, so a range's
+    end state is P h_start + R, with P the end state from the identity with V = 0 and R
+    the end state from zero; two ranges compose as P2 (P1 S + R1) + R2.  Checked on the
+    recurrence itself (the batch-invariance PR's use_cp commit names the variant)."""
+    dk = dv = 6
+    q, k, v, g, beta, cu, h0 = rand_case(31, [17, 11], 1, 2, dk, dv, unit_k=True)
+    N, Hv = 2, 2
+    eye = np.broadcast_to(np.eye(dk), (N, Hv, dk, dk)).copy()
+    _, P = oracle.gated_delta_rule(q, k, np.zeros_like(v), g, beta, cu, initial_state=eye)
+    _, R = oracle.gated_delta_rule(q, k, v, g, beta, cu, initial_state=np.zeros_like(h0))
+    _, hT = oracle.gated_delta_rule(q, k, v, g, beta, cu, initial_state=h0)
+    np.testing.assert_allclose(hT, np.einsum("nhik,nhkj->nhij", P, h0) + R, atol=1e-12)
+    # two ranges of the first sequence, [0, 7) and [7, 17), composed
+    tau = 7
+    sl = lambda a, lo, hi: a[lo:hi]  # noqa: E731
+    parts = []
+    for lo, hi in ((0, tau), (tau, 17)):
+        args = [sl(a, lo, hi) for a in (q, k, v, g, beta)]
+        _, Pr = oracle.gated_delta_rule(args[0], args[1], np.zeros_like(args[2]), args[3],
+                                        args[4], [0, hi - lo], initial_state=eye[:1])
+        _, Rr = oracle.gated_delta_rule(*args, [0, hi - lo],
+                                        initial_state=np.zeros_like(h0[:1]))
+        parts.append((Pr, Rr))
+    S = h0[:1]
+    for Pr, Rr in parts:
+        S = np.einsum("nhik,nhkj->nhij", Pr, S) + Rr
+    np.testing.assert_allclose(S, hT[:1], atol=1e-12)
+
+
 def test_contraction_bound():
     """Unit k, beta in (0,1], g <= 0: ||I - beta k k^T||_2 = 1, so
     ||S_t||_2 <= e^{g_t} ||S_{t-1}||_2 + beta_t ||v_t||."""
