@@ -447,9 +447,14 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
                 float pv[32];
                 tmem_row32(tmem + lane_off + colP + 32 * hf, pv);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
+                for (int i = 0; i < 32; i += 4) {
                     const int s = 32 * hf + i;
-                    v[i] = (s < lim && r < L) ? rowf * pv[i] * fast_exp2(g2r - S.c2[s]) : 0.f;
+                    const float4 c4 = *reinterpret_cast<const float4 *>(&S.c2[s]);
+                    const float e[4] = {fast_exp2(g2r - c4.x), fast_exp2(g2r - c4.y),
+                                        fast_exp2(g2r - c4.z), fast_exp2(g2r - c4.w)};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        v[i + u] = (s + u < lim && r < L) ? rowf * pv[i + u] * e[u] : 0.f;
                 }
             }
             if (arow) {
