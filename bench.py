@@ -259,11 +259,13 @@ def run_ours(args, world, rank, local):
     if "prefill" in legs:
         # (1) the step: one gdn_layer_prefill call (conv over q|k|v, then the chunk scan;
         #     the v channels' conv runs on the caller's side stream under the chunk
-        #     preparation), timed as a whole
-        def layer_step():
+        #     preparation), timed as a whole; also timed with the v channels' conv fused
+        #     into the state pass (GDN_LAYER_FUSED_VCONV), for the record
+        def layer_step(fused=False):
             gdn.gdn_layer_prefill(x, w, None, g, beta, cu, s["Hk"], s["Hv"], s["dk"], s["dv"],
                                   conv_state_out=conv_out, o=o, final_state=hT, y=y,
-                                  cu_seqlens_host=cu_h, workspace=ws, side_stream=side)
+                                  cu_seqlens_host=cu_h, workspace=ws,
+                                  side_stream=None if fused else side, fused_vconv=fused)
 
         # (2) the same work as two calls, each bracketed, for the per-kernel roofline
         def component_step(evs):
@@ -296,6 +298,19 @@ def run_ours(args, world, rank, local):
         launches += args.steps * (2 + scan_launches)
         ms_step = max_over_ranks(statistics.mean(step_ms), world)
         value = world * T / (ms_step * 1e-3)
+
+        for _ in range(args.warmup):
+            flush_l2()
+            layer_step(True)
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush_l2()
+            sevs[i][0].record(stream)
+            layer_step(True)
+            sevs[i][1].record(stream)
+        torch.cuda.synchronize()
+        launches += args.steps * (1 + scan_launches)
+        vconv_fused_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in sevs)
 
         for _ in range(args.warmup):
             flush_l2()
@@ -505,7 +520,8 @@ def run_ours(args, world, rank, local):
     }
     if "prefill" in legs:
         result["kernels_ms"] = {"conv1d_fwd": conv_avg, "chunk_prefill": scan_avg,
-                                "conv_plus_chunk_as_two_calls": conv_avg + scan_avg}
+                                "conv_plus_chunk_as_two_calls": conv_avg + scan_avg,
+                                "layer_v_conv_fused_into_state_pass": vconv_fused_ms}
         result["roofline"] = {
             "kernel": "chunk_prefill", "bound": "tensor", "achieved": achieved_tf,
             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",

@@ -24,8 +24,8 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (GDN_PREFILL_SIMT, GDN_PREFILL_TILES2, GDN_PREFILL_TILES3,  # noqa: F401
-                   GDN_QK_L2NORM, GdnError)
+from ._lib import (GDN_LAYER_FUSED_VCONV, GDN_PREFILL_SIMT, GDN_PREFILL_TILES2,  # noqa: F401
+                   GDN_PREFILL_TILES3, GDN_QK_L2NORM, GdnError)
 
 __all__ = ["gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
            "gdn_chunk_prefill_noalloc", "gdn_chunk_prefill_cp",
@@ -297,12 +297,14 @@ def split_qkv(y, Hk, Hv, dk, dv):
 def gdn_layer_prefill(x_qkv, conv_w, conv_bias, g, beta, cu_seqlens, Hk, Hv, dk, dv,
                       conv_state_in=None, conv_state_out=None, initial_state=None,
                       final_state=None, scale=1.0, chunk=64, l2norm=True, y=None, o=None,
-                      cu_seqlens_host=None, workspace=None, status=None, side_stream=None):
+                      cu_seqlens_host=None, workspace=None, status=None, side_stream=None,
+                      fused_vconv=False, tiles=None):
     """conv1d + SiLU over packed q||k||v, then the chunked scan with in-kernel q/k L2 norm,
     in one call of the C entry gdn_layer_prefill.  With ``side_stream`` (a second
     torch.cuda.Stream) the v channels' conv runs on it, overlapping the chunk preparation;
-    without one everything runs on the current stream.  Either way the results equal the
-    two calls in sequence.
+    without one everything runs on the current stream.  ``fused_vconv`` instead convolves
+    the v channels inside the scan's state pass (GDN_LAYER_FUSED_VCONV).  Every path gives
+    the bits of the two calls in sequence (y included, when passed).
 
     Returns (o [T, Hv, dv], final_state [N, Hv, dk, dv], conv_state_out [N, 3, C]).
     """
@@ -326,7 +328,8 @@ def gdn_layer_prefill(x_qkv, conv_w, conv_bias, g, beta, cu_seqlens, Hk, Hv, dk,
         o = torch.empty((T, Hv, dv), dtype=torch.bfloat16, device=dev)
     if final_state is None:
         final_state = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=dev)
-    flags = GDN_QK_L2NORM if l2norm else 0
+    flags = (GDN_QK_L2NORM if l2norm else 0) | (GDN_LAYER_FUSED_VCONV if fused_vconv else 0)
+    flags |= _tile_flag(tiles)
     ws_bytes = int(lib.gdn_chunk_prefill_workspace_size(N, T, Hk, Hv, dk, dv, 64, flags))
     if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)

@@ -14,6 +14,7 @@ GDN_QK_L2NORM = 0x1
 GDN_PREFILL_SIMT = 0x100
 GDN_PREFILL_TILES2 = 0x200
 GDN_PREFILL_TILES3 = 0x400
+GDN_LAYER_FUSED_VCONV = 0x800
 
 STATUS = {
     0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_LAYOUT",

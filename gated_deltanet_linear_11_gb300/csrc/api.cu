@@ -152,7 +152,8 @@ gdn_status_t chunk_prefill_impl(const gdn_tensor_t *q, const gdn_tensor_t *k,
                                 const float *initial_state, const gdn_tensor_t *o,
                                 float *final_state, void *workspace, size_t workspace_bytes,
                                 int32_t *status_dev, void *stream, cudaEvent_t v_ready,
-                                int32_t range_chunks = 0) {
+                                int32_t range_chunks = 0,
+                                const gdn_host::VConvArgs *vconv = nullptr) {
     View Q, K, V, O;
     gdn_status_t s;
     if ((s = view_of(q, Q)) != GDN_OK) return s;
@@ -194,9 +195,12 @@ gdn_status_t chunk_prefill_impl(const gdn_tensor_t *q, const gdn_tensor_t *k,
     a.scale = scale; a.flags = flags;
     a.in_f32 = Q.dtype == GDN_F32; a.out_f32 = O.dtype == GDN_F32;
     a.status = status_dev; a.ws = workspace; a.ws_bytes = workspace_bytes;
+    a.vconv = vconv;
 
     const bool tc = !(flags & GDN_PREFILL_SIMT) &&
                     gdn_host::chunk_tc_supported(a.dk, a.dv, chunk, a.in_f32);
+    // the fused v conv exists in the plain tensor-core scan only
+    if (vconv && (!tc || a.out_f32 || range_chunks != 0)) return GDN_ERR_UNSUPPORTED;
     if (range_chunks != 0) {
         // the context-parallel scan exists on the tensor-core path only
         if (!tc || a.out_f32) return GDN_ERR_UNSUPPORTED;
@@ -364,6 +368,29 @@ gdn_status_t gdn_layer_prefill(const void *x, int64_t T, int32_t Hk, int32_t Hv,
     if (s != GDN_OK) return s;
     if ((max_len + 15) / 16 > 65535) return GDN_ERR_SHAPE;
 
+    if (flags & GDN_LAYER_FUSED_VCONV) {
+        // the q/k channels' conv, then the scan, whose state pass convolves each V tile
+        // from x itself (and writes y's v channels and their conv states): the v channels
+        // make no round trip through memory before the scan
+        if ((flags & GDN_PREFILL_SIMT) || !gdn_host::chunk_tc_supported(dk, dv, 64, 0))
+            return GDN_ERR_UNSUPPORTED;
+        s = gdn_host::launch_conv1d_fwd(x, C, conv_w, conv_bias, cu_seqlens_dev, N, max_len,
+                                        conv_state_in, conv_state_out, y, st, 0,
+                                        (int32_t)(2 * qk));
+        if (s != GDN_OK) return s;
+        gdn_host::VConvArgs vc;
+        vc.x = x;
+        vc.y = y;
+        vc.w = conv_w;
+        vc.b = conv_bias;
+        vc.s_in = conv_state_in;
+        vc.s_out = conv_state_out;
+        vc.xc = C;
+        vc.cv0 = (int32_t)(2 * qk);
+        return chunk_prefill_impl(&tq, &tk, &tv, g, beta, cu_seqlens_dev, cu_seqlens_host, N,
+                                  64, scale, flags, initial_state, &to, final_state, workspace,
+                                  workspace_bytes, status_dev, stream, nullptr, 0, &vc);
+    }
     if (!side_stream) {
         // one stream: the conv over every channel, then the chunk scan
         s = gdn_host::launch_conv1d_fwd(x, C, conv_w, conv_bias, cu_seqlens_dev, N, max_len,

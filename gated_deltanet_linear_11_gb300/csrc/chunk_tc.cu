@@ -35,6 +35,8 @@
 //    warps: warps w and w+4 share TMEM lanes 32(w%4).. and take half the tile's columns
 //    each; a ninth warp issues the MMAs (as a converged warp, one elected lane issuing) and
 //    a tenth the TMA and bulk loads.
+//    chunk_state_vconv_kernel is the same pass for the layer entry's opt-in fusion: it
+//    reads the raw activations of V and applies the width-4 conv + SiLU itself.
 //
 // Every wait on an mbarrier is bounded in time; on expiry the CTA records GDN_ERR_TIMEOUT
 // in the status word, stops issuing work, frees its TMEM and returns.
@@ -46,6 +48,7 @@
 #include <cstring>
 
 #include "common.cuh"
+#include "conv_taps.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.cuh"
 
@@ -91,6 +94,18 @@ struct TcParams {
     const int32_t *rtab;     // per range: its sequence | first << 30 | last << 29
     float *sA, *sP;
     const float *sS;
+    // The layer's v-channel conv fused into the state pass (vconv = 1, plain scan only):
+    // maps.v then views the raw activations, and each state CTA convolves its own V
+    // columns (width 4, SiLU) one chunk ahead, writes them to y and, at the end, the
+    // sequence's new conv state for those channels.
+    int vconv;
+    const bf16 *xr;          // raw activations [T][xc]
+    bf16 *y;                 // conv output [T][xc]
+    const bf16 *cw, *cb;     // taps [xc][4]; bias [xc] or null
+    const bf16 *cs_in;       // conv states [N][3][xc], or null for zeros
+    bf16 *cs_out;            // new conv states [N][3][xc], or null
+    int64_t xc;              // channels per row
+    int cv0;                 // first v channel
 };
 
 constexpr int32_t kRangeFirst = 1 << 30, kRangeLast = 1 << 29, kRangeSeq = (1 << 29) - 1;
@@ -555,9 +570,17 @@ struct StateSmem {
     uint64_t bar_tma[2], bar_d1, bar_d2, bar_d3, bar_fin;
     uint32_t tmem;
     int abort;               // set by the first thread whose wait runs out
+    // The fused-conv kernel only (the plain kernel's allocation ends before them):
+    alignas(1024) uint8_t vc[2][8192];   // the convolved V tile per stage (V's layout)
+    uint8_t xv[3][8192];     // raw V tiles, a ring of three chunks
+    float taps[5][64];       // the tile's taps, oldest first, and biases
+    uint64_t bar_x[3];
 };
+// shared memory of the plain state kernel: StateSmem up to the fused-conv fields
+constexpr size_t kStateSmemPlain = offsetof(StateSmem, vc);
 static_assert(offsetof(StateSmem, dvl) == offsetof(StateSmem, dvh) + 8192,
               "the [hi | lo] operand is one MN-major tile with a 8192-byte block stride");
+static_assert(sizeof(StateSmem) + 1024 <= 227 * 1024, "one state CTA fits on an SM");
 
 // Bounded wait by one thread.  Gives up (false) when the phase has not completed within
 // kWaitNs, or as soon as another thread of the CTA has given up; the caller then skips
@@ -599,6 +622,112 @@ __device__ __forceinline__ void issue_chunk_loads(StateSmem &S, const TcMaps &ma
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  :: "r"(tc::smem_u32(S.x[stage])), "l"(src), "r"(kWsTile),
                     "r"(tc::smem_u32(bar)) : "memory");
+}
+
+// ---------------------------------------------------------------- fused v conv
+// (chunk_state_vconv_kernel only.)  The width-4 causal conv + SiLU of the tile's V
+// channels, with gdn_conv1d_fwd's arithmetic for every element (bias, then the taps
+// oldest first, fused multiply-adds in fp32, its SiLU, round to nearest bf16), read from
+// the raw activation tile that the loader put in the ring S.xv.  The eight compute warps
+// convolve chunk c+1 during chunk c, in the window after the barrier that publishes h,
+// while the chain waits for its first products: compute thread t takes the channel pair
+// t & 31 of the tokens 8 (t >> 5) .. +7, so a warp's row accesses are one 128-byte row,
+// free of bank conflicts, and the taps are five pair loads.  The three inputs before a
+// chunk come from the previous chunk's raw tile (still in the ring), or for a sequence's
+// first chunk from its conv state (zeros without one).
+constexpr int kVcTok = 8;                       // tokens per thread
+
+// The tile's taps and biases, fp32 pairs [tap 0..3, bias][channel pair] (threads 0..63,
+// one column each).
+template <int NT>
+__device__ __forceinline__ void vconv_load_taps(StateSmem &S, const TcParams &p, int hv, int j0) {
+    const int col = threadIdx.x;
+    if (col < NT) {
+        const int64_t chn = p.cv0 + (int64_t)hv * kD + j0 + col;
+        const uint2 w = *reinterpret_cast<const uint2 *>(p.cw + chn * 4);
+        float *tp = reinterpret_cast<float *>(S.taps);
+        tp[0 * 64 + col] = __uint_as_float(w.x << 16);
+        tp[1 * 64 + col] = __uint_as_float(w.x & 0xffff0000u);
+        tp[2 * 64 + col] = __uint_as_float(w.y << 16);
+        tp[3 * 64 + col] = __uint_as_float(w.y & 0xffff0000u);
+        tp[4 * 64 + col] = p.cb ? __bfloat162float(p.cb[chn]) : 0.f;
+    }
+}
+
+// Two bf16 of a tile row (channels 2 cp, 2 cp + 1) as floats.
+__device__ __forceinline__ float2 tile_pair(const uint8_t *tile, int row, int cp) {
+    const uint32_t u = *reinterpret_cast<const uint32_t *>(tile + tc::swz(row, cp >> 2) + 4 * (cp & 3));
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+// Tokens r0 .. r0+7 of chunk cc, channel pair cp.
+__device__ __forceinline__ void vconv_rows(StateSmem &S, const TcParams &p, int n, int cp,
+                                           int r0, int cc, int64_t chn, int t0, int L) {
+    const uint8_t *cur = S.xv[cc % 3], *prev = S.xv[(cc + 2) % 3];
+    uint8_t *out = S.vc[cc & 1];
+    float2 xw[kVcTok + 3];                 // rows r0-3 .. r0+7
+#pragma unroll
+    for (int i = 0; i < kVcTok + 3; ++i) {
+        const int rho = r0 - 3 + i;
+        if (rho >= 0) {
+            xw[i] = tile_pair(cur, rho, cp);
+        } else if (cc > 0) {
+            xw[i] = tile_pair(prev, 64 + rho, cp);
+        } else if (p.cs_in) {
+            const uint32_t u = *reinterpret_cast<const uint32_t *>(
+                p.cs_in + ((int64_t)n * 3 + 3 + rho) * p.xc + chn);
+            xw[i] = make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+        } else {
+            xw[i] = make_float2(0.f, 0.f);
+        }
+    }
+    const float2 *tp = reinterpret_cast<const float2 *>(S.taps);
+    const float2 w0 = tp[0 * 32 + cp], w1 = tp[1 * 32 + cp], w2 = tp[2 * 32 + cp],
+                 w3 = tp[3 * 32 + cp], b = tp[4 * 32 + cp];
+#pragma unroll
+    for (int k = 0; k < kVcTok; ++k) {
+        const int r = r0 + k;
+        float2 z = fma2(w0, xw[k], b);
+        z = fma2(w1, xw[k + 1], z);
+        z = fma2(w2, xw[k + 2], z);
+        z = fma2(w3, xw[k + 3], z);
+        const __nv_bfloat162 o2 = __floats2bfloat162_rn(silu(z.x), silu(z.y));
+        const uint32_t ou = *reinterpret_cast<const uint32_t *>(&o2);
+        *reinterpret_cast<uint32_t *>(out + tc::swz(r, cp >> 2) + 4 * (cp & 3)) = ou;
+        if (r < L) *reinterpret_cast<uint32_t *>(p.y + (int64_t)(t0 + r) * p.xc + chn) = ou;
+    }
+}
+
+// Chunk cc of sequence n (tokens t0.., L of them) into S.vc[cc & 1] and y.
+template <int NT>
+__device__ __forceinline__ void vconv_chunk(StateSmem &S, const TcParams &p, int n, int hv,
+                                            int j0, int cc, int t0, int L) {
+    const int t = threadIdx.x;
+    const int cp = t & 31;
+    if (2 * cp >= NT) return;
+    const int64_t chn = p.cv0 + (int64_t)hv * kD + j0 + 2 * cp;
+    vconv_rows(S, p, n, cp, kVcTok * (t >> 5), cc, chn, t0, L);
+}
+
+// The sequence's new conv state for the tile's channels: xs = [old state (3) ; x_seq],
+// rows xs[len], xs[len+1], xs[len+2].  One thread per 8 channels writes its three rows in
+// order, each after the old row len + j >= j it reads, so cs_out may alias cs_in.
+template <int NT>
+__device__ __forceinline__ void vconv_state_out(const TcParams &p, int n, int hv, int j0,
+                                                int start, int len) {
+    const int grp = threadIdx.x;
+    if (!p.cs_out || grp >= NT / 8) return;
+    const int64_t chn = p.cv0 + (int64_t)hv * kD + j0 + 8 * grp;
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        const int m = len + j;
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if (m >= 3)
+            u = *reinterpret_cast<const uint4 *>(p.xr + (int64_t)(start + m - 3) * p.xc + chn);
+        else if (p.cs_in)
+            u = *reinterpret_cast<const uint4 *>(p.cs_in + ((int64_t)n * 3 + m) * p.xc + chn);
+        *reinterpret_cast<uint4 *>(p.cs_out + ((int64_t)n * 3 + j) * p.xc + chn) = u;
+    }
 }
 
 // NC consecutive TMEM columns of this thread's lane (NC = 32, 24 or 16).
@@ -671,7 +800,7 @@ struct StateJob {
     float *hT;               // this head's end state [dk][dv], or null
 };
 
-template <int NT>
+template <int NT, bool VCONV>
 __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, const TcParams &p,
                                           const CUtensorMap *omap, int j0, int hv,
                                           const StateJob &job) {
@@ -762,26 +891,47 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
         // before the compute warps folded it).  Issuing them costs the MMA issuer nothing.
         const bool leader = lane == 0;
         int issued = 0;                                        // chunks 0..issued-1 are loaded
+        // With the fused conv V is not part of a stage: raw V tile j goes into ring slot
+        // j % 3 two chunks ahead (j + 2 after the barrier that publishes chunk j's h), so
+        // chunk c+1's tile is there when the output warps convolve it during chunk c, and
+        // the slot it replaces (chunk j - 1's, the halo of chunk j's conv) is done with.
+        const bool stage_v = job.with_v && !VCONV;
+        int x_issued = 0;                                      // raw tiles 0..x_issued-1
+        auto issue_x = [&](int j) {
+            uint64_t *bar = &S.bar_x[j % 3];
+            tc::mbar_expect_tx(bar, 8192);
+            tc::tma_load_3d(S.xv[j % 3], &maps.v, bar, j0, hv, start + j * kC);
+            x_issued = j + 1;
+        };
         if (leader) {
+            if (VCONV)
+                for (int j = 0; j < 2 && j < nch; ++j) issue_x(j);
             for (int c = 0; c < 2 && c < nch; ++c) {
-                issue_chunk_loads(S, maps, p, c, start + c * kC, hk, hv, j0, s0 + c, job.with_v);
+                issue_chunk_loads(S, maps, p, c, start + c * kC, hk, hv, j0, s0 + c, stage_v);
                 issued = c + 1;
             }
         }
         for (int c = 0; c < nch; ++c) {
             __syncwarp();
             __syncthreads();                                   // h published as bf16
+            if (VCONV && leader && c + 2 < nch && !*abort) issue_x(c + 2);
             if (leader && c >= 1 && c + 1 < nch && !*abort) {
                 issue_chunk_loads(S, maps, p, (c + 1) & 1, start + (c + 1) * kC, hk, hv, j0,
-                                  s0 + c + 1, job.with_v);
+                                  s0 + c + 1, stage_v);
                 issued = c + 2;
             }
         }
         if (leader) {
-            // wait (bounded) for the last load into each stage before the CTA may exit
+            // wait (bounded) for the last load into each stage and ring slot before the
+            // CTA may exit
             for (int s = 0; s < 2; ++s) {
                 const int last = issued - 1 - ((issued - 1 - s) & 1);   // last chunk into stage s
                 if (last >= 0) wait_bounded(&S.bar_tma[s], (last >> 1) & 1);
+            }
+            for (int s = 0; s < (VCONV ? 3 : 0); ++s) {
+                int last = -1;                                  // last raw tile into slot s
+                for (int j = s; j < x_issued; j += 3) last = j;
+                if (last >= 0) wait_bounded(&S.bar_x[s], (last / 3) & 1);
             }
         }
         __syncwarp();
@@ -818,6 +968,13 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
 
     bool ok = true;
     const int r = row & 63;
+    if (VCONV && nch > 0) {
+        // the tile's taps, then chunk 0's V (chunk c+1's is made during chunk c)
+        vconv_load_taps<NT>(S, p, hv, j0);
+        asm volatile("bar.sync 3, %0;" :: "n"(kComputeThreads) : "memory");
+        ok = wait_one(&S.bar_x[0], 0, abort);
+        if (ok) vconv_chunk<NT>(S, p, n, hv, j0, 0, start, min(kC, len));
+    }
     float aL_prev = 1.f;   // e^{gamma_L} of the previous chunk
     for (int c = 0; c < nch; ++c) {
         const int st = c & 1;
@@ -854,10 +1011,18 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
         // this row's V columns, read ahead of the D1 wait (the chain rows' R needs them)
         uint4 vraw[NCH];
         if (chain) {
+            const uint8_t *vt = VCONV ? S.vc[st] : S.v[st];
 #pragma unroll
             for (int cc = 0; cc < NCH; ++cc)
-                vraw[cc] = job.with_v ? *reinterpret_cast<const uint4 *>(S.v[st] + tc::swz(r, c0 + cc))
+                vraw[cc] = job.with_v ? *reinterpret_cast<const uint4 *>(vt + tc::swz(r, c0 + cc))
                                       : make_uint4(0u, 0u, 0u, 0u);
+        }
+
+        // the next chunk's V, while the chain waits for D1
+        if (VCONV && c + 1 < nch && ok) {
+            ok = wait_one(&S.bar_x[(c + 1) % 3], ((c + 1) / 3) & 1, abort);
+            if (ok)
+                vconv_chunk<NT>(S, p, n, hv, j0, c + 1, t0 + kC, min(kC, len - (c + 1) * kC));
         }
 
         // --- B: R = beta (V - e^gamma nk K h) on the chain rows; e^gamma nq Q h on the rest
@@ -1006,6 +1171,7 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
     if (tid == kOutLeader) tc::bulk_wait_all();   // O tiles written before the CTA exits
     tc::fence_before_sync();
     __syncthreads();
+    if (VCONV && !*abort) vconv_state_out<NT>(p, n, hv, j0, start, len);
     if (!*abort && job.hT) {
         float4 *dst = reinterpret_cast<float4 *>(job.hT + (size_t)row * kD + j0 + ch);
 #pragma unroll
@@ -1018,8 +1184,8 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
 
 // One CTA per (sequence, v-head, dv tile).  The tiles of a head are either two of 64
 // columns or, when that leaves SMs idle (p.ntiles == 3), 48 + 48 + 32 columns.
-__global__ void __launch_bounds__(kStateThreads, 1)
-chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
+template <bool VCONV>
+__device__ __forceinline__ void state_kernel_body(const TcMaps &maps, const TcParams &p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     StateSmem &S = *reinterpret_cast<StateSmem *>(
         (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023));
@@ -1039,6 +1205,8 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         tc::mbar_init(&S.bar_d2, 1);
         tc::mbar_init(&S.bar_d3, 1);
         tc::mbar_init(&S.bar_fin, 1);
+        if (VCONV)
+            for (int i = 0; i < 3; ++i) tc::mbar_init(&S.bar_x[i], 1);
         S.abort = 0;
         tc::mbar_fence_init();
         tc::prefetch_tmap(&maps.k);
@@ -1088,11 +1256,22 @@ chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ 
         }
     }
     if (p.ntiles != 3)
-        state_cta<64>(S, maps, p, &maps.o, 64 * jt, hv, job);
+        state_cta<64, VCONV>(S, maps, p, &maps.o, 64 * jt, hv, job);
     else if (jt < 2)
-        state_cta<48>(S, maps, p, &maps.o48, 48 * jt, hv, job);
+        state_cta<48, VCONV>(S, maps, p, &maps.o48, 48 * jt, hv, job);
     else
-        state_cta<32>(S, maps, p, &maps.o32, 96, hv, job);
+        state_cta<32, VCONV>(S, maps, p, &maps.o32, 96, hv, job);
+}
+
+__global__ void __launch_bounds__(kStateThreads, 1)
+chunk_state_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
+    state_kernel_body<false>(maps, p);
+}
+
+// The same with the layer's v-channel conv fused in (p.vconv = 1).
+__global__ void __launch_bounds__(kStateThreads, 1)
+chunk_state_vconv_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
+    state_kernel_body<true>(maps, p);
 }
 
 // ====================================================== context-parallel composition
@@ -1259,8 +1438,12 @@ namespace {
 // state pass, for the tiling choice.
 gdn_status_t setup_scan(const ScanArgs &a, int64_t n_chains, gdn::TcMaps &maps,
                         gdn::TcParams &p, size_t &prep_smem, size_t &state_smem) {
+    // with the fused v conv the V map views the raw activations' v channels
+    const VConvArgs *vc = a.vconv;
+    const void *vsrc = vc ? (const void *)((const gdn::bf16 *)vc->x + vc->cv0) : a.v;
+    const int64_t vtok = vc ? vc->xc : a.v_tok;
     if (!make_map(&maps.q, a.q, a.T, a.Hk, a.q_tok) || !make_map(&maps.k, a.k, a.T, a.Hk, a.k_tok) ||
-        !make_map(&maps.v, a.v, a.T, a.Hv, a.v_tok) || !make_map(&maps.o, a.o, a.T, a.Hv, a.o_tok) ||
+        !make_map(&maps.v, vsrc, a.T, a.Hv, vtok) || !make_map(&maps.o, a.o, a.T, a.Hv, a.o_tok) ||
         !make_map(&maps.o48, a.o, a.T, a.Hv, a.o_tok, 48) ||
         !make_map(&maps.o32, a.o, a.T, a.Hv, a.o_tok, 32))
         return GDN_ERR_CUDA;
@@ -1279,6 +1462,17 @@ gdn_status_t setup_scan(const ScanArgs &a, int64_t n_chains, gdn::TcMaps &maps,
     p.scale = a.scale;
     p.l2norm = (a.flags & GDN_QK_L2NORM) ? 1 : 0;
     p.status = a.status;
+    if (vc) {
+        p.vconv = 1;
+        p.xr = (const gdn::bf16 *)vc->x;
+        p.y = (gdn::bf16 *)vc->y;
+        p.cw = (const gdn::bf16 *)vc->w;
+        p.cb = (const gdn::bf16 *)vc->b;
+        p.cs_in = (const gdn::bf16 *)vc->s_in;
+        p.cs_out = (gdn::bf16 *)vc->s_out;
+        p.xc = vc->xc;
+        p.cv0 = vc->cv0;
+    }
     // Three dv tiles per head (48 + 48 + 32 columns) when they still fit one wave on the
     // SMs, else two of 64.  So the tiling follows N and the device's SM count; it changes
     // how the columns are grouped, not the arithmetic of any column (every column's
@@ -1294,7 +1488,7 @@ gdn_status_t setup_scan(const ScanArgs &a, int64_t n_chains, gdn::TcMaps &maps,
         p.ntiles = (sms > 0 && (int64_t)3 * a.Hv * n_chains <= sms) ? 3 : 2;
 
     prep_smem = sizeof(gdn::PrepSmem) + 1024;
-    state_smem = sizeof(gdn::StateSmem) + 1024;
+    state_smem = (vc ? sizeof(gdn::StateSmem) : gdn::kStateSmemPlain) + 1024;
     // the shared-memory opt-in is a per-device attribute: set it once on each device
     static std::atomic<bool> attr_set[kMaxDevices];
     int dev = 0;
@@ -1306,7 +1500,10 @@ gdn_status_t setup_scan(const ScanArgs &a, int64_t n_chains, gdn::TcMaps &maps,
             cudaFuncSetAttribute(gdn::chunk_prep_kernel,
                                  cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess ||
             cudaFuncSetAttribute(gdn::chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)state_smem) != cudaSuccess ||
+                                 (int)(gdn::kStateSmemPlain + 1024)) != cudaSuccess ||
+            cudaFuncSetAttribute(gdn::chunk_state_vconv_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(sizeof(gdn::StateSmem) + 1024)) != cudaSuccess ||
             cudaFuncSetAttribute(gdn::cp_compose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)gdn::kComposeSmem) != cudaSuccess)
             return GDN_ERR_CUDA;
@@ -1327,8 +1524,9 @@ gdn_status_t launch_prep(const gdn::TcMaps &maps, const gdn::TcParams &p, int64_
 gdn_status_t launch_state(const gdn::TcMaps &maps, const gdn::TcParams &p, int grid_z,
                           size_t state_smem, cudaStream_t st) {
     dim3 g2(p.ntiles, p.Hv, grid_z);
-    return launch_dependent(gdn::chunk_state_kernel, g2, dim3(gdn::kStateThreads), state_smem,
-                            st, maps, p) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    return launch_dependent(p.vconv ? gdn::chunk_state_vconv_kernel : gdn::chunk_state_kernel, g2,
+                            dim3(gdn::kStateThreads), state_smem, st, maps, p) == cudaSuccess
+               ? GDN_OK : GDN_ERR_CUDA;
 }
 
 // Ranges of the context-parallel split: ceil(chunks / range_chunks) per sequence, at
@@ -1394,6 +1592,7 @@ gdn_status_t launch_chunk_tc_cp(const ScanArgs &a, const int32_t *cu_host, int32
                                 cudaStream_t st) {
     if (a.N == 0) return GDN_OK;
     if (a.out_f32) return GDN_ERR_DTYPE;
+    if (a.vconv) return GDN_ERR_UNSUPPORTED;
     if (range_chunks <= 0) return GDN_ERR_SHAPE;
     const int64_t nr = cp_range_count(cu_host, a.N, range_chunks);
     if (nr < 0) return GDN_ERR_SHAPE;

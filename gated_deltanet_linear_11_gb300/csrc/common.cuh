@@ -91,6 +91,18 @@ gdn_status_t launch_conv1d_update(const void *x, int32_t N, int32_t C, const voi
                                   const int32_t *idx, void *y, int32_t *status,
                                   cudaStream_t st);
 
+// The layer's v-channel conv, fused into the tensor-core state pass: V is then computed
+// from the raw activations x (its channels cv0.. of rows xc wide) instead of read.
+struct VConvArgs {
+    const void *x;           // raw activations [T][xc] bf16
+    void *y;                 // conv output [T][xc] bf16: the state pass writes its v channels
+    const void *w, *b;       // taps [xc][4] bf16; bias [xc] bf16 or null
+    const void *s_in;        // conv states [N][3][xc] bf16, or null for zeros
+    void *s_out;             // new conv states [N][3][xc] bf16, or null
+    int64_t xc;
+    int32_t cv0;
+};
+
 struct ScanArgs {
     const void *q, *k, *v;
     void *o;
@@ -108,6 +120,7 @@ struct ScanArgs {
     int32_t *status;
     void *ws;
     size_t ws_bytes;
+    const VConvArgs *vconv;  // null: V is read from v
 };
 gdn_status_t launch_chunk_simt(const ScanArgs &a, cudaStream_t st);
 // before_state: an event the state kernel's launch waits on (the producer of v), or NULL

@@ -146,6 +146,8 @@ gdn_status_t gdn_conv1d_update(const void *x, int32_t N, int32_t C, const void *
  * either, since no column's arithmetic depends on its tile. */
 #define GDN_PREFILL_TILES2 0x200u
 #define GDN_PREFILL_TILES3 0x400u
+/* gdn_layer_prefill only: fuse the v channels' conv into the scan's state pass. */
+#define GDN_LAYER_FUSED_VCONV 0x800u
 
 size_t gdn_chunk_prefill_workspace_size(int32_t N, int64_t T, int32_t Hk, int32_t Hv,
                                         int32_t dk, int32_t dv, int32_t chunk,
@@ -254,16 +256,25 @@ gdn_status_t gdn_recurrent_decode(const gdn_tensor_t *q, const gdn_tensor_t *k,
 /*
  * gdn_layer_prefill -- the layer's prefill in one call: gdn_conv1d_fwd over the packed
  * q | k | v channels, then gdn_chunk_prefill on q, k, v as strided views of its output.
- * Sources: those of the two entries it chains.
+ * Sources: those of the two entries it chains; the fused conv follows "[Feature] Add
+ * batch invariance support to GDN_ATTN backend - #45819", Birol's comment, part 3(a)
+ * (the conv output feeds the scan directly).
  * side_stream: NULL, or a second cudaStream_t of the caller's (it must differ from
- * `stream`).  With NULL everything runs on `stream` in order.  With a side stream the conv
- * of the v channels runs on it while the q/k channels' conv and the chunk preparation,
- * which reads only q and k, run on `stream`; the state pass waits for v, and `stream`
- * waits for the side stream before the call returns, so the caller sees one ordered
- * stream (CUDA-graph capture included).  The library owns no stream: the fork and join
- * use two events that this call creates and destroys.  Calls that share a side stream are
- * ordered on it.  Results are bit-identical to calling the two entries in sequence, with
- * or without a side stream.
+ * `stream`).  With NULL everything runs on `stream` in order.
+ * With a side stream the conv of the v channels runs on it while the q/k channels' conv
+ * and the chunk preparation, which reads only q and k, run on `stream`; the state pass
+ * waits for v, and `stream` waits for the side stream before the call returns, so the
+ * caller sees one ordered stream (CUDA-graph capture included).  The library owns no
+ * stream: the fork and join use two events that this call creates and destroys.  Calls
+ * that share a side stream are ordered on it.
+ * GDN_LAYER_FUSED_VCONV (tensor-core shapes only, else GDN_ERR_UNSUPPORTED; side_stream
+ * is then unused): the conv kernel runs over the q/k channels only, and the scan's state
+ * pass convolves each V tile from x itself one chunk ahead, writing it to y and, at the
+ * end, the v channels' conv states.  It saves the v channels' round trip through memory
+ * but adds its arithmetic to the latency-bound state pass, which makes the call slower
+ * on the 27B shapes, so it is not the default.
+ * Every path gives exactly the bits of calling the two entries in sequence (y, o,
+ * final_state and conv_state_out alike).
  *
  * x [T, C] bf16, C = 2*Hk*dk + Hv*dv, rows contiguous; y [T, C] bf16 receives the conv
  * output; o [T, Hv, dv] bf16 contiguous; everything else as in gdn_conv1d_fwd and

@@ -62,7 +62,8 @@ def test_prefill_writes_only_its_outputs(simt):
     assert_guards_intact(h_full, 2, N, "final state")
 
 
-def test_layer_prefill_writes_only_its_outputs():
+@pytest.mark.parametrize("fused_vconv", [False, True])
+def test_layer_prefill_writes_only_its_outputs(fused_vconv):
     s = dict(Hk=2, Hv=6, dk=128, dv=128)
     C = inputs.conv_channels(**s)
     lens = [100, 1, 67]
@@ -78,7 +79,7 @@ def test_layer_prefill_writes_only_its_outputs():
                           x["beta"].cuda(), cv["cu_seqlens"].cuda(), s["Hk"], s["Hv"], 128,
                           128, conv_state_in=cv["conv_state"].cuda(), conv_state_out=cs,
                           initial_state=x["initial_state"].cuda(), final_state=h, y=y, o=o,
-                          cu_seqlens_host=cv["cu_seqlens"])
+                          cu_seqlens_host=cv["cu_seqlens"], fused_vconv=fused_vconv)
     torch.cuda.synchronize()
     assert_guards_intact(y_full, pad, T, "conv output y")
     assert_guards_intact(o_full, pad, T, "o")

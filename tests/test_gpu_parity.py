@@ -295,23 +295,30 @@ def test_layer_prefill_27b_heads_sampled():
     np.testing.assert_array_equal(np64(st), st_ref)
 
 
-@pytest.mark.parametrize("l2norm,side", [(True, True), (False, True), (True, False)])
-def test_layer_prefill_entry_equals_two_calls_bits(l2norm, side):
-    """gdn_layer_prefill (with a caller's side stream, the conv of the v channels runs on
-    it, overlapping the chunk preparation; without one, everything runs on the current
-    stream) gives exactly the bits of gdn_conv1d_fwd followed by gdn_chunk_prefill."""
+@pytest.mark.parametrize("l2norm,mode", [(True, "fused"), (False, "fused"), (True, "fused3"),
+                                         (True, "side"), (False, "side"), (True, "separate")])
+def test_layer_prefill_entry_equals_two_calls_bits(l2norm, mode):
+    """gdn_layer_prefill gives exactly the bits of gdn_conv1d_fwd followed by
+    gdn_chunk_prefill, for y, o, the final states and the conv states, on every path: the
+    conv with the v channels on a caller's side stream overlapping the chunk preparation,
+    everything on the current stream, and the v channels' conv fused into the state pass
+    ("fused3" under the 48 + 48 + 32 column tiling).  The batch has an empty sequence and
+    ones shorter than the conv window."""
     s = dict(Hk=2, Hv=6, dk=128, dv=128)
     C = inputs.conv_channels(**s)
-    lens = [70, 1, 0, 129, 64]
+    lens = [70, 1, 0, 129, 64, 2]
     cv = inputs.conv_inputs(81, lens, C, with_state=True, with_bias=True)
     x = inputs.scan_inputs(82, lens, s["Hk"], s["Hv"], 128, 128, init_state_std=0.02)
     args = [cv["x"].cuda(), cv["w"].cuda(), cv["bias"].cuda(), x["g"].cuda(),
             x["beta"].cuda(), cv["cu_seqlens"].cuda()]
+    y1 = torch.empty_like(args[0])
     o1, h1, st1 = gdn.gdn_layer_prefill(*args, s["Hk"], s["Hv"], 128, 128,
                                         conv_state_in=cv["conv_state"].cuda(),
                                         initial_state=x["initial_state"].cuda(), l2norm=l2norm,
-                                        scale=0.7, cu_seqlens_host=cv["cu_seqlens"],
-                                        side_stream=torch.cuda.Stream() if side else None)
+                                        scale=0.7, cu_seqlens_host=cv["cu_seqlens"], y=y1,
+                                        fused_vconv=mode in ("fused", "fused3"),
+                                        side_stream=torch.cuda.Stream() if mode == "side" else None,
+                                        tiles=3 if mode == "fused3" else None)
     y, st2 = gdn.gdn_conv1d_fwd(args[0], args[1], args[2], args[5], cv["conv_state"].cuda(),
                                 cu_seqlens_host=cv["cu_seqlens"])
     q, k, v = gdn.split_qkv(y, s["Hk"], s["Hv"], 128, 128)
@@ -319,9 +326,35 @@ def test_layer_prefill_entry_equals_two_calls_bits(l2norm, side):
                                    scale=0.7, initial_state=x["initial_state"].cuda(),
                                    cu_seqlens_host=cv["cu_seqlens"])
     torch.cuda.synchronize()
+    assert_bits_equal(y1, y, "conv output y")
     assert_bits_equal(o1, o2, "o")
     assert_bits_equal(h1, h2, "final state")
     assert_bits_equal(st1, st2, "conv state")
+
+
+def test_layer_prefill_fused_conv_without_conv_state():
+    """The fused v conv of fresh sequences (no conv state: zeros before each sequence,
+    including one sequence's first chunk that follows another's tokens in the packed
+    rows) against the oracle layer, every v-head."""
+    s = dict(Hk=2, Hv=6, dk=128, dv=128)
+    C = inputs.conv_channels(**s)
+    lens = [130, 3, 64, 65]
+    cv = inputs.conv_inputs(83, lens, C, with_state=False, with_bias=True)
+    rng = np.random.default_rng(84)
+    T = sum(lens)
+    g, beta = inputs.gates(rng, T, s["Hv"], 2.0)
+    cu = cv["cu_seqlens"]
+    y = torch.empty_like(cv["x"]).cuda()
+    o, hT, st = gdn.gdn_layer_prefill(cv["x"].cuda(), cv["w"].cuda(), cv["bias"].cuda(),
+                                      g.cuda(), beta.cuda(), cu.cuda(), s["Hk"], s["Hv"], 128,
+                                      128, y=y, cu_seqlens_host=cu, fused_vconv=True)
+    o_ref, h_ref, st_ref = oracle.layer_prefill(cv["x"], cv["w"], cv["bias"], g, beta, cu,
+                                                s["Hk"], s["Hv"], 128, 128)
+    assert_out_close(o, o_ref)
+    assert_state_close(hT, h_ref)
+    np.testing.assert_array_equal(np64(st), st_ref)
+    y_ref, _ = oracle.conv1d_varlen(cv["x"], cv["w"], cv["bias"], cu)
+    assert_out_close(y, y_ref, what="conv output y")
 
 
 @pytest.mark.parametrize("l2norm", [False, True])
