@@ -603,6 +603,11 @@ def multiseq_leg(gdn, inputs, dev, flush_l2, peak_tf, warmup, steps):
                "of 64 chunks", [32768], 2, 6, True, 64),
               ("27B heads / 8 (Hk=2, Hv=6), 1 x 32768 tokens, context-parallel in ranges "
                "of 32 chunks", [32768], 2, 6, True, 32)]
+    # and in the range length gdn_chunk_prefill_cp_range_hint picks for that sequence
+    hint = gdn.gdn_chunk_prefill_cp_range_hint(32768, 6)
+    if hint:
+        cases.append(("27B heads / 8 (Hk=2, Hv=6), 1 x 32768 tokens, context-parallel in "
+                      "ranges of %d chunks (the range hint)" % hint, [32768], 2, 6, True, hint))
     cases = [c if len(c) == 6 else c + (0,) for c in cases]
     gen = torch.Generator(device=dev)
     gen.manual_seed(7)

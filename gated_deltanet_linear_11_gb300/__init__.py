@@ -29,7 +29,7 @@ from ._lib import (GDN_LAYER_FUSED_VCONV, GDN_PREFILL_SIMT, GDN_PREFILL_TILES2, 
 
 __all__ = ["gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
            "gdn_chunk_prefill_noalloc", "gdn_chunk_prefill_cp",
-           "gdn_chunk_prefill_cp_workspace_size",
+           "gdn_chunk_prefill_cp_workspace_size", "gdn_chunk_prefill_cp_range_hint",
            "gdn_recurrent_decode", "gdn_fused_decode", "gdn_chunk_prefill_workspace_size",
            "gdn_layer_prefill", "gdn_layer_decode", "GdnError", "load"]
 
@@ -181,6 +181,13 @@ def gdn_chunk_prefill_cp_workspace_size(cu_seqlens_host, T, Hk, Hv, dk, dv, rang
     return int(lib.gdn_chunk_prefill_cp_workspace_size(
         ctypes.c_void_p(cu_h.data_ptr()), cu_h.numel() - 1, T, Hk, Hv, dk, dv, chunk,
         range_chunks))
+
+
+def gdn_chunk_prefill_cp_range_hint(seq_len, Hv):
+    """range_chunks for one sequence of ``seq_len`` tokens over ``Hv`` v-heads alone on
+    the current device, or 0 when the plain scan is expected to be as fast (C entry
+    gdn_chunk_prefill_cp_range_hint; depends on the sequence's own length only)."""
+    return int(_lib.load().gdn_chunk_prefill_cp_range_hint(int(seq_len), int(Hv)))
 
 
 def gdn_chunk_prefill_cp(q, k, v, g, beta, cu_seqlens, range_chunks, chunk=64, scale=1.0,

@@ -245,6 +245,10 @@ size_t gdn_chunk_prefill_cp_workspace_size(const int32_t *cu_seqlens_host, int32
     return gdn_host::chunk_tc_cp_workspace(cu_seqlens_host, N, T, Hk, Hv, range_chunks);
 }
 
+int32_t gdn_chunk_prefill_cp_range_hint(int64_t seq_len, int32_t Hv) {
+    return gdn_host::cp_range_hint(seq_len, Hv);
+}
+
 gdn_status_t gdn_chunk_prefill_cp(const gdn_tensor_t *q, const gdn_tensor_t *k,
                                   const gdn_tensor_t *v, const float *g, const float *beta,
                                   const int32_t *cu_seqlens_dev,

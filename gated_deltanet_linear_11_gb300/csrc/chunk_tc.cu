@@ -1310,18 +1310,27 @@ __global__ void cp_tables_kernel(const int32_t *cu, int N, int range_chunks, int
     cu_split[n_ranges] = cu[N];
 }
 
-// Start states of a sequence's ranges, in order: one CTA per (16 dv columns, v-head,
+// Start states of a sequence's ranges, in order: one CTA per (8 dv columns, v-head,
 // sequence), one thread per dk row.  S = the first range's end state; for each later
-// range r: its start is S, then S <- P_r S + R_r (fp32, k in increasing order).
-constexpr int kComposeCols = 16;
-constexpr int kComposeLd = kD + 1;          // padded P rows: thread i reads row i
-constexpr size_t kComposeSmem = (size_t)kD * kComposeLd * 4 + (size_t)kD * kComposeCols * 4;
+// range r: its start is S, then S <- P_r S + R_r (fp32, k in increasing order).  The
+// chain is sequential over ranges, so its step time is what counts: the next P (64 KiB)
+// is copied into the other half of a shared-memory double buffer by 16-byte asynchronous
+// copies while the current step computes, and R_r is read before the wait for P_r.
+constexpr int kComposeCols = 8;
+constexpr int kComposeLd = kD + 4;          // P rows, 16-byte aligned; float4 reads of a row
+constexpr size_t kComposeSmem = 2 * (size_t)kD * kComposeLd * 4 + (size_t)kD * kComposeCols * 4;
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 :: "r"(tc::smem_u32(smem)), "l"(gmem) : "memory");
+}
+
 __global__ void __launch_bounds__(kD)
 cp_compose_kernel(const float *sA, const float *sP, float *sS, const int32_t *seq_first,
                   int N, int Hv, int n_ranges) {
-    extern __shared__ float csm[];
-    float (*Psm)[kComposeLd] = reinterpret_cast<float (*)[kComposeLd]>(csm);
-    float (*Ssm)[kComposeCols] = reinterpret_cast<float (*)[kComposeCols]>(csm + kD * kComposeLd);
+    extern __shared__ __align__(16) float csm[];
+    float (*Psm)[kD][kComposeLd] = reinterpret_cast<float (*)[kD][kComposeLd]>(csm);
+    float (*Ssm)[kComposeCols] = reinterpret_cast<float (*)[kComposeCols]>(csm + 2 * kD * kComposeLd);
     grid_dependents_launch();
     grid_dependency_wait();
     const int j0 = blockIdx.x * kComposeCols, hv = blockIdx.y, n = blockIdx.z;
@@ -1331,31 +1340,61 @@ cp_compose_kernel(const float *sA, const float *sP, float *sS, const int32_t *se
     if (R <= 1) return;
     const size_t hd = (size_t)kD * kD;
     auto head = [&](const float *base, int range) { return base + ((size_t)range * Hv + hv) * hd; };
-#pragma unroll
-    for (int j = 0; j < kComposeCols; ++j) Ssm[i][j] = head(sA, first)[(size_t)i * kD + j0 + j];
+    // P of range idx into buffer b: 4096 16-byte pieces, 32 per thread, one commit group
+    auto fetch_p = [&](int idx, int b) {
+        const float *P = head(sP, idx);
+        for (int c = i; c < kD * kD / 4; c += kD) {
+            const int row = c / (kD / 4), col = 4 * (c % (kD / 4));
+            cp_async16(&Psm[b][row][col], P + (size_t)row * kD + col);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    if (R > 2) fetch_p(first + 1, 1);
+    {
+        const float4 *src = reinterpret_cast<const float4 *>(head(sA, first) + (size_t)i * kD + j0);
+        const float4 a = src[0], b = src[1];
+        Ssm[i][0] = a.x; Ssm[i][1] = a.y; Ssm[i][2] = a.z; Ssm[i][3] = a.w;
+        Ssm[i][4] = b.x; Ssm[i][5] = b.y; Ssm[i][6] = b.z; Ssm[i][7] = b.w;
+    }
     for (int r = 1; r < R; ++r) {
         const int idx = first + r;
-        float *dst = const_cast<float *>(head(sS, idx)) + (size_t)i * kD + j0;
-#pragma unroll
-        for (int j = 0; j < kComposeCols; ++j) dst[j] = Ssm[i][j];
-        if (r == R - 1) break;
-        const float *P = head(sP, idx);
-        for (int e = i; e < kD * kD; e += kD) Psm[e / kD][e % kD] = P[e];
-        float acc[kComposeCols];
-        const float *Rr = head(sA, idx) + (size_t)i * kD + j0;
-#pragma unroll
-        for (int j = 0; j < kComposeCols; ++j) acc[j] = Rr[j];
-        __syncthreads();
-        for (int k = 0; k < kD; ++k) {
-            const float pk = Psm[i][k];
-#pragma unroll
-            for (int j = 0; j < kComposeCols; ++j) acc[j] = fmaf(pk, Ssm[k][j], acc[j]);
+        {
+            float4 *dst = reinterpret_cast<float4 *>(sS + ((size_t)idx * Hv + hv) * hd + (size_t)i * kD + j0);
+            dst[0] = make_float4(Ssm[i][0], Ssm[i][1], Ssm[i][2], Ssm[i][3]);
+            dst[1] = make_float4(Ssm[i][4], Ssm[i][5], Ssm[i][6], Ssm[i][7]);
         }
-        __syncthreads();                       // every read of S and P is done
+        if (r == R - 1) break;
+        float acc[kComposeCols];
+        {
+            const float4 *src = reinterpret_cast<const float4 *>(head(sA, idx) + (size_t)i * kD + j0);
+            const float4 a = src[0], b = src[1];
+            acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+            acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+        }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();                       // P_idx in buffer r & 1, visible to all
+        if (r + 1 < R - 1) fetch_p(idx + 1, (r + 1) & 1);
+        const float *prow = Psm[r & 1][i];
+#pragma unroll 4
+        for (int k = 0; k < kD; k += 4) {
+            const float4 p4 = *reinterpret_cast<const float4 *>(prow + k);
+            const float pk[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float4 s0 = *reinterpret_cast<const float4 *>(&Ssm[k + u][0]);
+                const float4 s1 = *reinterpret_cast<const float4 *>(&Ssm[k + u][4]);
+                acc[0] = fmaf(pk[u], s0.x, acc[0]); acc[1] = fmaf(pk[u], s0.y, acc[1]);
+                acc[2] = fmaf(pk[u], s0.z, acc[2]); acc[3] = fmaf(pk[u], s0.w, acc[3]);
+                acc[4] = fmaf(pk[u], s1.x, acc[4]); acc[5] = fmaf(pk[u], s1.y, acc[5]);
+                acc[6] = fmaf(pk[u], s1.z, acc[6]); acc[7] = fmaf(pk[u], s1.w, acc[7]);
+            }
+        }
+        __syncthreads();                       // every read of S and of this P is done
 #pragma unroll
         for (int j = 0; j < kComposeCols; ++j) Ssm[i][j] = acc[j];
         __syncthreads();
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");   // nothing in flight at exit
 }
 
 // Self-test of the bounded waits: one CTA waits, with the helper the kernels above use,
@@ -1563,6 +1602,39 @@ CpLayout cp_layout(int64_t nr, int32_t N, int64_t T, int32_t Hk, int32_t Hv) {
 }
 
 }  // namespace
+
+// Range length for one sequence of nch chunks over Hv v-heads alone on this device, by a
+// cost count in chunk-times (one chunk of one state CTA's chain): each state pass costs
+// its waves of CTAs (one per SM, in the dv tiling the kernels pick) times the range
+// length plus kCpCta (a CTA's start and end); the split adds kCpPerRange per range (the
+// composition runs range after range, and each range's end state and transition map go
+// through memory) and kCpFixed (its extra launches).  The constants are fitted to the
+// plain scan and the 32-, 64- and 74-chunk splits of one 32768-token sequence over 6
+// v-heads on the GB300 (the fit reproduces those three times within 1%).  0 when the
+// plain scan is expected to be at least as fast.
+int32_t cp_range_hint(int64_t seq_len, int32_t Hv) {
+    constexpr int64_t kCpCta = 1, kCpPerRange = 2, kCpFixed = 18;
+    const int sms = sm_count();
+    if (sms <= 0 || Hv <= 0 || seq_len <= 0) return 0;
+    const int64_t nch = (seq_len + gdn::kC - 1) / gdn::kC;
+    auto tiles = [&](int64_t chains) -> int64_t { return 3 * Hv * chains <= sms ? 3 : 2; };
+    auto waves = [&](int64_t ctas) -> int64_t { return (ctas + sms - 1) / sms; };
+    int64_t best = waves(tiles(1) * Hv) * (nch + kCpCta);
+    int32_t best_r = 0;
+    for (int64_t r = 1; r < nch; ++r) {
+        const int64_t nr = (nch + r - 1) / r;
+        if (2 * nr > 65535) continue;
+        const int64_t mid = nr > 2 ? nr - 2 : 0;
+        const int64_t t = tiles(2 * nr);
+        const int64_t cost = (waves(t * Hv * (nr + mid)) + waves(t * Hv * (nr - 1))) * (r + kCpCta) +
+                             kCpPerRange * nr + kCpFixed;
+        if (cost < best) {
+            best = cost;
+            best_r = (int32_t)r;
+        }
+    }
+    return best_r;
+}
 
 size_t chunk_tc_cp_workspace(const int32_t *cu_host, int32_t N, int64_t T, int32_t Hk,
                              int32_t Hv, int32_t range_chunks) {

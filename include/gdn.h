@@ -191,6 +191,20 @@ size_t gdn_chunk_prefill_cp_workspace_size(const int32_t *cu_seqlens_host, int32
                                            int64_t T, int32_t Hk, int32_t Hv, int32_t dk,
                                            int32_t dv, int32_t chunk, int32_t range_chunks);
 
+/*
+ * gdn_chunk_prefill_cp_range_hint -- a range_chunks for one sequence of seq_len tokens
+ * over Hv v-heads run alone on the current device, or 0 when the plain gdn_chunk_prefill
+ * is expected to be at least as fast.  A host-side estimate (no launch, no allocation):
+ * each state pass is counted as its waves of CTAs (one per SM, the dv tiling of the
+ * kernels) times the range length, plus a fixed allowance for the composition; the
+ * range length with the lowest count wins.  It depends on seq_len, Hv and the device's
+ * SM count only, never on other sequences, so passing it keeps a sequence's bits the
+ * same in any batch on that device (a value chosen from a whole batch would not: see
+ * gdn_chunk_prefill_cp).  0 also when there is no current device or an argument is not
+ * positive.
+ */
+int32_t gdn_chunk_prefill_cp_range_hint(int64_t seq_len, int32_t Hv);
+
 gdn_status_t gdn_chunk_prefill_cp(const gdn_tensor_t *q, const gdn_tensor_t *k,
                                   const gdn_tensor_t *v, const float *g, const float *beta,
                                   const int32_t *cu_seqlens_dev,

@@ -228,6 +228,17 @@ def test_cp_rejections(lib):
     assert cp_prefill(lib, qh, k, v, o, [0, 8], 1, 2) == 3
 
 
+def test_cp_range_hint_without_device(lib):
+    """The range hint is a host-side estimate that needs the device's SM count: without a
+    current device, and for arguments that are not positive, it answers 0 (the plain
+    scan)."""
+    import torch
+    f = lib.gdn_chunk_prefill_cp_range_hint
+    assert f(0, 6) == 0 and f(-5, 6) == 0 and f(4096, 0) == 0
+    if not torch.cuda.is_available():
+        assert f(32768, 6) == 0
+
+
 def test_selftest_needs_a_status_word(lib):
     assert lib.gdn_selftest_bounded_wait(None, None) == 1   # GDN_ERR_NULL, nothing launched
 

@@ -111,6 +111,22 @@ def test_cp_batch_invariance_and_tilings():
         assert_bits_equal(h1, h_b[n:n + 1], "state of sequence %d alone vs in the batch" % n)
 
 
+def test_cp_range_hint():
+    """The range hint follows the wave arithmetic of the two passes: a single-chunk
+    sequence cannot be split, the 27B layer's 4096 tokens over 48 v-heads already fill
+    the SMs (when there are fewer than 3 * 48 * 2 of them), one 32768-token sequence over
+    6 v-heads is split, and the hint depends on the sequence alone (the same answer
+    whenever asked)."""
+    hint = gdn.gdn_chunk_prefill_cp_range_hint
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert hint(64, 6) == 0
+    if sms < 3 * 48 * 2:
+        assert hint(4096, 48) == 0
+    r = hint(32768, 6)
+    assert 0 < r < 512
+    assert hint(32768, 6) == r
+
+
 def test_cp_27b_shapes_sampled_heads():
     """27B head shapes (Hk = 16, Hv = 48), one 4096-token sequence from a random state,
     in ranges of 16 chunks; the oracle runs three sampled v-heads of different k-heads."""
