@@ -85,8 +85,9 @@ struct TcParams {
     //   cp = 1: grid z = 2 n_ranges.  z < n_ranges: range z from its first state (the
     //           sequence's initial state for a sequence's first range, else zero), end
     //           state to sA (to hT when the range is the whole sequence), O only for first
-    //           ranges.  z >= n_ranges: the transition map of range z - n_ranges (V taken
-    //           as zero, start = I), to sP; first and last ranges need none.
+    //           ranges; the last of several ranges is skipped (no composition reads its
+    //           end state).  z >= n_ranges: the transition map of range z - n_ranges (V
+    //           taken as zero, start = I), to sP; first and last ranges need none.
     //   cp = 2: grid z = n_ranges.  Every range but a first from its start state in sS,
     //           O stored, a last range's end state to hT.
     int cp;
@@ -1240,8 +1241,11 @@ __device__ __forceinline__ void state_kernel_body(const TcMaps &maps, const TcPa
         job.h0 = nullptr;
         job.hT = nullptr;
         if (p.cp == 1 && !trans) {
+            // a later sequence's last range: its end state from zero would feed no
+            // composition (nothing follows it), so the first pass skips it
+            job.active = first || !last;
             job.h0 = first && p.h0 ? p.h0 + ((size_t)seq * p.Hv + hv) * hd : nullptr;
-            job.hT = first && last ? hT_seq : p.sA + roff;
+            job.hT = first && last ? hT_seq : (job.active ? p.sA + roff : nullptr);
             job.write_o = first;
         } else if (p.cp == 1) {
             job.active = !first && !last;
@@ -1626,7 +1630,8 @@ int32_t cp_range_hint(int64_t seq_len, int32_t Hv) {
         if (2 * nr > 65535) continue;
         const int64_t mid = nr > 2 ? nr - 2 : 0;
         const int64_t t = tiles(2 * nr);
-        const int64_t cost = (waves(t * Hv * (nr + mid)) + waves(t * Hv * (nr - 1))) * (r + kCpCta) +
+        // first pass: every range but the last, and the middle ranges' transition maps
+        const int64_t cost = (waves(t * Hv * (nr - 1 + mid)) + waves(t * Hv * (nr - 1))) * (r + kCpCta) +
                              kCpPerRange * nr + kCpFixed;
         if (cost < best) {
             best = cost;
