@@ -161,8 +161,6 @@ __device__ __forceinline__ void tmem_row32(uint32_t taddr, float (&v)[32]) {
     tc::tmem_wait_ld();
 }
 
-// Sum of squares of one 128-element bf16 row held in a K-major tile of two 64-wide
-// blocks (block stride `blk` bytes), fixed order.
 // Packed fp32 pair arithmetic (two lanes per instruction), rounded like the scalar ops.
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     float2 d;
@@ -190,6 +188,8 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
     return d;
 }
 
+// Sum of squares of one 128-element bf16 row held in a K-major tile of two 64-wide
+// blocks (block stride `blk` bytes), fixed order.
 __device__ __forceinline__ float row_sumsq(const uint8_t *tile, int row, uint32_t blk) {
     float acc = 0.f;
 #pragma unroll
@@ -832,7 +832,7 @@ __device__ __forceinline__ void state_cta(StateSmem &S, const TcMaps &maps, cons
         constexpr uint32_t id3 = tc::idesc_bf16(128, 2 * NT, 1, 1);
         const bool leader = lane == 0;
         bool ok = true;   // meaningful in lane 0
-        // lane 0's verdict, broadcast: go on issuing unless a wait ran out
+        // lane 0's wait result, broadcast: go on issuing unless a wait ran out
         auto go = [&]() { return __shfl_sync(0xffffffffu, (ok && !*abort) ? 1 : 0, 0) != 0; };
         // A chunk's tiles are waited for before the barrier that publishes its h: for
         // chunk c+1 right after chunk c's state update is issued, while the compute warps
