@@ -1318,11 +1318,11 @@ __global__ void cp_tables_kernel(const int32_t *cu, int N, int range_chunks, int
 // sequence), one thread per dk row.  S = the first range's end state; for each later
 // range r: its start is S, then S <- P_r S + R_r (fp32, k in increasing order).  The
 // chain is sequential over ranges, so its step time is what counts: the next P (64 KiB)
-// is copied into the other half of a shared-memory double buffer by 16-byte asynchronous
-// copies while the current step computes, and R_r is read before the wait for P_r.
+// and the next R columns (4 KiB) are copied into the other half of a shared-memory double
+// buffer by 16-byte asynchronous copies while the current step computes.
 constexpr int kComposeCols = 8;
 constexpr int kComposeLd = kD + 4;          // P rows, 16-byte aligned; float4 reads of a row
-constexpr size_t kComposeSmem = 2 * (size_t)kD * kComposeLd * 4 + (size_t)kD * kComposeCols * 4;
+constexpr size_t kComposeSmem = 2 * (size_t)kD * kComposeLd * 4 + 3 * (size_t)kD * kComposeCols * 4;
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
@@ -1335,6 +1335,8 @@ cp_compose_kernel(const float *sA, const float *sP, float *sS, const int32_t *se
     extern __shared__ __align__(16) float csm[];
     float (*Psm)[kD][kComposeLd] = reinterpret_cast<float (*)[kD][kComposeLd]>(csm);
     float (*Ssm)[kComposeCols] = reinterpret_cast<float (*)[kComposeCols]>(csm + 2 * kD * kComposeLd);
+    float (*Rsm)[kD][kComposeCols] =
+        reinterpret_cast<float (*)[kD][kComposeCols]>(csm + 2 * kD * kComposeLd + kD * kComposeCols);
     grid_dependents_launch();
     grid_dependency_wait();
     const int j0 = blockIdx.x * kComposeCols, hv = blockIdx.y, n = blockIdx.z;
@@ -1344,13 +1346,17 @@ cp_compose_kernel(const float *sA, const float *sP, float *sS, const int32_t *se
     if (R <= 1) return;
     const size_t hd = (size_t)kD * kD;
     auto head = [&](const float *base, int range) { return base + ((size_t)range * Hv + hv) * hd; };
-    // P of range idx into buffer b: 4096 16-byte pieces, 32 per thread, one commit group
+    // P of range idx (4096 16-byte pieces, 32 per thread) and this CTA's columns of its R
+    // (two pieces per thread: its own row) into buffer b, one commit group
     auto fetch_p = [&](int idx, int b) {
         const float *P = head(sP, idx);
         for (int c = i; c < kD * kD / 4; c += kD) {
             const int row = c / (kD / 4), col = 4 * (c % (kD / 4));
             cp_async16(&Psm[b][row][col], P + (size_t)row * kD + col);
         }
+        const float *Rr = head(sA, idx) + (size_t)i * kD + j0;
+        cp_async16(&Rsm[b][i][0], Rr);
+        cp_async16(&Rsm[b][i][4], Rr + 4);
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
     if (R > 2) fetch_p(first + 1, 1);
@@ -1368,15 +1374,11 @@ cp_compose_kernel(const float *sA, const float *sP, float *sS, const int32_t *se
             dst[1] = make_float4(Ssm[i][4], Ssm[i][5], Ssm[i][6], Ssm[i][7]);
         }
         if (r == R - 1) break;
-        float acc[kComposeCols];
-        {
-            const float4 *src = reinterpret_cast<const float4 *>(head(sA, idx) + (size_t)i * kD + j0);
-            const float4 a = src[0], b = src[1];
-            acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
-            acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
-        }
         asm volatile("cp.async.wait_group 0;" ::: "memory");
-        __syncthreads();                       // P_idx in buffer r & 1, visible to all
+        __syncthreads();                       // P_idx and R_idx in buffer r & 1, visible to all
+        float acc[kComposeCols];
+#pragma unroll
+        for (int j = 0; j < kComposeCols; ++j) acc[j] = Rsm[r & 1][i][j];
         if (r + 1 < R - 1) fetch_p(idx + 1, (r + 1) & 1);
         const float *prow = Psm[r & 1][i];
 #pragma unroll 4
