@@ -210,6 +210,52 @@ def test_prefill_no_tokens_at_all(simt):
     assert torch.equal(hT.cpu(), x["initial_state"])
 
 
+@pytest.mark.parametrize("case", ["beta0", "forget", "nodecay"])
+def test_prefill_degenerate_gates(case):
+    """The method's degenerate gates through the tensor-core path, against the oracle:
+    beta = 0 (nothing is written, the state only decays: o_t = e^{gamma_t} q_t . S0),
+    g = -30 at every token (the state forgets all but the newest write, so
+    o_t = beta_t (k_t . q_t) v_t, with decays that underflow to exact zeros), and g = 0
+    (no decay: the plain delta rule)."""
+    lens = [130, 64, 1, 77]
+    x = inputs.scan_inputs(61, lens, 2, 6, 128, 128, g_shift=-3.0, init_state_std=0.05)
+    if case == "beta0":
+        x["beta"] = torch.zeros_like(x["beta"])
+    elif case == "forget":
+        x["g"] = torch.full_like(x["g"], -30.0)
+    else:
+        x["g"] = torch.zeros_like(x["g"])
+    o, hT = run_prefill(x)
+    o_ref, h_ref = ref_prefill(x)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(hT).all()
+    assert_out_close(o, o_ref)
+    assert_state_close(hT, h_ref)
+
+
+def test_prefill_65535_sequences():
+    """The most sequences one call takes (N = 65535, the state pass's grid limit), almost
+    all empty: every empty sequence ends with its (zero) initial state exactly, and the
+    40 non-empty ones, spread over the batch, match the oracle."""
+    N = 65535
+    rng = np.random.default_rng(62)
+    lens = np.zeros(N, np.int64)
+    busy = np.sort(rng.choice(N, 40, replace=False))
+    lens[busy] = rng.integers(1, 140, 40)
+    x = inputs.scan_inputs(62, lens.tolist(), 1, 1, 128, 128)
+    o, hT = run_prefill(x)
+    torch.cuda.synchronize()
+    empty = torch.ones(N, dtype=torch.bool, device="cuda")
+    empty[torch.from_numpy(busy).cuda()] = False
+    assert int(torch.count_nonzero(hT[empty])) == 0
+    # the oracle on the non-empty sequences alone: their tokens are the whole packed
+    # batch, in the same order
+    xb = dict(x)
+    xb["cu_seqlens"] = torch.from_numpy(np.concatenate([[0], np.cumsum(lens[busy])]).astype(np.int32))
+    o_ref, h_ref = ref_prefill(xb)
+    assert_out_close(o, o_ref)
+    assert_state_close(hT[torch.from_numpy(busy).cuda()], h_ref)
+
+
 @pytest.mark.parametrize("simt", [True, False])
 def test_prefill_weak_decay_long(simt):
     """g = -softplus(N(0,1) - 3): long memory, errors carried across many chunks."""
