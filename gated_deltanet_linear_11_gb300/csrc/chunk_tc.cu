@@ -221,39 +221,43 @@ __device__ __forceinline__ float fast_exp2(float x) {
 //     T10 = -T11 A10 T00,   T32 = -T33 A32 T22,
 //     [T20 T21; T30 T31] = -T1 [A20 A21; A30 A31] T0.
 // Each block of A is read for the last time before the block of T at the same place is
-// written, with a barrier in between.  Every product is a 16x16 block computed by 64
-// threads holding 2x2 register tiles.  All 128 threads call this; Y ([64][kLdY]) is a
-// scratch for the 16- and 32-column intermediates.
+// written, with a barrier in between.  Every product is a 16x16 block computed by one
+// warp whose lanes hold 2x4 register tiles (two A values and four B values per step feed
+// eight FMAs).  All 128 threads call this; Y ([64][kLdY]) is a scratch for the 16- and
+// 32-column intermediates.
 constexpr int kLd = 66;
 constexpr int kLdY = 34;
 
-// acc += A[ar.., ac..] (16x16) * B[br.., bc..] (16x16) for this thread's 2x2 tile.
+// acc += A[ar.., ac..] (16x16) * B[br.., bc..] (16x16) for this lane's 2x4 tile: rows
+// 2 tr, 2 tr + 1 and columns 4 tc .. 4 tc + 3 of the block, k in increasing order.
+// Partly unrolled: the prep kernel's code size shows up as instruction-fetch stalls.
 template <int LA, int LB>
-__device__ __forceinline__ void blk_mma(float (&acc)[2][2], const float (*A)[LA], int ar, int ac,
-                                        const float (*B)[LB], int br, int bc, int tr, int tc) {
-    // partly unrolled: nine call sites, and the prep kernel's code size shows up as
-    // instruction-fetch stalls
+__device__ __forceinline__ void blk_mma(float (&acc)[2][4], const float (*A)[LA], int ar, int ac,
+                                          const float (*B)[LB], int br, int bc, int tr, int tc) {
 #pragma unroll 4
     for (int m = 0; m < 16; ++m) {
         const float a0 = A[ar + 2 * tr][ac + m], a1 = A[ar + 2 * tr + 1][ac + m];
-        const float2 bb = *reinterpret_cast<const float2 *>(&B[br + m][bc + 2 * tc]);
-        acc[0][0] = fmaf(a0, bb.x, acc[0][0]);
-        acc[0][1] = fmaf(a0, bb.y, acc[0][1]);
-        acc[1][0] = fmaf(a1, bb.x, acc[1][0]);
-        acc[1][1] = fmaf(a1, bb.y, acc[1][1]);
+        const float2 b01 = *reinterpret_cast<const float2 *>(&B[br + m][bc + 4 * tc]);
+        const float2 b23 = *reinterpret_cast<const float2 *>(&B[br + m][bc + 4 * tc + 2]);
+        acc[0][0] = fmaf(a0, b01.x, acc[0][0]); acc[0][1] = fmaf(a0, b01.y, acc[0][1]);
+        acc[0][2] = fmaf(a0, b23.x, acc[0][2]); acc[0][3] = fmaf(a0, b23.y, acc[0][3]);
+        acc[1][0] = fmaf(a1, b01.x, acc[1][0]); acc[1][1] = fmaf(a1, b01.y, acc[1][1]);
+        acc[1][2] = fmaf(a1, b23.x, acc[1][2]); acc[1][3] = fmaf(a1, b23.y, acc[1][3]);
     }
 }
-
 template <int LD>
 __device__ __forceinline__ void blk_store(float (*D)[LD], int dr, int dc, int tr, int tc,
-                                          const float (&acc)[2][2], float sgn) {
-    *reinterpret_cast<float2 *>(&D[dr + 2 * tr][dc + 2 * tc]) = make_float2(sgn * acc[0][0], sgn * acc[0][1]);
-    *reinterpret_cast<float2 *>(&D[dr + 2 * tr + 1][dc + 2 * tc]) = make_float2(sgn * acc[1][0], sgn * acc[1][1]);
+                                            const float (&acc)[2][4], float sgn) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        *reinterpret_cast<float2 *>(&D[dr + 2 * tr + i][dc + 4 * tc]) = make_float2(sgn * acc[i][0], sgn * acc[i][1]);
+        *reinterpret_cast<float2 *>(&D[dr + 2 * tr + i][dc + 4 * tc + 2]) = make_float2(sgn * acc[i][2], sgn * acc[i][3]);
+    }
 }
 
 __device__ void tinv64_inplace(float (*AT)[kLd], float (*Y)[kLdY]) {
     const int tid = threadIdx.x;
-    const int half = tid >> 6, t = tid & 63, tr = t >> 3, tc = t & 7;
+    const int w = tid >> 5, lane = tid & 31, tr = lane >> 2, tc = lane & 3;
     {   // diagonal blocks by forward substitution, one column per thread
         const int b = (tid >> 4) & 3, j = tid & 15, o = 16 * b;
         float x[16];
@@ -268,51 +272,50 @@ __device__ void tinv64_inplace(float (*AT)[kLd], float (*Y)[kLdY]) {
                 x[r] = acc;
             }
         }
-        __syncthreads();                       // every read of the A_ii is done
+        __syncthreads();
         if (tid < 64) {
 #pragma unroll
             for (int r = 0; r < 16; ++r) AT[o + r][o + j] = x[r];
         }
     }
     __syncthreads();
-    {   // X = A10 T00 (half 0) and A32 T22 (half 1), into Y rows 32.. and 48..
-        float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-        const int o = 32 * half;
+    if (w < 2) {   // X = A10 T00 (warp 0) and A32 T22 (warp 1), into Y rows 32.. and 48..
+        float acc[2][4] = {};
+        const int o = 32 * w;
         blk_mma(acc, AT, o + 16, o, AT, o, o, tr, tc);
-        blk_store(Y, 32 + 16 * half, 0, tr, tc, acc, 1.f);
+        blk_store(Y, 32 + 16 * w, 0, tr, tc, acc, 1.f);
     }
     __syncthreads();
-    {   // T10 = -T11 X over A10,  T32 = -T33 X over A32
-        float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-        const int o = 32 * half;
-        blk_mma(acc, AT, o + 16, o + 16, Y, 32 + 16 * half, 0, tr, tc);
+    if (w < 2) {   // T10 = -T11 X over A10,  T32 = -T33 X over A32
+        float acc[2][4] = {};
+        const int o = 32 * w;
+        blk_mma(acc, AT, o + 16, o + 16, Y, 32 + 16 * w, 0, tr, tc);
         blk_store(AT, o + 16, o, tr, tc, acc, -1.f);
     }
     __syncthreads();
-    {   // Z = [A20 A21; A30 A31] T0 into Y[0:32][0:32]; half h makes block row h
-        const int ar = 32 + 16 * half;
-        float z0[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, z1[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-        blk_mma(z0, AT, ar, 0, AT, 0, 0, tr, tc);     // A_r0 T00
-        blk_mma(z0, AT, ar, 16, AT, 16, 0, tr, tc);   // + A_r1 T10
-        blk_mma(z1, AT, ar, 16, AT, 16, 16, tr, tc);  // A_r1 T11
-        blk_store(Y, 16 * half, 0, tr, tc, z0, 1.f);
-        blk_store(Y, 16 * half, 16, tr, tc, z1, 1.f);
+    {   // Z = [A20 A21; A30 A31] T0 into Y[0:32][0:32]; warp w: block row w >> 1, column w & 1
+        const int half = w >> 1, which = w & 1, ar = 32 + 16 * half;
+        float acc[2][4] = {};
+        if (which == 0) {
+            blk_mma(acc, AT, ar, 0, AT, 0, 0, tr, tc);     // A_r0 T00
+            blk_mma(acc, AT, ar, 16, AT, 16, 0, tr, tc);   // + A_r1 T10
+        } else {
+            blk_mma(acc, AT, ar, 16, AT, 16, 16, tr, tc);  // A_r1 T11
+        }
+        blk_store(Y, 16 * half, 16 * which, tr, tc, acc, 1.f);
     }
     __syncthreads();
-    {   // [T20 T21; T30 T31] = -T1 Z over A2x, A3x; half h makes block row 2 + h
-        float w0[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, w1[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    {   // [T20 T21; T30 T31] = -T1 Z; warp w: block row 2 + (w >> 1), column w & 1
+        const int half = w >> 1, which = w & 1;
+        float acc[2][4] = {};
         if (half == 0) {
-            blk_mma(w0, AT, 32, 32, Y, 0, 0, tr, tc);    // T22 Z20
-            blk_mma(w1, AT, 32, 32, Y, 0, 16, tr, tc);   // T22 Z21
+            blk_mma(acc, AT, 32, 32, Y, 0, 16 * which, tr, tc);    // T22 Z2x
         } else {
-            blk_mma(w0, AT, 48, 32, Y, 0, 0, tr, tc);    // T32 Z20
-            blk_mma(w0, AT, 48, 48, Y, 16, 0, tr, tc);   // + T33 Z30
-            blk_mma(w1, AT, 48, 32, Y, 0, 16, tr, tc);   // T32 Z21
-            blk_mma(w1, AT, 48, 48, Y, 16, 16, tr, tc);  // + T33 Z31
+            blk_mma(acc, AT, 48, 32, Y, 0, 16 * which, tr, tc);    // T32 Z2x
+            blk_mma(acc, AT, 48, 48, Y, 16, 16 * which, tr, tc);   // + T33 Z3x
         }
         // the stores go to columns 0..31, which no thread reads in this step
-        blk_store(AT, 32 + 16 * half, 0, tr, tc, w0, -1.f);
-        blk_store(AT, 32 + 16 * half, 16, tr, tc, w1, -1.f);
+        blk_store(AT, 32 + 16 * half, 16 * which, tr, tc, acc, -1.f);
     }
     __syncthreads();
 }
@@ -503,7 +506,11 @@ chunk_prep_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ T
         for (int hf = 0; hf < 2; ++hf) {
             float lrow[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) lrow[i] = (32 * hf + i < r) ? AT[r][32 * hf + i] : 0.f;
+            for (int i = 0; i < 32; i += 2) {   // two columns per load
+                const float2 t2 = *reinterpret_cast<const float2 *>(&AT[r][32 * hf + i]);
+                lrow[i] = (32 * hf + i < r) ? t2.x : 0.f;
+                lrow[i + 1] = (32 * hf + i + 1 < r) ? t2.y : 0.f;
+            }
             pack_row<32>(S.x(), tid, 4 * hf, lrow);
         }
     } else if (ok) {
