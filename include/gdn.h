@@ -23,10 +23,11 @@
  *    oldest first, in the activation dtype (bf16).
  *  * v-head h reads q/k head h / (Hv / Hk).  g and beta are per v-head, fp32 [T, Hv].
  *  * Every device pointer and stream is owned by the caller.  The library allocates no
- *    device or pinned memory and keeps no global state beyond per-device cached properties
- *    (SM count, kernel attributes set once) and driver entry points.  Inputs are read-only; only the documented outputs are
- *    written.  All calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
- *    default stream) and may be issued from several host threads.
+ *    device or pinned memory and keeps no global state beyond per-device cached
+ *    properties (SM count, kernel attributes set once) and driver entry points.  Inputs
+ *    are read-only; only the documented outputs are written.  All calls are asynchronous
+ *    on `stream` (a cudaStream_t; NULL = legacy default stream) and may be issued from
+ *    several host threads.
  *  * Validation failures return before anything is launched.  Launch failures return
  *    GDN_ERR_CUDA.  Errors found on the device (an out-of-range state index) are
  *    written to the optional device int `status_dev` (0 untouched = OK), which the
