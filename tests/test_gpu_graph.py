@@ -122,11 +122,11 @@ def test_fused_decode_graph_replay_matches_eager():
     assert_bits_equal(cs, cs_e, "fused graph conv state")
 
 
-@pytest.mark.parametrize("use_side", [True, False])
+@pytest.mark.parametrize("use_side", [True, False, "fused"])
 def test_layer_prefill_graph_replay_matches_eager(use_side):
     """gdn_layer_prefill captured once in a CUDA graph (with a side stream, that stream
-    forks from and joins the capturing stream; without one, one stream) and replayed on
-    new inputs gives the eager call's bits."""
+    forks from and joins the capturing stream; without one, one stream; with the v conv
+    fused into the state pass) and replayed on new inputs gives the eager call's bits."""
     s = dict(Hk=2, Hv=4, dk=128, dv=128)
     C = inputs.conv_channels(**s)
     lens = [150, 0, 183]
@@ -149,14 +149,15 @@ def test_layer_prefill_graph_replay_matches_eager(use_side):
     ws_bytes = gdn.gdn_chunk_prefill_workspace_size(N, T, s["Hk"], s["Hv"], 128, 128, 64)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    v_stream = torch.cuda.Stream() if use_side else None
+    v_stream = torch.cuda.Stream() if use_side is True else None
 
     def call(x, out):
         o, hT, cs_out, y = out
         gdn.gdn_layer_prefill(x, w, bias, g, beta, cu, s["Hk"], s["Hv"], 128, 128,
                               conv_state_in=cs_in, conv_state_out=cs_out, initial_state=h0,
                               final_state=hT, scale=0.5, y=y, o=o, cu_seqlens_host=cu_h,
-                              workspace=ws, status=status, side_stream=v_stream)
+                              workspace=ws, status=status, side_stream=v_stream,
+                              fused_vconv=use_side == "fused")
 
     eager = []
     for x in xs:
