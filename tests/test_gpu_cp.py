@@ -143,3 +143,49 @@ def test_cp_27b_shapes_sampled_heads():
             initial_state=x["initial_state"][:, hv:hv + 1])
         assert_out_close(o[:, hv:hv + 1], o_ref, what="cp o head %d" % hv)
         assert_state_close(hT[:, hv:hv + 1], h_ref, what="cp state head %d" % hv)
+
+
+def test_cp_graph_replay_matches_eager():
+    """gdn_chunk_prefill_cp captured once in a CUDA graph (its table, prep, two state and
+    composition launches, no host synchronisation) and replayed on new inputs gives the
+    eager call's bits."""
+    lens = [700, 0, 190]
+    xs = [inputs.scan_inputs(110 + i, lens, 2, 6, 128, 128, init_state_std=0.02)
+          for i in range(3)]
+    cu_h = xs[0]["cu_seqlens"]
+    T, N = int(cu_h[-1]), len(lens)
+    ws = torch.empty(max(gdn.gdn_chunk_prefill_cp_workspace_size(cu_h, T, 2, 6, 128, 128, 2),
+                         256), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    static = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in xs[0].items()}
+    o = torch.empty((T, 6, 128), dtype=torch.bfloat16, device="cuda")
+    hT = torch.empty((N, 6, 128, 128), dtype=torch.float32, device="cuda")
+
+    def call():
+        gdn.gdn_chunk_prefill_cp(static["q"], static["k"], static["v"], static["g"],
+                                 static["beta"], static["cu_seqlens"], 2,
+                                 initial_state=static["initial_state"], o=o, final_state=hT,
+                                 cu_seqlens_host=cu_h, workspace=ws, status=status)
+
+    eager = []
+    for x in xs:
+        for key in ("q", "k", "v", "g", "beta", "initial_state"):
+            static[key].copy_(x[key])
+        call()
+        eager.append((o.clone(), hT.clone()))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for i, x in enumerate(xs):
+        for key in ("q", "k", "v", "g", "beta", "initial_state"):
+            static[key].copy_(x[key])
+        graph.replay()
+        torch.cuda.synchronize()
+        assert_bits_equal(o, eager[i][0], "cp graph replay %d o" % i)
+        assert_bits_equal(hT, eager[i][1], "cp graph replay %d final state" % i)
+    assert int(status.item()) == 0
