@@ -183,11 +183,15 @@ def gdn_chunk_prefill_cp_workspace_size(cu_seqlens_host, T, Hk, Hv, dk, dv, rang
         range_chunks))
 
 
-def gdn_chunk_prefill_cp_range_hint(seq_len, Hv):
+def gdn_chunk_prefill_cp_range_hint(seq_len, Hv, sm_count=None):
     """range_chunks for one sequence of ``seq_len`` tokens over ``Hv`` v-heads alone on
-    the current device, or 0 when the plain scan is expected to be as fast (C entry
-    gdn_chunk_prefill_cp_range_hint; depends on the sequence's own length only)."""
-    return int(_lib.load().gdn_chunk_prefill_cp_range_hint(int(seq_len), int(Hv)))
+    the current device (or on one with ``sm_count`` SMs), or 0 when the plain scan is
+    expected to be as fast (C entries gdn_chunk_prefill_cp_range_hint and
+    gdn_chunk_prefill_cp_range_hint_for; depends on the sequence's own length only)."""
+    lib = _lib.load()
+    if sm_count is None:
+        return int(lib.gdn_chunk_prefill_cp_range_hint(int(seq_len), int(Hv)))
+    return int(lib.gdn_chunk_prefill_cp_range_hint_for(int(seq_len), int(Hv), int(sm_count)))
 
 
 def gdn_chunk_prefill_cp(q, k, v, g, beta, cu_seqlens, range_chunks, chunk=64, scale=1.0,

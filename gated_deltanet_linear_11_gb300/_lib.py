@@ -25,7 +25,8 @@ STATUS = {
 EXPORTS = ("gdn_status_string", "gdn_version", "gdn_conv1d_fwd", "gdn_conv1d_update",
            "gdn_chunk_prefill_workspace_size", "gdn_chunk_prefill",
            "gdn_chunk_prefill_noalloc", "gdn_chunk_prefill_cp_workspace_size",
-           "gdn_chunk_prefill_cp", "gdn_chunk_prefill_cp_range_hint", "gdn_recurrent_decode", "gdn_fused_decode",
+           "gdn_chunk_prefill_cp", "gdn_chunk_prefill_cp_range_hint",
+           "gdn_chunk_prefill_cp_range_hint_for", "gdn_recurrent_decode", "gdn_fused_decode",
            "gdn_layer_prefill", "gdn_selftest_bounded_wait")
 
 NOALLOC_SCRATCH_BYTES = 128 << 20
@@ -74,6 +75,7 @@ def load(path: str = LIB_PATH):
         "gdn_chunk_prefill_cp": ([tp, tp, tp, vp, vp, vp, vp, i32, i32, f32, u32, i32, vp, tp,
                                   vp, vp, ctypes.c_size_t, vp, vp], i32),
         "gdn_chunk_prefill_cp_range_hint": ([i64, i32], i32),
+        "gdn_chunk_prefill_cp_range_hint_for": ([i64, i32, i32], i32),
         "gdn_recurrent_decode": ([tp, tp, tp, vp, vp, vp, i32, vp, f32, u32, tp, vp, vp],
                                  i32),
         "gdn_fused_decode": ([vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp,

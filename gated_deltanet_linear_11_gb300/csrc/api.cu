@@ -249,6 +249,10 @@ int32_t gdn_chunk_prefill_cp_range_hint(int64_t seq_len, int32_t Hv) {
     return gdn_host::cp_range_hint(seq_len, Hv);
 }
 
+int32_t gdn_chunk_prefill_cp_range_hint_for(int64_t seq_len, int32_t Hv, int32_t sm_count) {
+    return gdn_host::cp_range_hint(seq_len, Hv, sm_count);
+}
+
 gdn_status_t gdn_chunk_prefill_cp(const gdn_tensor_t *q, const gdn_tensor_t *k,
                                   const gdn_tensor_t *v, const float *g, const float *beta,
                                   const int32_t *cu_seqlens_dev,

@@ -1625,9 +1625,8 @@ CpLayout cp_layout(int64_t nr, int32_t N, int64_t T, int32_t Hk, int32_t Hv) {
 // plain scan and the 32-, 64- and 74-chunk splits of one 32768-token sequence over 6
 // v-heads on the GB300 (the fit reproduces those three times within 1%).  0 when the
 // plain scan is expected to be at least as fast.
-int32_t cp_range_hint(int64_t seq_len, int32_t Hv) {
+int32_t cp_range_hint(int64_t seq_len, int32_t Hv, int32_t sms) {
     constexpr int64_t kCpCta = 1, kCpPerRange = 2, kCpFixed = 18;
-    const int sms = sm_count();
     if (sms <= 0 || Hv <= 0 || seq_len <= 0) return 0;
     const int64_t nch = (seq_len + gdn::kC - 1) / gdn::kC;
     auto tiles = [&](int64_t chains) -> int64_t { return 3 * Hv * chains <= sms ? 3 : 2; };
@@ -1648,6 +1647,10 @@ int32_t cp_range_hint(int64_t seq_len, int32_t Hv) {
         }
     }
     return best_r;
+}
+
+int32_t cp_range_hint(int64_t seq_len, int32_t Hv) {
+    return cp_range_hint(seq_len, Hv, sm_count());
 }
 
 size_t chunk_tc_cp_workspace(const int32_t *cu_host, int32_t N, int64_t T, int32_t Hk,

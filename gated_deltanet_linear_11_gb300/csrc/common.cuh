@@ -131,8 +131,10 @@ size_t chunk_tc_workspace(int32_t N, int64_t T, int32_t Hk, int32_t Hv);
 // host copy of cu).  Workspace bytes (0 when the arguments are invalid) and the launch.
 size_t chunk_tc_cp_workspace(const int32_t *cu_host, int32_t N, int64_t T, int32_t Hk,
                              int32_t Hv, int32_t range_chunks);
-// range length for one sequence of seq_len tokens alone on the current device (0: plain)
+// range length for one sequence of seq_len tokens alone on the current device, or on a
+// device with sms SMs (0: plain)
 int32_t cp_range_hint(int64_t seq_len, int32_t Hv);
+int32_t cp_range_hint(int64_t seq_len, int32_t Hv, int32_t sms);
 gdn_status_t launch_chunk_tc_cp(const ScanArgs &a, const int32_t *cu_host, int32_t range_chunks,
                                 cudaStream_t st);
 // one CTA whose bounded mbarrier wait runs out (GDN_ERR_TIMEOUT into *status)

@@ -206,6 +206,10 @@ size_t gdn_chunk_prefill_cp_workspace_size(const int32_t *cu_seqlens_host, int32
  */
 int32_t gdn_chunk_prefill_cp_range_hint(int64_t seq_len, int32_t Hv);
 
+/* The same estimate for a device with sm_count SMs (e.g. planning for another GPU); no
+ * CUDA call is made.  0 when an argument is not positive. */
+int32_t gdn_chunk_prefill_cp_range_hint_for(int64_t seq_len, int32_t Hv, int32_t sm_count);
+
 gdn_status_t gdn_chunk_prefill_cp(const gdn_tensor_t *q, const gdn_tensor_t *k,
                                   const gdn_tensor_t *v, const float *g, const float *beta,
                                   const int32_t *cu_seqlens_dev,

@@ -228,6 +228,24 @@ def test_cp_rejections(lib):
     assert cp_prefill(lib, qh, k, v, o, [0, 8], 1, 2) == 3
 
 
+def test_cp_range_hint_model(lib):
+    """The range hint's wave-count model with an explicit SM count (no device needed):
+    on 152 SMs one 32768-token sequence over 6 v-heads splits into 40-chunk ranges (the
+    length measured fastest on the GB300), the 27B layer's 4096 tokens over 48 v-heads and
+    any single-chunk sequence stay plain, every SM count gets a valid range length (or
+    0), and bad arguments answer 0."""
+    f = lib.gdn_chunk_prefill_cp_range_hint_for
+    assert f(32768, 6, 152) == 40
+    assert f(4096, 48, 152) == 0
+    assert f(64, 6, 152) == 0 and f(1, 1, 152) == 0
+    assert f(32768, 6, 0) == 0 and f(0, 6, 152) == 0 and f(32768, 0, 152) == 0
+    for sms in (8, 32, 76, 152, 304):
+        r = f(32768, 6, sms)
+        assert 0 <= r < 512
+    # a sequence whose chains fill the device on their own is never split
+    assert f(4096, 64, 64) == 0
+
+
 def test_cp_range_hint_without_device(lib):
     """The range hint is a host-side estimate that needs the device's SM count: without a
     current device, and for arguments that are not positive, it answers 0 (the plain

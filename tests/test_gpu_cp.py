@@ -125,6 +125,7 @@ def test_cp_range_hint():
     r = hint(32768, 6)
     assert 0 < r < 512
     assert hint(32768, 6) == r
+    assert hint(32768, 6, sm_count=sms) == r     # the device's own SM count
 
 
 def test_cp_27b_shapes_sampled_heads():
