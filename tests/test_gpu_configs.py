@@ -108,7 +108,8 @@ def test_mix_4b_batch_invariance_bits_and_oracle_subset():
     xg = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     # the whole prefill batch in one call, in a shuffled order of sequences
     perm = np.random.default_rng(9).permutation(N)
-    tok_p = np.concatenate([np.arange(cu[i], cu[i + 1]) for i in perm])
+    cu_np = cu.numpy().astype(np.int64)
+    tok_p = np.concatenate([np.arange(cu_np[i], cu_np[i + 1]) for i in perm])
     cu_p = np.zeros(N + 1, np.int32)
     cu_p[1:] = np.cumsum([int(cu[i + 1] - cu[i]) for i in perm])
     tp = torch.from_numpy(tok_p).cuda()
