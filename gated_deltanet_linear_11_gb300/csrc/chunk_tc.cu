@@ -1633,15 +1633,19 @@ int32_t cp_range_hint(int64_t seq_len, int32_t Hv, int32_t sms) {
     auto waves = [&](int64_t ctas) -> int64_t { return (ctas + sms - 1) / sms; };
     int64_t best = waves(tiles(1) * Hv) * (nch + kCpCta);
     int32_t best_r = 0;
-    for (int64_t r = 1; r < nch; ++r) {
+    // every range count the launches allow, each with the shortest range length that
+    // gives it (a longer one only costs more)
+    for (int64_t want = 2; want <= std::min<int64_t>(nch, 65535 / 2); ++want) {
+        const int64_t r = (nch + want - 1) / want;
         const int64_t nr = (nch + r - 1) / r;
-        if (2 * nr > 65535) continue;
+        if (nr != want) continue;               // this count is not reachable exactly
         const int64_t mid = nr > 2 ? nr - 2 : 0;
         const int64_t t = tiles(2 * nr);
         // first pass: every range but the last, and the middle ranges' transition maps
         const int64_t cost = (waves(t * Hv * (nr - 1 + mid)) + waves(t * Hv * (nr - 1))) * (r + kCpCta) +
                              kCpPerRange * nr + kCpFixed;
-        if (cost < best) {
+        // ties go to the shorter range, never away from the plain scan
+        if (cost < best || (cost == best && best_r != 0)) {
             best = cost;
             best_r = (int32_t)r;
         }
