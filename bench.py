@@ -42,10 +42,11 @@ METRIC = "GDN prefill tokens/s per layer (% bf16 TC peak); decode step state GB/
 SHAPE = dict(Hk=16, Hv=48, dk=128, dv=128)
 CHUNK = 64
 # Pieces of the sequence in the e2e leg's copy / compute pipeline, in sixteenths of T.
-# The host link is the bound (all inputs take ~0.41 ms to copy in), so the pieces shrink
-# toward the end: what runs after the last copy-in (the last piece's layer and copy-out)
-# is short, and there are few pieces, each of which costs host time.
-E2E_SIXTEENTHS = (6, 6, 3, 1)
+# The host link is the bound (all inputs take ~0.41 ms to copy in, the outputs ~0.28 ms
+# out), so a small first piece lets the first copy-out start early, the pieces shrink
+# toward the end so that little runs after the last copy-in, and there are few pieces,
+# each of which costs host time.
+E2E_SIXTEENTHS = (2, 7, 5, 2)
 
 
 def prefill_flops_per_token(Hk, Hv, dk, dv, C=CHUNK):
