@@ -1322,90 +1322,128 @@ __global__ void cp_tables_kernel(const int32_t *cu, int N, int range_chunks, int
 }
 
 // Start states of a sequence's ranges, in order: one CTA per (8 dv columns, v-head,
-// sequence), one thread per dk row.  S = the first range's end state; for each later
-// range r: its start is S, then S <- P_r S + R_r (fp32, k in increasing order).  The
-// chain is sequential over ranges, so its step time is what counts: the next P (64 KiB)
-// and the next R columns (4 KiB) are copied into the other half of a shared-memory double
-// buffer by 16-byte asynchronous copies while the current step computes.
+// sequence).  S = the first range's end state; for each later range r: its start is S,
+// then S <- P_r S + R_r in fp32, each element as (((R + the k < 32 terms) + the
+// 32 <= k < 64 terms) + the 64 <= k < 96 terms) + the k >= 96 terms, every part in
+// increasing k.  The chain is sequential over ranges, so a step's latency is what counts:
+// a thread takes two dk rows (i, i + 64) of one k quarter, so each broadcast read of S
+// serves both rows; then every thread adds up the four quarters of 4 of the 1024 outputs.
+// P (64 KiB) and this CTA's R columns (4 KiB) of the next two ranges are in flight
+// (16-byte asynchronous copies into a three-deep ring) while the current step computes,
+// and the products run as packed fp32 pairs (fma.rn.f32x2, rounded like two fmaf).  P
+// rows are stored with their 16-byte groups permuted (group g of row i at g ^ (i & 7)),
+// so the eight rows a quarter-warp reads at once fall on distinct banks.
 constexpr int kComposeCols = 8;
-constexpr int kComposeLd = kD + 4;          // P rows, 16-byte aligned; float4 reads of a row
-constexpr size_t kComposeSmem = 2 * (size_t)kD * kComposeLd * 4 + 3 * (size_t)kD * kComposeCols * 4;
+constexpr int kComposeSplit = 4;                       // k quarters
+constexpr int kComposeThreads = kComposeSplit * kD / 2;
+constexpr int kComposeDepth = 3;                       // P / R ring slots
+constexpr size_t kComposeSmem = (size_t)kComposeDepth * kD * kD * 4 +
+                                (size_t)(1 + kComposeSplit + kComposeDepth) * kD * kComposeCols * 4;
+static_assert(kComposeSmem <= 227 * 1024, "composition ring exceeds shared memory");
+static_assert(kComposeThreads * 4 == kD * kComposeCols, "one float4 of S per thread");
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
                  :: "r"(tc::smem_u32(smem)), "l"(gmem) : "memory");
 }
 
-__global__ void __launch_bounds__(kD)
+__global__ void __launch_bounds__(kComposeThreads, 1)
 cp_compose_kernel(const float *sA, const float *sP, float *sS, const int32_t *seq_first,
                   int N, int Hv, int n_ranges) {
     extern __shared__ __align__(16) float csm[];
-    float (*Psm)[kD][kComposeLd] = reinterpret_cast<float (*)[kD][kComposeLd]>(csm);
-    float (*Ssm)[kComposeCols] = reinterpret_cast<float (*)[kComposeCols]>(csm + 2 * kD * kComposeLd);
+    float (*Psm)[kD][kD] = reinterpret_cast<float (*)[kD][kD]>(csm);
+    float *after_p = csm + kComposeDepth * kD * kD;
+    float (*Ssm)[kComposeCols] = reinterpret_cast<float (*)[kComposeCols]>(after_p);
+    float (*Hsm)[kD][kComposeCols] =
+        reinterpret_cast<float (*)[kD][kComposeCols]>(after_p + kD * kComposeCols);
     float (*Rsm)[kD][kComposeCols] =
-        reinterpret_cast<float (*)[kD][kComposeCols]>(csm + 2 * kD * kComposeLd + kD * kComposeCols);
+        reinterpret_cast<float (*)[kD][kComposeCols]>(after_p + (1 + kComposeSplit) * kD * kComposeCols);
     grid_dependents_launch();
     grid_dependency_wait();
     const int j0 = blockIdx.x * kComposeCols, hv = blockIdx.y, n = blockIdx.z;
-    const int i = threadIdx.x;
+    const int i = threadIdx.x & (kD / 2 - 1), kq = threadIdx.x / (kD / 2);   // rows i, i + 64
+    const int orow = threadIdx.x >> 1, ocol = 4 * (threadIdx.x & 1);         // the float4 it sums
     const int first = seq_first[n];
     const int R = (n + 1 < N ? seq_first[n + 1] : n_ranges) - first;
     if (R <= 1) return;
     const size_t hd = (size_t)kD * kD;
     auto head = [&](const float *base, int range) { return base + ((size_t)range * Hv + hv) * hd; };
-    // P of range idx (4096 16-byte pieces, 32 per thread) and this CTA's columns of its R
-    // (two pieces per thread: its own row) into buffer b, one commit group
-    auto fetch_p = [&](int idx, int b) {
-        const float *P = head(sP, idx);
-        for (int c = i; c < kD * kD / 4; c += kD) {
-            const int row = c / (kD / 4), col = 4 * (c % (kD / 4));
-            cp_async16(&Psm[b][row][col], P + (size_t)row * kD + col);
+    auto start = [&](int range) { return sS + ((size_t)range * Hv + hv) * hd + (size_t)orow * kD + j0 + ocol; };
+    // Step r (1 <= r <= R - 2) reads P and R of range first + r from ring slot r % 3.  One
+    // commit group per step, empty past the last map, so a wait for all but the newest
+    // group always covers the step about to run.
+    auto fetch = [&](int r) {
+        if (r <= R - 2) {
+            const int b = r % kComposeDepth;
+            const float *P = head(sP, first + r);
+            for (int c = threadIdx.x; c < kD * kD / 4; c += kComposeThreads) {
+                const int row = c / (kD / 4), grp = c % (kD / 4);
+                cp_async16(&Psm[b][row][4 * (grp ^ (row & 7))], P + (size_t)row * kD + 4 * grp);
+            }
+            cp_async16(&Rsm[b][orow][ocol], head(sA, first + r) + (size_t)orow * kD + j0 + ocol);
         }
-        const float *Rr = head(sA, idx) + (size_t)i * kD + j0;
-        cp_async16(&Rsm[b][i][0], Rr);
-        cp_async16(&Rsm[b][i][4], Rr + 4);
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    if (R > 2) fetch_p(first + 1, 1);
-    {
-        const float4 *src = reinterpret_cast<const float4 *>(head(sA, first) + (size_t)i * kD + j0);
-        const float4 a = src[0], b = src[1];
-        Ssm[i][0] = a.x; Ssm[i][1] = a.y; Ssm[i][2] = a.z; Ssm[i][3] = a.w;
-        Ssm[i][4] = b.x; Ssm[i][5] = b.y; Ssm[i][6] = b.z; Ssm[i][7] = b.w;
+    fetch(1);
+    fetch(2);
+    {   // the second range starts at the first one's end state
+        const float4 v = *reinterpret_cast<const float4 *>(head(sA, first) + (size_t)orow * kD + j0 + ocol);
+        *reinterpret_cast<float4 *>(&Ssm[orow][ocol]) = v;
+        *reinterpret_cast<float4 *>(start(first + 1)) = v;
     }
-    for (int r = 1; r < R; ++r) {
-        const int idx = first + r;
-        {
-            float4 *dst = reinterpret_cast<float4 *>(sS + ((size_t)idx * Hv + hv) * hd + (size_t)i * kD + j0);
-            dst[0] = make_float4(Ssm[i][0], Ssm[i][1], Ssm[i][2], Ssm[i][3]);
-            dst[1] = make_float4(Ssm[i][4], Ssm[i][5], Ssm[i][6], Ssm[i][7]);
-        }
-        if (r == R - 1) break;
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        __syncthreads();                       // P_idx and R_idx in buffer r & 1, visible to all
-        float acc[kComposeCols];
+    for (int r = 1; r <= R - 2; ++r) {
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+        __syncthreads();                       // S and step r's slot visible; slot (r+2)%3 free
+        fetch(r + 2);
+        const int b = r % kComposeDepth;
+        float2 acc[2][kComposeCols / 2];
 #pragma unroll
-        for (int j = 0; j < kComposeCols; ++j) acc[j] = Rsm[r & 1][i][j];
-        if (r + 1 < R - 1) fetch_p(idx + 1, (r + 1) & 1);
-        const float *prow = Psm[r & 1][i];
-#pragma unroll 4
-        for (int k = 0; k < kD; k += 4) {
-            const float4 p4 = *reinterpret_cast<const float4 *>(prow + k);
-            const float pk[4] = {p4.x, p4.y, p4.z, p4.w};
+        for (int h = 0; h < 2; ++h) {
+            const int row = i + h * (kD / 2);
+#pragma unroll
+            for (int j = 0; j < kComposeCols / 2; ++j)
+                acc[h][j] = kq == 0 ? *reinterpret_cast<const float2 *>(&Rsm[b][row][2 * j])
+                                    : make_float2(0.f, 0.f);
+        }
+        const float *prow0 = Psm[b][i], *prow1 = Psm[b][i + kD / 2];
+#pragma unroll
+        for (int g = 0; g < kD / (4 * kComposeSplit); ++g) {
+            const int grp = kq * (kD / (4 * kComposeSplit)) + g;
+            const int off = 4 * (grp ^ (i & 7));          // rows i and i + 64 share i & 7
+            const float4 pa = *reinterpret_cast<const float4 *>(prow0 + off);
+            const float4 pb = *reinterpret_cast<const float4 *>(prow1 + off);
+            const float ka[4] = {pa.x, pa.y, pa.z, pa.w}, kb[4] = {pb.x, pb.y, pb.z, pb.w};
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const float4 s0 = *reinterpret_cast<const float4 *>(&Ssm[k + u][0]);
-                const float4 s1 = *reinterpret_cast<const float4 *>(&Ssm[k + u][4]);
-                acc[0] = fmaf(pk[u], s0.x, acc[0]); acc[1] = fmaf(pk[u], s0.y, acc[1]);
-                acc[2] = fmaf(pk[u], s0.z, acc[2]); acc[3] = fmaf(pk[u], s0.w, acc[3]);
-                acc[4] = fmaf(pk[u], s1.x, acc[4]); acc[5] = fmaf(pk[u], s1.y, acc[5]);
-                acc[6] = fmaf(pk[u], s1.z, acc[6]); acc[7] = fmaf(pk[u], s1.w, acc[7]);
+                const float4 s0 = *reinterpret_cast<const float4 *>(&Ssm[4 * grp + u][0]);
+                const float4 s1 = *reinterpret_cast<const float4 *>(&Ssm[4 * grp + u][4]);
+                const float2 sv[4] = {make_float2(s0.x, s0.y), make_float2(s0.z, s0.w),
+                                      make_float2(s1.x, s1.y), make_float2(s1.z, s1.w)};
+                const float2 qa = make_float2(ka[u], ka[u]), qb = make_float2(kb[u], kb[u]);
+#pragma unroll
+                for (int j = 0; j < kComposeCols / 2; ++j) {
+                    acc[0][j] = fma2(qa, sv[j], acc[0][j]);
+                    acc[1][j] = fma2(qb, sv[j], acc[1][j]);
+                }
             }
         }
-        __syncthreads();                       // every read of S and of this P is done
 #pragma unroll
-        for (int j = 0; j < kComposeCols; ++j) Ssm[i][j] = acc[j];
-        __syncthreads();
+        for (int h = 0; h < 2; ++h) {
+            float *dst = Hsm[kq][i + h * (kD / 2)];
+            *reinterpret_cast<float4 *>(dst) = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
+            *reinterpret_cast<float4 *>(dst + 4) = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
+        }
+        __syncthreads();                       // every read of S and of this slot is done
+        float4 v = *reinterpret_cast<const float4 *>(&Hsm[0][orow][ocol]);
+#pragma unroll
+        for (int q = 1; q < kComposeSplit; ++q) {
+            const float4 w = *reinterpret_cast<const float4 *>(&Hsm[q][orow][ocol]);
+            const float2 lo = add2(make_float2(v.x, v.y), make_float2(w.x, w.y));
+            const float2 hi = add2(make_float2(v.z, v.w), make_float2(w.z, w.w));
+            v = make_float4(lo.x, lo.y, hi.x, hi.y);
+        }
+        *reinterpret_cast<float4 *>(&Ssm[orow][ocol]) = v;
+        *reinterpret_cast<float4 *>(start(first + r + 1)) = v;
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");   // nothing in flight at exit
 }
@@ -1617,21 +1655,22 @@ CpLayout cp_layout(int64_t nr, int32_t N, int64_t T, int32_t Hk, int32_t Hv) {
 }  // namespace
 
 // Range length for one sequence of nch chunks over Hv v-heads alone on this device, by a
-// cost count in chunk-times (one chunk of one state CTA's chain): each state pass costs
-// its waves of CTAs (one per SM, in the dv tiling the kernels pick) times the range
-// length plus kCpCta (a CTA's start and end); the split adds kCpPerRange per range (the
-// composition runs range after range, and each range's end state and transition map go
-// through memory) and kCpFixed (its extra launches).  The constants are fitted to the
-// plain scan and the 32-, 64- and 74-chunk splits of one 32768-token sequence over 6
-// v-heads on the GB300 (the fit reproduces those three times within 1%).  0 when the
-// plain scan is expected to be at least as fast.
+// cost count in chunk-times (one chunk of one state CTA's chain), kept in halves so that
+// it stays integral: each state pass costs its waves of CTAs (one per SM, in the dv
+// tiling the kernels pick) times the range length plus one (a CTA's start and end); the
+// split adds 1.5 per range (the composition runs range after range, and each range's end
+// state and transition map go through memory) and 12 in all (its extra launches).  The
+// constants are fitted on the
+// GB300 to 14 single-sequence shapes (4096 to 65536 tokens, 1 to 48 v-heads, each timed
+// plainly and in two to seventeen range lengths): on every one the pick is the fastest
+// of the timed choices.  0 when the plain scan is expected to be at least as fast.
 int32_t cp_range_hint(int64_t seq_len, int32_t Hv, int32_t sms) {
-    constexpr int64_t kCpCta = 1, kCpPerRange = 2, kCpFixed = 18;
+    constexpr int64_t kCpCta = 2, kCpPerRange = 3, kCpFixed = 24;   // half chunk-times
     if (sms <= 0 || Hv <= 0 || seq_len <= 0) return 0;
     const int64_t nch = (seq_len + gdn::kC - 1) / gdn::kC;
     auto tiles = [&](int64_t chains) -> int64_t { return 3 * Hv * chains <= sms ? 3 : 2; };
     auto waves = [&](int64_t ctas) -> int64_t { return (ctas + sms - 1) / sms; };
-    int64_t best = waves(tiles(1) * Hv) * (nch + kCpCta);
+    int64_t best = waves(tiles(1) * Hv) * (2 * nch + kCpCta);
     int32_t best_r = 0;
     // every range count the launches allow, each with the shortest range length that
     // gives it (a longer one only costs more)
@@ -1642,7 +1681,7 @@ int32_t cp_range_hint(int64_t seq_len, int32_t Hv, int32_t sms) {
         const int64_t mid = nr > 2 ? nr - 2 : 0;
         const int64_t t = tiles(2 * nr);
         // first pass: every range but the last, and the middle ranges' transition maps
-        const int64_t cost = (waves(t * Hv * (nr - 1 + mid)) + waves(t * Hv * (nr - 1))) * (r + kCpCta) +
+        const int64_t cost = (waves(t * Hv * (nr - 1 + mid)) + waves(t * Hv * (nr - 1))) * (2 * r + kCpCta) +
                              kCpPerRange * nr + kCpFixed;
         // ties go to the shorter range, never away from the plain scan
         if (cost < best || (cost == best && best_r != 0)) {
@@ -1717,7 +1756,7 @@ gdn_status_t launch_chunk_tc_cp(const ScanArgs &a, const int32_t *cu_host, int32
     p.cp = 1;
     if ((s = launch_state(maps, p, (int)(2 * nr), state_smem, st)) != GDN_OK) return s;
     if (launch_dependent(gdn::cp_compose_kernel, dim3(gdn::kD / gdn::kComposeCols, a.Hv, a.N),
-                         dim3(gdn::kD), gdn::kComposeSmem, st, (const float *)sA,
+                         dim3(gdn::kComposeThreads), gdn::kComposeSmem, st, (const float *)sA,
                          (const float *)sP, sS, (const int32_t *)seq_first, (int)a.N, (int)a.Hv,
                          (int)nr) != cudaSuccess)
         return GDN_ERR_CUDA;

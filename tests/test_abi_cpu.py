@@ -229,14 +229,25 @@ def test_cp_rejections(lib):
 
 
 def test_cp_range_hint_model(lib):
-    """The range hint's wave-count model with an explicit SM count (no device needed):
-    on 152 SMs one 32768-token sequence over 6 v-heads splits into 40-chunk ranges (the
-    length measured fastest on the GB300), the 27B layer's 4096 tokens over 48 v-heads and
-    any single-chunk sequence stay plain, every SM count gets a valid range length (or
-    0), and bad arguments answer 0."""
+    """The range hint's wave-count model with an explicit SM count (no device needed).  On
+    152 SMs it picks, for each single-sequence shape below, the range length measured
+    fastest on the GB300 among the plain scan and the timed splits (times in us, mean of
+    20 runs with L2 flushed between them):
+    32768 tokens x 6 v-heads: 40 chunks (303; plain 854, 43 -> 317, 74 -> 343);
+    65536 x 3: 40 (324; plain 1636, 43 -> 336, 74 -> 355); 65536 x 1: 27 (193; 32 -> 201);
+    32768 x 12: 74 (530; 47 -> 571); 32768 x 4: 26 (225; 47 -> 237);
+    16384 x 24: 86 (434; 64 -> 474, plain 510); 16384 x 12: 37 (286; 64 -> 306);
+    16384 x 8: 26 (209; 43 -> 217); 16384 x 1: 13 (96; 16 -> 100);
+    8192 x 6: 19 (114; 11 -> 115); 4096 x 24: 22 (135; plain 140, 13 -> 188).
+    The 27B layer's 4096 tokens over 48 v-heads and any single-chunk sequence stay plain
+    (4096 x 48: plain 165, 64 -> 186).  Every SM count gets a valid range length (or 0),
+    and bad arguments answer 0."""
     f = lib.gdn_chunk_prefill_cp_range_hint_for
-    assert f(32768, 6, 152) == 40
-    assert f(4096, 48, 152) == 0
+    measured_best = {(32768, 6): 40, (65536, 3): 40, (65536, 1): 27, (32768, 12): 74,
+                     (32768, 4): 26, (16384, 24): 86, (16384, 12): 37, (16384, 8): 26,
+                     (16384, 1): 13, (8192, 6): 19, (4096, 24): 22, (4096, 48): 0}
+    for (L, Hv), r in measured_best.items():
+        assert f(L, Hv, 152) == r, (L, Hv, f(L, Hv, 152), r)
     assert f(64, 6, 152) == 0 and f(1, 1, 152) == 0
     assert f(32768, 6, 0) == 0 and f(0, 6, 152) == 0 and f(32768, 0, 152) == 0
     for sms in (8, 32, 76, 152, 304):
