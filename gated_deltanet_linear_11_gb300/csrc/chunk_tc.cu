@@ -67,6 +67,8 @@ struct TcMaps {
     CUtensorMap o48, o32;   // O as 48- and 32-column plain (unswizzled) boxes
 };
 
+constexpr int kStateOrderMax = 256;
+
 struct TcParams {
     const float *g, *beta;
     const int32_t *cu;
@@ -107,6 +109,11 @@ struct TcParams {
     bf16 *cs_out;            // new conv states [N][3][xc], or null
     int64_t xc;              // channels per row
     int cv0;                 // first v channel
+    // Plain scan: state CTAs take their sequences in this order (grid z -> sequence), the
+    // longest first, so that the longest chains start in the first wave rather than in the
+    // tail; n_order = 0 (more than kStateOrderMax sequences): grid z is the sequence.
+    int n_order;
+    uint16_t order[kStateOrderMax];
 };
 
 constexpr int32_t kRangeFirst = 1 << 30, kRangeLast = 1 << 29, kRangeSeq = (1 << 29) - 1;
@@ -1199,7 +1206,8 @@ __device__ __forceinline__ void state_kernel_body(const TcMaps &maps, const TcPa
         (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023));
     grid_dependents_launch();
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int jt = blockIdx.x, hv = blockIdx.y, n = blockIdx.z;
+    const int jt = blockIdx.x, hv = blockIdx.y;
+    const int n = p.cp == 0 && (int)blockIdx.z < p.n_order ? (int)p.order[blockIdx.z] : (int)blockIdx.z;
     // TMEM, barriers and tensor-map prefetches touch no memory of the previous kernel, so
     // they run before the dependency wait below
     if (warp == 0) {
@@ -1706,7 +1714,6 @@ size_t chunk_tc_cp_workspace(const int32_t *cu_host, int32_t N, int64_t T, int32
 
 gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStream_t st,
                              cudaEvent_t before_state) {
-    (void)cu_host;
     if (a.N == 0) return GDN_OK;
     if (a.out_f32) return GDN_ERR_DTYPE;
     gdn::TcMaps maps;
@@ -1714,6 +1721,16 @@ gdn_status_t launch_chunk_tc(const ScanArgs &a, const int32_t *cu_host, cudaStre
     size_t prep_smem = 0, state_smem = 0;
     gdn_status_t s = setup_scan(a, a.N, maps, p, prep_smem, state_smem);
     if (s != GDN_OK) return s;
+    // The state CTAs' sequence order: by chunk count, longest first (ties in batch order).
+    // A chain's arithmetic does not depend on when it runs, so this changes no bits.
+    if (a.N > 1 && a.N <= gdn::kStateOrderMax) {
+        int32_t idx[gdn::kStateOrderMax];
+        for (int32_t n = 0; n < a.N; ++n) idx[n] = n;
+        auto chunks = [&](int32_t n) { return ((int64_t)cu_host[n + 1] - cu_host[n] + gdn::kC - 1) / gdn::kC; };
+        std::stable_sort(idx, idx + a.N, [&](int32_t x, int32_t y) { return chunks(x) > chunks(y); });
+        p.n_order = a.N;
+        for (int32_t n = 0; n < a.N; ++n) p.order[n] = (uint16_t)idx[n];
+    }
     if ((s = launch_prep(maps, p, a.T, prep_smem, st)) != GDN_OK) return s;
     if (before_state && cudaStreamWaitEvent(st, before_state, 0) != cudaSuccess)
         return GDN_ERR_CUDA;
