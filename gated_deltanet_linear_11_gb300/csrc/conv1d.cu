@@ -16,6 +16,23 @@ namespace gdn {
 
 constexpr int kConvThreads = 128;   // threads per block, 8 channels each
 constexpr int kConvTile = 16;       // tokens per thread (anchored at the sequence start)
+constexpr int kConvGroup = 2;       // rows per commit group of the full-tile copy
+static_assert(kConvTile % kConvGroup == 0 && kConvTile / kConvGroup <= 8, "copy groups");
+
+// Wait until at most n of this thread's copy groups are still in flight (n is a constant
+// once the caller's loop is unrolled, so the switch folds to one instruction).
+__device__ __forceinline__ void cp_async_wait_upto(int n) {
+    switch (n) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+    }
+}
 
 // Channels [c_begin, c_end) of the C-wide rows.
 // grid: (ceil((c_end - c_begin) / (8*kConvThreads)), ceil(max_len / kConvTile) (>=1), N)
@@ -58,9 +75,10 @@ conv1d_fwd_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
     const int cnt = min(kConvTile, L - t0);
     if (cnt == kConvTile) {
         // Full tile: every row goes to shared memory by an asynchronous 16-byte copy at
-        // once (in two commit groups), so a CTA keeps its whole tile in flight without
-        // holding registers; each thread reads back only the slots it copied itself.
-        // Straight-line code keeps the sliding window in renamed registers.
+        // once (in commit groups of kConvGroup rows), so a CTA keeps its whole tile in
+        // flight without holding registers and starts on the first rows while the rest
+        // arrive; each thread reads back only the slots it copied itself.  Straight-line
+        // code keeps the sliding window in renamed registers.
         const bf16 *xp = x + (size_t)(start + t0) * C + c0;
         bf16 *yp = y + (size_t)(start + t0) * C + c0;
         const uint32_t slot0 = (uint32_t)__cvta_generic_to_shared(&conv_tile_buf[0][threadIdx.x]);
@@ -69,13 +87,11 @@ conv1d_fwd_kernel(const bf16 *__restrict__ x, const bf16 *__restrict__ w,
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
                          :: "r"(slot0 + (uint32_t)(i * kConvThreads * 16)), "l"(xp + (size_t)i * C)
                          : "memory");
-            if (i == kConvTile / 2 - 1 || i == kConvTile - 1)
-                asm volatile("cp.async.commit_group;" ::: "memory");
+            if (i % kConvGroup == kConvGroup - 1) asm volatile("cp.async.commit_group;" ::: "memory");
         }
 #pragma unroll
         for (int i = 0; i < kConvTile; ++i) {
-            if (i == 0) asm volatile("cp.async.wait_group 1;" ::: "memory");
-            if (i == kConvTile / 2) asm volatile("cp.async.wait_group 0;" ::: "memory");
+            if (i % kConvGroup == 0) cp_async_wait_upto(kConvTile / kConvGroup - 1 - i / kConvGroup);
             float cur[8];
             unpack8(conv_tile_buf[i][threadIdx.x], cur);
             *reinterpret_cast<uint4 *>(yp + (size_t)i * C) = conv_out(tp, win[0], win[1], win[2], cur);

@@ -287,6 +287,40 @@ def test_prefill_batch_invariance_bits(simt, lens):
         assert_bits_equal(hT[n:n + 1], h1, "state of sequence %d" % n)
 
 
+@pytest.mark.parametrize("N", [2, 256, 257])
+def test_prefill_sequence_order_changes_no_bits(N):
+    """The state pass takes up to 256 sequences longest first (a grid-order table built on
+    the host) and more in batch order.  Either way every sequence's o and final state are
+    the bits of the same sequence run alone, and reversing the batch changes nothing."""
+    rng = np.random.default_rng(N)
+    lens = [int(x) for x in rng.integers(1, 140, size=N)]
+    lens[N // 2] = 400                      # the longest sits mid-batch
+    lens[-1] = 260
+    x = inputs.scan_inputs(47, lens, 2, 4, 128, 128, init_state_std=0.02)
+    o, hT = run_prefill(x)
+    cu = x["cu_seqlens"].numpy()
+    rev = {}
+    order = list(range(N))[::-1]
+    for key in ("q", "k", "v", "g", "beta"):
+        rev[key] = torch.cat([x[key][cu[n]:cu[n + 1]] for n in order])
+    rev["cu_seqlens"] = torch.tensor(np.concatenate([[0], np.cumsum([lens[n] for n in order])]),
+                                     dtype=torch.int32)
+    rev["initial_state"] = x["initial_state"][order]
+    o_r, h_r = run_prefill(rev)
+    cu_r = rev["cu_seqlens"].numpy()
+    for j, n in enumerate(order):
+        assert_bits_equal(o_r[cu_r[j]:cu_r[j + 1]], o[cu[n]:cu[n + 1]], "o of sequence %d reversed" % n)
+        assert_bits_equal(h_r[j:j + 1], hT[n:n + 1], "state of sequence %d reversed" % n)
+    for n in sorted({0, 1, N // 2, N - 1} | set(int(i) for i in rng.integers(0, N, size=6))):
+        s0, s1 = int(cu[n]), int(cu[n + 1])
+        solo = {k: x[k][s0:s1] for k in ("q", "k", "v", "g", "beta")}
+        solo["cu_seqlens"] = torch.tensor([0, lens[n]], dtype=torch.int32)
+        solo["initial_state"] = x["initial_state"][n:n + 1]
+        o1, h1 = run_prefill(solo)
+        assert_bits_equal(o[s0:s1], o1, "o of sequence %d" % n)
+        assert_bits_equal(hT[n:n + 1], h1, "state of sequence %d" % n)
+
+
 @pytest.mark.parametrize("simt", [True, False])
 def test_prefill_continuation_split_on_chunk_multiple_is_exact(simt):
     T, tau = 333, 128
