@@ -264,7 +264,9 @@ __device__ __forceinline__ void blk_store(float (*D)[LD], int dr, int dc, int tr
 
 __device__ void tinv64_inplace(float (*AT)[kLd], float (*Y)[kLdY]) {
     const int tid = threadIdx.x;
-    const int w = tid >> 5, lane = tid & 31, tr = lane >> 2, tc = lane & 3;
+    // lane = 8 tc + tr: a half-warp's float2 stores of a block hit 2-way bank conflicts at
+    // most (4-way with lane = 4 tr + tc); the loads stay conflict-free either way
+    const int w = tid >> 5, lane = tid & 31, tr = lane & 7, tc = lane >> 3;
     {   // diagonal blocks by forward substitution, one column per thread
         const int b = (tid >> 4) & 3, j = tid & 15, o = 16 * b;
         float x[16];
