@@ -99,6 +99,7 @@ gdn_status_t gdn_conv1d_fwd(const void *x, int64_t T, int32_t C, const void *w,
                             const int32_t *cu_seqlens_host, int32_t N,
                             const void *conv_state_in, void *conv_state_out, void *y,
                             void *stream) {
+    gdn_host::CallRange nvtx_range("gdn_conv1d_fwd");
     if ((!x && T > 0) || !w || !cu_seqlens_dev || !cu_seqlens_host || (!y && T > 0))
         return GDN_ERR_NULL;
     if (N < 0 || T < 0 || C <= 0 || N > 65535) return GDN_ERR_SHAPE;
@@ -119,6 +120,7 @@ gdn_status_t gdn_conv1d_update(const void *x, int32_t N, int32_t C, const void *
                                const void *bias, void *conv_state, int32_t P,
                                const int32_t *state_idx, void *y, int32_t *status_dev,
                                void *stream) {
+    gdn_host::CallRange nvtx_range("gdn_conv1d_update");
     if (N < 0 || C <= 0 || P < 0 || N > 65535) return GDN_ERR_SHAPE;
     if (N == 0) return GDN_OK;
     if (!x || !w || !conv_state || !y) return GDN_ERR_NULL;
@@ -233,6 +235,7 @@ gdn_status_t gdn_chunk_prefill(const gdn_tensor_t *q, const gdn_tensor_t *k,
                                float scale, uint32_t flags, const float *initial_state,
                                const gdn_tensor_t *o, float *final_state, void *workspace,
                                size_t workspace_bytes, int32_t *status_dev, void *stream) {
+    gdn_host::CallRange nvtx_range("gdn_chunk_prefill");
     return chunk_prefill_impl(q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, N, chunk,
                               scale, flags, initial_state, o, final_state, workspace,
                               workspace_bytes, status_dev, stream, nullptr);
@@ -261,6 +264,7 @@ gdn_status_t gdn_chunk_prefill_cp(const gdn_tensor_t *q, const gdn_tensor_t *k,
                                   const float *initial_state, const gdn_tensor_t *o,
                                   float *final_state, void *workspace, size_t workspace_bytes,
                                   int32_t *status_dev, void *stream) {
+    gdn_host::CallRange nvtx_range("gdn_chunk_prefill_cp");
     if (range_chunks <= 0) return GDN_ERR_SHAPE;
     return chunk_prefill_impl(q, k, v, g, beta, cu_seqlens_dev, cu_seqlens_host, N, chunk,
                               scale, flags, initial_state, o, final_state, workspace,
@@ -273,6 +277,7 @@ gdn_status_t gdn_recurrent_decode(const gdn_tensor_t *q, const gdn_tensor_t *k,
                                   const int32_t *state_idx, float scale, uint32_t flags,
                                   const gdn_tensor_t *o, int32_t *status_dev,
                                   void *stream) {
+    gdn_host::CallRange nvtx_range("gdn_recurrent_decode");
     View Q, K, V, O;
     gdn_status_t s;
     if ((s = view_of(q, Q)) != GDN_OK) return s;
@@ -304,6 +309,7 @@ gdn_status_t gdn_fused_decode(const void *x, int32_t N, int32_t Hk, int32_t Hv, 
                               void *conv_state, const float *a_raw, const float *b_raw,
                               float *state, int32_t P, const int32_t *state_idx, float scale,
                               uint32_t flags, void *o, int32_t *status_dev, void *stream) {
+    gdn_host::CallRange nvtx_range("gdn_fused_decode");
     if (N < 0 || P < 0 || N > 65535 || Hk <= 0 || Hv <= 0 || Hk > 65535) return GDN_ERR_SHAPE;
     if (Hv % Hk != 0) return GDN_ERR_SHAPE;
     if (dk != 128 || dv != 128) return GDN_ERR_UNSUPPORTED;
@@ -333,6 +339,7 @@ gdn_status_t gdn_layer_prefill(const void *x, int64_t T, int32_t Hk, int32_t Hv,
                                const float *initial_state, void *o, float *final_state,
                                void *workspace, size_t workspace_bytes, int32_t *status_dev,
                                void *side_stream, void *stream) {
+    gdn_host::CallRange nvtx_range("gdn_layer_prefill");
     if (Hk <= 0 || Hv <= 0 || dk <= 0 || dv <= 0 || T < 0 || N < 0 || N > 65535)
         return GDN_ERR_SHAPE;
     const int64_t qk = (int64_t)Hk * dk, C64 = 2 * qk + (int64_t)Hv * dv;
@@ -443,6 +450,7 @@ gdn_status_t gdn_layer_prefill(const void *x, int64_t T, int32_t Hk, int32_t Hv,
 }
 
 gdn_status_t gdn_selftest_bounded_wait(int32_t *status_dev, void *stream) {
+    gdn_host::CallRange nvtx_range("gdn_selftest_bounded_wait");
     if (!status_dev) return GDN_ERR_NULL;
     return gdn_host::launch_wait_selftest(status_dev, (cudaStream_t)stream);
 }

@@ -3,6 +3,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "../../include/gdn.h"
@@ -61,6 +62,17 @@ __device__ __forceinline__ void grid_dependents_launch() {
 }  // namespace gdn
 
 namespace gdn_host {
+// One NVTX range per call of the C ABI, named after the entry point, so that a timeline
+// tool (Nsight Systems, or ncu's --nvtx filters) shows each call and the kernels it
+// launched.  The NVTX v3 header needs no library: with no tool attached, a push or pop is
+// one call through a pointer that the first use resolves.
+struct CallRange {
+    explicit CallRange(const char *name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+    CallRange(const CallRange &) = delete;
+    CallRange &operator=(const CallRange &) = delete;
+};
+
 // cudaLaunchKernelEx with programmatic stream serialization allowed.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,

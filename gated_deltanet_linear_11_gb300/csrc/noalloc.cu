@@ -47,6 +47,7 @@ extern "C" gdn_status_t gdn_chunk_prefill_noalloc(
     const float *beta, const int32_t *cu_seqlens_dev, const int32_t *cu_seqlens_host,
     int32_t N, int32_t chunk, float scale, uint32_t flags, const float *initial_state,
     const gdn_tensor_t *o, float *final_state, int32_t *status_dev, void *stream) {
+    gdn_host::CallRange nvtx_range("gdn_chunk_prefill_noalloc");
     if (!q || !v || !cu_seqlens_host) return GDN_ERR_NULL;
     if (q->ndim < 3 || q->ndim > 4 || v->ndim != q->ndim) return GDN_ERR_SHAPE;
     const int off = q->ndim - 3;

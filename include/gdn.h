@@ -24,14 +24,19 @@
  *  * v-head h reads q/k head h / (Hv / Hk).  g and beta are per v-head, fp32 [T, Hv].
  *  * Every device pointer and stream is owned by the caller.  The library allocates no
  *    device or pinned memory and keeps no global state beyond per-device cached
- *    properties (SM count, kernel attributes set once) and driver entry points.  Inputs
- *    are read-only; only the documented outputs are written.  All calls are asynchronous
- *    on `stream` (a cudaStream_t; NULL = legacy default stream) and may be issued from
- *    several host threads.
+ *    properties (SM count, kernel attributes set once), driver entry points and the
+ *    NVTX function table that the first range resolves.  Inputs are read-only; only the
+ *    documented outputs are written.  All calls are asynchronous on `stream` (a
+ *    cudaStream_t; NULL = legacy default stream) and may be issued from several host
+ *    threads.
  *  * Validation failures return before anything is launched.  Launch failures return
  *    GDN_ERR_CUDA.  Errors found on the device (an out-of-range state index) are
  *    written to the optional device int `status_dev` (0 untouched = OK), which the
  *    caller reads after synchronising; the offending item is skipped, nothing faults.
+ *  * Each entry point that validates or launches holds an NVTX range named after itself
+ *    (gdn_chunk_prefill, ...) for the duration of the host call, so timeline tools show
+ *    every call with the kernels it launched.  With no tool attached a range is a call
+ *    through a resolved pointer.
  *  * Results are batch-invariant: each sequence's outputs and states are bit-identical
  *    whatever other sequences share the launch (the reduction order of every value
  *    depends only on that sequence's own data and its position relative to its start).
