@@ -16,16 +16,26 @@ scan over the packed q||k||v channels (q, k, v are strided views of the conv out
 nothing is copied).
 
 There is no CPU fallback: without the built library every call raises.
+
+Two environment variables serve debugging and callers' failure tests, read at each call:
+
+* ``GDN_DEBUG=1`` adds ``GDN_CHECK_FINITE`` to every call that takes flags: the library
+  copies the gate inputs to the host first and fails with ``GDN_ERR_NONFINITE`` (11) on a
+  NaN or an infinity, before launching anything (it waits for the stream).
+* ``GDN_FORCE_ERROR="gdn_chunk_prefill=7,gdn_fused_decode=10"`` makes each named entry
+  raise :class:`GdnError` with that status code at once, without calling the library:
+  host-side fault injection for code that handles this package's errors.
 """
 from __future__ import annotations
 
 import ctypes
+import os
 
 import torch
 
 from . import _lib
-from ._lib import (GDN_LAYER_FUSED_VCONV, GDN_PREFILL_SIMT, GDN_PREFILL_TILES2,  # noqa: F401
-                   GDN_PREFILL_TILES3, GDN_QK_L2NORM, GdnError)
+from ._lib import (GDN_CHECK_FINITE, GDN_LAYER_FUSED_VCONV, GDN_PREFILL_SIMT,  # noqa: F401
+                   GDN_PREFILL_TILES2, GDN_PREFILL_TILES3, GDN_QK_L2NORM, GdnError)
 
 __all__ = ["gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
            "gdn_chunk_prefill_noalloc", "gdn_chunk_prefill_cp",
@@ -64,6 +74,22 @@ def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
+def _debug_flags():
+    """GDN_CHECK_FINITE when GDN_DEBUG is set (to anything but "" or "0")."""
+    return GDN_CHECK_FINITE if os.environ.get("GDN_DEBUG", "") not in ("", "0") else 0
+
+
+def _forced(name):
+    """Raise the status GDN_FORCE_ERROR assigns to entry `name`, if any."""
+    spec = os.environ.get("GDN_FORCE_ERROR", "")
+    for item in filter(None, (x.strip() for x in spec.split(","))):
+        entry, sep, code = item.partition("=")
+        if not sep or not code.strip().lstrip("-").isdigit():
+            raise ValueError("GDN_FORCE_ERROR items are name=code, got %r" % item)
+        if entry.strip() == name:
+            raise GdnError(int(code), name + " (GDN_FORCE_ERROR)")
+
+
 def _need_cuda(*ts):
     for t in ts:
         if t is not None and not t.is_cuda:
@@ -89,6 +115,7 @@ def gdn_conv1d_fwd(x, w, bias, cu_seqlens, conv_state_in=None, conv_state_out=No
     x [T, C] bf16; w [C, 4] (or [C, 1, 4]) bf16; bias [C] or None; cu_seqlens [N+1] int32;
     conv_state_in [N, 3, C] or None (zeros); conv_state_out may be conv_state_in.
     """
+    _forced("gdn_conv1d_fwd")
     lib = _lib.load()
     _need_cuda(x, w, bias, conv_state_in, conv_state_out, y)
     T, C = x.shape
@@ -108,6 +135,7 @@ def gdn_conv1d_fwd(x, w, bias, cu_seqlens, conv_state_in=None, conv_state_out=No
 
 def gdn_conv1d_update(x, w, bias, conv_state, state_idx=None, y=None, status=None):
     """One-token conv step; conv_state [P, 3, C] is shifted in place.  Returns y [N, C]."""
+    _forced("gdn_conv1d_update")
     lib = _lib.load()
     _need_cuda(x, w, bias, conv_state, state_idx, y, status)
     N, C = x.shape
@@ -146,6 +174,7 @@ def gdn_chunk_prefill(q, k, v, g, beta, cu_seqlens, chunk=64, scale=1.0, l2norm=
     tiles: None (chosen from N and the SM count), 2 or 3 dv tiles per head in the
     tensor-core state pass; the bits are the same under every choice.
     """
+    _forced("gdn_chunk_prefill")
     lib = _lib.load()
     _need_cuda(q, k, v, g, beta, initial_state, o, final_state, workspace, status)
     cu, cu_h = _seqlens(cu_seqlens, cu_seqlens_host)
@@ -157,7 +186,7 @@ def gdn_chunk_prefill(q, k, v, g, beta, cu_seqlens, chunk=64, scale=1.0, l2norm=
     if final_state is None and output_final_state:
         final_state = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=q.device)
     flags = ((GDN_QK_L2NORM if l2norm else 0) | (GDN_PREFILL_SIMT if simt else 0) |
-             _tile_flag(tiles))
+             _tile_flag(tiles) | _debug_flags())
     ws_bytes = int(lib.gdn_chunk_prefill_workspace_size(N, T, Hk, Hv, dk, dv, chunk, flags))
     if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
@@ -201,6 +230,7 @@ def gdn_chunk_prefill_cp(q, k, v, g, beta, cu_seqlens, range_chunks, chunk=64, s
     """gdn_chunk_prefill with every sequence split into ranges of ``range_chunks`` chunks
     run side by side (the context-parallel scan; tensor-core path only).  Returns
     (o, final_state)."""
+    _forced("gdn_chunk_prefill_cp")
     lib = _lib.load()
     _need_cuda(q, k, v, g, beta, initial_state, o, final_state, workspace, status)
     cu, cu_h = _seqlens(cu_seqlens, cu_seqlens_host)
@@ -211,7 +241,7 @@ def gdn_chunk_prefill_cp(q, k, v, g, beta, cu_seqlens, range_chunks, chunk=64, s
         o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
     if final_state is None and output_final_state:
         final_state = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=q.device)
-    flags = (GDN_QK_L2NORM if l2norm else 0) | _tile_flag(tiles)
+    flags = (GDN_QK_L2NORM if l2norm else 0) | _tile_flag(tiles) | _debug_flags()
     ws_bytes = int(lib.gdn_chunk_prefill_cp_workspace_size(
         ctypes.c_void_p(cu_h.data_ptr()), N, T, Hk, Hv, dk, dv, chunk, range_chunks))
     if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
@@ -235,6 +265,7 @@ def gdn_chunk_prefill_noalloc(q, k, v, g, beta, cu_seqlens, chunk=64, scale=1.0,
     still the caller's; pass ``o``/``final_state`` (and the device ``cu_seqlens``, ``g`` and
     ``beta`` as contiguous tensors) to avoid any allocation on the Python side as well.
     Returns (o, final_state)."""
+    _forced("gdn_chunk_prefill_noalloc")
     lib = _lib.load()
     _need_cuda(q, k, v, g, beta, initial_state, o, final_state, status)
     cu, cu_h = _seqlens(cu_seqlens, cu_seqlens_host)
@@ -245,7 +276,8 @@ def gdn_chunk_prefill_noalloc(q, k, v, g, beta, cu_seqlens, chunk=64, scale=1.0,
         o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
     if final_state is None and output_final_state:
         final_state = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=q.device)
-    flags = (GDN_QK_L2NORM if l2norm else 0) | (GDN_PREFILL_SIMT if simt else 0)
+    flags = ((GDN_QK_L2NORM if l2norm else 0) | (GDN_PREFILL_SIMT if simt else 0) |
+             _debug_flags())
     dq, dk_, dv_, do = _desc(q), _desc(k), _desc(v), _desc(o)
     rc = lib.gdn_chunk_prefill_noalloc(
         ctypes.byref(dq), ctypes.byref(dk_), ctypes.byref(dv_), _vp(g.contiguous()),
@@ -259,6 +291,7 @@ def gdn_chunk_prefill_noalloc(q, k, v, g, beta, cu_seqlens, chunk=64, scale=1.0,
 def gdn_recurrent_decode(q, k, v, g, beta, state, state_idx=None, scale=1.0, l2norm=False,
                          o=None, status=None):
     """One token per sequence; state [P, Hv, dk, dv] fp32 updated in place.  Returns o."""
+    _forced("gdn_recurrent_decode")
     lib = _lib.load()
     _need_cuda(q, k, v, g, beta, state, state_idx, o, status)
     if o is None:
@@ -267,7 +300,8 @@ def gdn_recurrent_decode(q, k, v, g, beta, state, state_idx=None, scale=1.0, l2n
     rc = lib.gdn_recurrent_decode(
         ctypes.byref(dq), ctypes.byref(dk_), ctypes.byref(dv_), _vp(g.contiguous()),
         _vp(beta.contiguous()), _vp(state), state.shape[0], _vp(state_idx), float(scale),
-        GDN_QK_L2NORM if l2norm else 0, ctypes.byref(do), _vp(status), _stream())
+        (GDN_QK_L2NORM if l2norm else 0) | _debug_flags(), ctypes.byref(do), _vp(status),
+        _stream())
     _lib.check(rc, "gdn_recurrent_decode")
     return o
 
@@ -278,6 +312,7 @@ def gdn_fused_decode(x_qkv, conv_w, conv_bias, a_raw, b_raw, conv_state, state, 
     place), q/k/v split, optional q/k L2 norm, beta = sigmoid(b_raw), g = -softplus(a_raw),
     recurrent step (state updated in place).  x_qkv [N, C] bf16; a_raw, b_raw [N, Hv] fp32.
     Returns o [N, Hv, dv] bf16."""
+    _forced("gdn_fused_decode")
     lib = _lib.load()
     _need_cuda(x_qkv, conv_w, conv_bias, a_raw, b_raw, conv_state, state, state_idx, o, status)
     N = x_qkv.shape[0]
@@ -289,8 +324,8 @@ def gdn_fused_decode(x_qkv, conv_w, conv_bias, a_raw, b_raw, conv_state, state, 
     rc = lib.gdn_fused_decode(
         _vp(x_qkv), N, Hk, Hv, dk, dv, _vp(conv_w), _vp(conv_bias), _vp(conv_state),
         _vp(a_raw.contiguous()), _vp(b_raw.contiguous()), _vp(state), state.shape[0],
-        _vp(state_idx), float(scale), GDN_QK_L2NORM if l2norm else 0, _vp(o), _vp(status),
-        _stream())
+        _vp(state_idx), float(scale), (GDN_QK_L2NORM if l2norm else 0) | _debug_flags(),
+        _vp(o), _vp(status), _stream())
     _lib.check(rc, "gdn_fused_decode")
     return o
 
@@ -319,6 +354,7 @@ def gdn_layer_prefill(x_qkv, conv_w, conv_bias, g, beta, cu_seqlens, Hk, Hv, dk,
 
     Returns (o [T, Hv, dv], final_state [N, Hv, dk, dv], conv_state_out [N, 3, C]).
     """
+    _forced("gdn_layer_prefill")
     if chunk != 64:
         raise ValueError("gdn_layer_prefill runs the 64-token chunk scan")
     lib = _lib.load()
@@ -340,7 +376,7 @@ def gdn_layer_prefill(x_qkv, conv_w, conv_bias, g, beta, cu_seqlens, Hk, Hv, dk,
     if final_state is None:
         final_state = torch.empty((N, Hv, dk, dv), dtype=torch.float32, device=dev)
     flags = (GDN_QK_L2NORM if l2norm else 0) | (GDN_LAYER_FUSED_VCONV if fused_vconv else 0)
-    flags |= _tile_flag(tiles)
+    flags |= _tile_flag(tiles) | _debug_flags()
     ws_bytes = int(lib.gdn_chunk_prefill_workspace_size(N, T, Hk, Hv, dk, dv, 64, flags))
     if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)

@@ -15,11 +15,13 @@ GDN_PREFILL_SIMT = 0x100
 GDN_PREFILL_TILES2 = 0x200
 GDN_PREFILL_TILES3 = 0x400
 GDN_LAYER_FUSED_VCONV = 0x800
+GDN_CHECK_FINITE = 0x1000
 
 STATUS = {
     0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_LAYOUT",
     4: "GDN_ERR_DTYPE", 5: "GDN_ERR_SEQLENS", 6: "GDN_ERR_UNSUPPORTED", 7: "GDN_ERR_CUDA",
     8: "GDN_ERR_TIMEOUT", 9: "GDN_ERR_WORKSPACE", 10: "GDN_ERR_INDEX",
+    11: "GDN_ERR_NONFINITE",
 }
 
 EXPORTS = ("gdn_status_string", "gdn_version", "gdn_conv1d_fwd", "gdn_conv1d_update",

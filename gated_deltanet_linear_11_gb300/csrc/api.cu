@@ -4,6 +4,9 @@
 // before launching anything; nothing here allocates device memory.
 #include <string.h>
 
+#include <cmath>
+#include <vector>
+
 #include "common.cuh"
 
 namespace {
@@ -59,6 +62,22 @@ gdn_status_t view_of(const gdn_tensor_t *t, View &out) {
     return GDN_OK;
 }
 
+// GDN_CHECK_FINITE: n floats at each of two device arrays, copied to the host in order on
+// `st` (waiting for it), must all be finite.
+gdn_status_t check_finite(const float *a, const float *b, size_t n, cudaStream_t st) {
+    if (n == 0) return GDN_OK;
+    std::vector<float> h(n);
+    for (const float *src : {a, b}) {
+        if (cudaMemcpyAsync(h.data(), src, n * sizeof(float), cudaMemcpyDeviceToHost, st) !=
+                cudaSuccess ||
+            cudaStreamSynchronize(st) != cudaSuccess)
+            return GDN_ERR_CUDA;
+        for (size_t i = 0; i < n; ++i)
+            if (!std::isfinite(h[i])) return GDN_ERR_NONFINITE;
+    }
+    return GDN_OK;
+}
+
 gdn_status_t check_seqlens(const int32_t *cu, int32_t N, int64_t T, int32_t *max_len) {
     if (!cu) return GDN_ERR_NULL;
     if (cu[0] != 0 || (int64_t)cu[N] != T) return GDN_ERR_SEQLENS;
@@ -88,6 +107,7 @@ const char *gdn_status_string(gdn_status_t s) {
     case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded device wait gave up";
     case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace missing or too small";
     case GDN_ERR_INDEX: return "GDN_ERR_INDEX: state index outside the pool";
+    case GDN_ERR_NONFINITE: return "GDN_ERR_NONFINITE: a gate input is NaN or infinite";
     }
     return "GDN_ERR_UNKNOWN";
 }
@@ -185,6 +205,9 @@ gdn_status_t chunk_prefill_impl(const gdn_tensor_t *q, const gdn_tensor_t *k,
         }
         return GDN_OK;
     }
+    if ((flags & GDN_CHECK_FINITE) &&
+        (s = check_finite(g, beta, (size_t)Q.T * V.H, st)) != GDN_OK)
+        return s;
 
     gdn_host::ScanArgs a;
     memset(&a, 0, sizeof(a));
@@ -292,6 +315,9 @@ gdn_status_t gdn_recurrent_decode(const gdn_tensor_t *q, const gdn_tensor_t *k,
     if (!state_idx && P < Q.T) return GDN_ERR_SHAPE;
     if (Q.dtype != K.dtype || Q.dtype != V.dtype) return GDN_ERR_DTYPE;
     if (!aligned16(state)) return GDN_ERR_LAYOUT;
+    if ((flags & GDN_CHECK_FINITE) &&
+        (s = check_finite(g, beta, (size_t)Q.T * V.H, (cudaStream_t)stream)) != GDN_OK)
+        return s;
     gdn_host::DecodeArgs a;
     memset(&a, 0, sizeof(a));
     a.q = Q.ptr; a.k = K.ptr; a.v = V.ptr; a.o = O.ptr;
@@ -321,6 +347,10 @@ gdn_status_t gdn_fused_decode(const void *x, int32_t N, int32_t Hk, int32_t Hv, 
     if (!aligned16(x) || !aligned16(conv_w) || !aligned16(conv_bias) || !aligned16(conv_state) ||
         !aligned16(state) || !aligned16(o))
         return GDN_ERR_LAYOUT;
+    if (flags & GDN_CHECK_FINITE) {
+        const gdn_status_t s = check_finite(a_raw, b_raw, (size_t)N * Hv, (cudaStream_t)stream);
+        if (s != GDN_OK) return s;
+    }
     gdn_host::FusedDecodeArgs a;
     memset(&a, 0, sizeof(a));
     a.x = x; a.w = conv_w; a.bias = conv_bias; a.conv_state = conv_state;
@@ -382,6 +412,12 @@ gdn_status_t gdn_layer_prefill(const void *x, int64_t T, int32_t Hk, int32_t Hv,
     gdn_status_t s = check_seqlens(cu_seqlens_host, N, T, &max_len);
     if (s != GDN_OK) return s;
     if ((max_len + 15) / 16 > 65535) return GDN_ERR_SHAPE;
+    if (flags & GDN_CHECK_FINITE) {
+        // before the conv launches; the scan below need not repeat it
+        if (!g || !beta) return GDN_ERR_NULL;
+        if ((s = check_finite(g, beta, (size_t)T * Hv, st)) != GDN_OK) return s;
+        flags &= ~GDN_CHECK_FINITE;
+    }
 
     if (flags & GDN_LAYER_FUSED_VCONV) {
         // the q/k channels' conv, then the scan, whose state pass convolves each V tile

@@ -288,3 +288,45 @@ def test_layer_prefill_rejections(lib):
     assert call(y=None) == 1               # nowhere to put the conv output
     assert call(cu_h=badp) == 5            # cu_seqlens[N] != T
     assert call(x=FAKE + 4) == 3           # misaligned input
+
+
+def test_forced_error_env(monkeypatch):
+    """GDN_FORCE_ERROR makes the named binding entries raise the given status at once,
+    before any argument or device check (host-side fault injection)."""
+    import torch
+    gdn = pytest.importorskip("gated_deltanet_linear_11_gb300")
+    z = torch.zeros(1)
+    monkeypatch.setenv("GDN_FORCE_ERROR", "gdn_chunk_prefill=7, gdn_fused_decode=10")
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.gdn_chunk_prefill(z, z, z, z, z, z)
+    assert e.value.code == 7 and "GDN_FORCE_ERROR" in str(e.value)
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.gdn_fused_decode(z, z, None, z, z, z, z, 1, 1, 128, 128)
+    assert e.value.code == 10
+    # entries not named run their own checks (here: CPU tensors are refused)
+    with pytest.raises(ValueError):
+        gdn.gdn_recurrent_decode(z, z, z, z, z, z)
+    monkeypatch.setenv("GDN_FORCE_ERROR", "gdn_chunk_prefill")
+    with pytest.raises(ValueError):
+        gdn.gdn_chunk_prefill(z, z, z, z, z, z)
+    monkeypatch.delenv("GDN_FORCE_ERROR")
+    with pytest.raises(ValueError):
+        gdn.gdn_chunk_prefill(z, z, z, z, z, z)
+
+
+def test_debug_env_sets_the_finite_check_flag(monkeypatch):
+    """GDN_DEBUG turns on GDN_CHECK_FINITE for every call that takes flags; the flag is a
+    bit of its own, and its status has a name."""
+    gdn = pytest.importorskip("gated_deltanet_linear_11_gb300")
+    monkeypatch.delenv("GDN_DEBUG", raising=False)
+    assert gdn._debug_flags() == 0
+    monkeypatch.setenv("GDN_DEBUG", "0")
+    assert gdn._debug_flags() == 0
+    monkeypatch.setenv("GDN_DEBUG", "1")
+    assert gdn._debug_flags() == _lib.GDN_CHECK_FINITE == 0x1000
+    others = (_lib.GDN_QK_L2NORM, _lib.GDN_PREFILL_SIMT, _lib.GDN_PREFILL_TILES2,
+              _lib.GDN_PREFILL_TILES3, _lib.GDN_LAYER_FUSED_VCONV)
+    assert all(f & _lib.GDN_CHECK_FINITE == 0 for f in others)
+    assert _lib.STATUS[11] == "GDN_ERR_NONFINITE"
+    text = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    assert "#define GDN_CHECK_FINITE 0x1000u" in text and "GDN_ERR_NONFINITE = 11" in text
