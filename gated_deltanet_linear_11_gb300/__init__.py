@@ -19,9 +19,11 @@ There is no CPU fallback: without the built library every call raises.
 
 Two environment variables serve debugging and callers' failure tests, read at each call:
 
-* ``GDN_DEBUG=1`` adds ``GDN_CHECK_FINITE`` to every call that takes flags: the library
-  copies the gate inputs to the host first and fails with ``GDN_ERR_NONFINITE`` (11) on a
-  NaN or an infinity, before launching anything (it waits for the stream).
+* ``GDN_DEBUG=1`` adds ``GDN_CHECK_INPUTS`` to every call that takes flags. Before
+  launching anything (it waits for the stream), the library copies the gate inputs to the
+  host and fails with ``GDN_ERR_NONFINITE`` (11) on a NaN or an infinity. It also fails
+  with ``GDN_ERR_SEQLENS`` (5) if a prefill's device ``cu_seqlens`` differs from its host
+  copy.
 * ``GDN_FORCE_ERROR="gdn_chunk_prefill=7,gdn_fused_decode=10"`` makes each named entry
   raise :class:`GdnError` with that status code at once, without calling the library:
   host-side fault injection for code that handles this package's errors.
@@ -34,7 +36,7 @@ import os
 import torch
 
 from . import _lib
-from ._lib import (GDN_CHECK_FINITE, GDN_LAYER_FUSED_VCONV, GDN_PREFILL_SIMT,  # noqa: F401
+from ._lib import (GDN_CHECK_INPUTS, GDN_LAYER_FUSED_VCONV, GDN_PREFILL_SIMT,  # noqa: F401
                    GDN_PREFILL_TILES2, GDN_PREFILL_TILES3, GDN_QK_L2NORM, GdnError)
 
 __all__ = ["gdn_conv1d_fwd", "gdn_conv1d_update", "gdn_chunk_prefill",
@@ -75,8 +77,8 @@ def _stream():
 
 
 def _debug_flags():
-    """GDN_CHECK_FINITE when GDN_DEBUG is set (to anything but "" or "0")."""
-    return GDN_CHECK_FINITE if os.environ.get("GDN_DEBUG", "") not in ("", "0") else 0
+    """GDN_CHECK_INPUTS when GDN_DEBUG is set (to anything but "" or "0")."""
+    return GDN_CHECK_INPUTS if os.environ.get("GDN_DEBUG", "") not in ("", "0") else 0
 
 
 def _forced(name):

@@ -15,7 +15,7 @@ GDN_PREFILL_SIMT = 0x100
 GDN_PREFILL_TILES2 = 0x200
 GDN_PREFILL_TILES3 = 0x400
 GDN_LAYER_FUSED_VCONV = 0x800
-GDN_CHECK_FINITE = 0x1000
+GDN_CHECK_INPUTS = 0x1000
 
 STATUS = {
     0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_LAYOUT",

@@ -62,7 +62,7 @@ gdn_status_t view_of(const gdn_tensor_t *t, View &out) {
     return GDN_OK;
 }
 
-// GDN_CHECK_FINITE: n floats at each of two device arrays, copied to the host in order on
+// GDN_CHECK_INPUTS: n floats at each of two device arrays, copied to the host in order on
 // `st` (waiting for it), must all be finite.
 gdn_status_t check_finite(const float *a, const float *b, size_t n, cudaStream_t st) {
     if (n == 0) return GDN_OK;
@@ -76,6 +76,18 @@ gdn_status_t check_finite(const float *a, const float *b, size_t n, cudaStream_t
             if (!std::isfinite(h[i])) return GDN_ERR_NONFINITE;
     }
     return GDN_OK;
+}
+
+// GDN_CHECK_INPUTS: the device offsets, copied back on `st` (waiting for it), must equal
+// the host copy that was validated.
+gdn_status_t check_seqlens_copy(const int32_t *cu_dev, const int32_t *cu_host, int32_t N,
+                                cudaStream_t st) {
+    std::vector<int32_t> h((size_t)N + 1);
+    if (cudaMemcpyAsync(h.data(), cu_dev, h.size() * sizeof(int32_t), cudaMemcpyDeviceToHost,
+                        st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    return memcmp(h.data(), cu_host, h.size() * sizeof(int32_t)) == 0 ? GDN_OK : GDN_ERR_SEQLENS;
 }
 
 gdn_status_t check_seqlens(const int32_t *cu, int32_t N, int64_t T, int32_t *max_len) {
@@ -205,8 +217,9 @@ gdn_status_t chunk_prefill_impl(const gdn_tensor_t *q, const gdn_tensor_t *k,
         }
         return GDN_OK;
     }
-    if ((flags & GDN_CHECK_FINITE) &&
-        (s = check_finite(g, beta, (size_t)Q.T * V.H, st)) != GDN_OK)
+    if ((flags & GDN_CHECK_INPUTS) &&
+        ((s = check_finite(g, beta, (size_t)Q.T * V.H, st)) != GDN_OK ||
+         (s = check_seqlens_copy(cu_seqlens_dev, cu_seqlens_host, N, st)) != GDN_OK))
         return s;
 
     gdn_host::ScanArgs a;
@@ -315,7 +328,7 @@ gdn_status_t gdn_recurrent_decode(const gdn_tensor_t *q, const gdn_tensor_t *k,
     if (!state_idx && P < Q.T) return GDN_ERR_SHAPE;
     if (Q.dtype != K.dtype || Q.dtype != V.dtype) return GDN_ERR_DTYPE;
     if (!aligned16(state)) return GDN_ERR_LAYOUT;
-    if ((flags & GDN_CHECK_FINITE) &&
+    if ((flags & GDN_CHECK_INPUTS) &&
         (s = check_finite(g, beta, (size_t)Q.T * V.H, (cudaStream_t)stream)) != GDN_OK)
         return s;
     gdn_host::DecodeArgs a;
@@ -347,7 +360,7 @@ gdn_status_t gdn_fused_decode(const void *x, int32_t N, int32_t Hk, int32_t Hv, 
     if (!aligned16(x) || !aligned16(conv_w) || !aligned16(conv_bias) || !aligned16(conv_state) ||
         !aligned16(state) || !aligned16(o))
         return GDN_ERR_LAYOUT;
-    if (flags & GDN_CHECK_FINITE) {
+    if (flags & GDN_CHECK_INPUTS) {
         const gdn_status_t s = check_finite(a_raw, b_raw, (size_t)N * Hv, (cudaStream_t)stream);
         if (s != GDN_OK) return s;
     }
@@ -412,11 +425,13 @@ gdn_status_t gdn_layer_prefill(const void *x, int64_t T, int32_t Hk, int32_t Hv,
     gdn_status_t s = check_seqlens(cu_seqlens_host, N, T, &max_len);
     if (s != GDN_OK) return s;
     if ((max_len + 15) / 16 > 65535) return GDN_ERR_SHAPE;
-    if (flags & GDN_CHECK_FINITE) {
+    if (flags & GDN_CHECK_INPUTS) {
         // before the conv launches; the scan below need not repeat it
         if (!g || !beta) return GDN_ERR_NULL;
-        if ((s = check_finite(g, beta, (size_t)T * Hv, st)) != GDN_OK) return s;
-        flags &= ~GDN_CHECK_FINITE;
+        if ((s = check_finite(g, beta, (size_t)T * Hv, st)) != GDN_OK ||
+            (s = check_seqlens_copy(cu_seqlens_dev, cu_seqlens_host, N, st)) != GDN_OK)
+            return s;
+        flags &= ~GDN_CHECK_INPUTS;
     }
 
     if (flags & GDN_LAYER_FUSED_VCONV) {

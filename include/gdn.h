@@ -63,7 +63,7 @@ typedef enum {
     GDN_ERR_TIMEOUT = 8,     /* a bounded device-side wait gave up (device status) */
     GDN_ERR_WORKSPACE = 9,   /* workspace missing, too small or misaligned */
     GDN_ERR_INDEX = 10,      /* a state index outside [0, P) (device status) */
-    GDN_ERR_NONFINITE = 11   /* GDN_CHECK_FINITE: a gate input holds a NaN or an infinity */
+    GDN_ERR_NONFINITE = 11   /* GDN_CHECK_INPUTS: a gate input is a NaN or an infinity */
 } gdn_status_t;
 
 typedef enum { GDN_BF16 = 0, GDN_F32 = 1, GDN_I32 = 2 } gdn_dtype_t;
@@ -81,15 +81,18 @@ typedef struct {
 
 /* Flags */
 #define GDN_QK_L2NORM 0x1u /* normalise q and k per head: x / sqrt(sum x^2 + 1e-6) */
-/* Debug check of the gate inputs (the entries that take flags: the prefills, the decodes
- * and the layer entry).  Before anything is launched the call copies g and beta (for
- * gdn_fused_decode the logits a_raw and b_raw) to pageable host memory, waiting for
- * `stream`, and returns GDN_ERR_NONFINITE if any value is a NaN or an infinity.  The
- * recurrence multiplies the state by e^g at every token, so one bad gate ruins every later
- * state of its sequence ("Qwen3.5-27B GPTQ Garbage Inference -- Root Cause Analysis",
- * "Why abliteration failed on Qwen3.5", item 3).  It synchronises the stream: not for use
- * under stream capture or on a latency-critical path. */
-#define GDN_CHECK_FINITE 0x1000u
+/* Debug checks of the inputs (the entries that take flags: the prefills, the decodes and
+ * the layer entry), run on the host before anything is launched, waiting for `stream`:
+ *  - the gate inputs (g and beta; for gdn_fused_decode the logits a_raw and b_raw) are
+ *    copied to pageable host memory, and a NaN or an infinity returns GDN_ERR_NONFINITE.
+ *    The recurrence multiplies the state by e^g at every token, so one bad gate ruins
+ *    every later state of its sequence ("Qwen3.5-27B GPTQ Garbage Inference -- Root Cause
+ *    Analysis", "Why abliteration failed on Qwen3.5", item 3);
+ *  - the prefills' device cu_seqlens is copied back and must equal the host copy, else
+ *    GDN_ERR_SEQLENS (the kernels index the packed batch by the device copy).
+ * It synchronises the stream: not for use under stream capture or on a latency-critical
+ * path. */
+#define GDN_CHECK_INPUTS 0x1000u
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *gdn_status_string(gdn_status_t s);

@@ -315,7 +315,7 @@ def test_forced_error_env(monkeypatch):
 
 
 def test_debug_env_sets_the_finite_check_flag(monkeypatch):
-    """GDN_DEBUG turns on GDN_CHECK_FINITE for every call that takes flags; the flag is a
+    """GDN_DEBUG turns on GDN_CHECK_INPUTS for every call that takes flags; the flag is a
     bit of its own, and its status has a name."""
     gdn = pytest.importorskip("gated_deltanet_linear_11_gb300")
     monkeypatch.delenv("GDN_DEBUG", raising=False)
@@ -323,10 +323,10 @@ def test_debug_env_sets_the_finite_check_flag(monkeypatch):
     monkeypatch.setenv("GDN_DEBUG", "0")
     assert gdn._debug_flags() == 0
     monkeypatch.setenv("GDN_DEBUG", "1")
-    assert gdn._debug_flags() == _lib.GDN_CHECK_FINITE == 0x1000
+    assert gdn._debug_flags() == _lib.GDN_CHECK_INPUTS == 0x1000
     others = (_lib.GDN_QK_L2NORM, _lib.GDN_PREFILL_SIMT, _lib.GDN_PREFILL_TILES2,
               _lib.GDN_PREFILL_TILES3, _lib.GDN_LAYER_FUSED_VCONV)
-    assert all(f & _lib.GDN_CHECK_FINITE == 0 for f in others)
+    assert all(f & _lib.GDN_CHECK_INPUTS == 0 for f in others)
     assert _lib.STATUS[11] == "GDN_ERR_NONFINITE"
     text = open(os.path.join(ROOT, "include", "gdn.h")).read()
-    assert "#define GDN_CHECK_FINITE 0x1000u" in text and "GDN_ERR_NONFINITE = 11" in text
+    assert "#define GDN_CHECK_INPUTS 0x1000u" in text and "GDN_ERR_NONFINITE = 11" in text

@@ -3,8 +3,9 @@
 Every mbarrier wait of the tensor-core kernels gives up after 2 s, records
 GDN_ERR_TIMEOUT in the caller's status word and lets the CTA return.  The self-test entry
 runs that path on a barrier phase that nothing completes; the context must stay usable
-afterwards.  The debug check of the gate inputs (GDN_CHECK_FINITE, set by GDN_DEBUG) must
-reject a NaN or an infinity before anything is launched.
+afterwards.  The debug checks of the inputs (GDN_CHECK_INPUTS, set by GDN_DEBUG) must
+reject a NaN or an infinity among the gates, and device offsets that differ from the
+host copy, before anything is launched.
 """
 import time
 
@@ -54,9 +55,10 @@ def test_bounded_wait_reports_timeout_and_the_context_stays_usable():
     assert_state_close(hT, h_ref)
 
 
-# ------------------------------------------------------- GDN_CHECK_FINITE (debug mode)
+# ------------------------------------------------------- GDN_CHECK_INPUTS (debug mode)
 
 GDN_ERR_NONFINITE = 11
+GDN_ERR_SEQLENS = 5
 
 
 def _same(a, b):
@@ -66,7 +68,8 @@ def _same(a, b):
 
 def test_check_finite_prefill(monkeypatch):
     """With GDN_DEBUG set, a NaN in g or an infinity in beta fails the call with
-    GDN_ERR_NONFINITE before anything is launched (o and the final state keep their
+    GDN_ERR_NONFINITE, and a device cu_seqlens that differs from the host copy with
+    GDN_ERR_SEQLENS, before anything is launched (o and the final state keep their
     sentinels); finite gates give the bits of the unchecked call."""
     x = inputs.scan_inputs(53, [70, 130], 2, 4, 128, 128, init_state_std=0.02)
     xg = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
@@ -96,6 +99,20 @@ def test_check_finite_prefill(monkeypatch):
     g_bad[150, 3] = float("nan")
     beta_bad = xg["beta"].clone()
     beta_bad[5, 0] = float("inf")
+    # a device cu_seqlens that disagrees with the host copy is refused before any launch
+    # (the call below runs only with the check on: no kernel ever sees these offsets)
+    cu_bad = xg["cu_seqlens"].clone()
+    cu_bad[1] += 64
+    o, hT = fresh()
+    o0, h0 = o.clone(), hT.clone()
+    assert gdn._debug_flags() == gdn.GDN_CHECK_INPUTS
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.gdn_chunk_prefill(xg["q"], xg["k"], xg["v"], xg["g"], xg["beta"], cu_bad, o=o,
+                              final_state=hT, initial_state=xg["initial_state"],
+                              cu_seqlens_host=cu_h)
+    assert e.value.code == GDN_ERR_SEQLENS
+    torch.cuda.synchronize()
+    assert _same(o, o0) and _same(hT, h0)
     for g, beta, cp in ((g_bad, xg["beta"], False), (xg["g"], beta_bad, False),
                         (g_bad, xg["beta"], True)):
         o, hT = fresh()
