@@ -76,19 +76,26 @@ def decode_bytes(N, Hk, Hv, dk, dv, C):
 
 
 def kernel_traffic(src_name):
-    """DRAM bytes per launch (read + write) from the last ncu capture of a kernel file,
-    if that capture was taken from the current source (matched by sha1), else None."""
+    """DRAM bytes per launch (read + write) from the last ncu capture of a kernel file, if
+    that capture was taken from the current sources, else None.  The record lists the
+    files whose device code the kernel compiles from (the .cu file and the headers it
+    takes device code from); it holds the sha1 of their contents, concatenated in that
+    order."""
     import hashlib
-    src = os.path.join(ROOT, "gated_deltanet_linear_11_gb300", "csrc", src_name)
+    csrc = os.path.join(ROOT, "gated_deltanet_linear_11_gb300", "csrc")
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
-        with open(src, "rb") as f:
-            digest = hashlib.sha1(f.read()).hexdigest()
         with open(path) as f:
             rec = json.load(f).get(src_name)
+        if not rec:
+            return None
+        h = hashlib.sha1()
+        for name in rec.get("sources", [src_name]):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("sha1") != digest:
+    if rec.get("sha1") != h.hexdigest():
         return None
     return rec.get("dram_bytes_per_launch")
 

@@ -31,9 +31,17 @@ __device__ __forceinline__ uint4 pack8(const float f[8]) {
     return u;
 }
 
-// SiLU with the fast exponential and divide intrinsics: the result is rounded to bf16,
-// whose unit roundoff (2^-9) is far above the intrinsics' error.
-__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+// SiLU z / (1 + e^-z), with e^-z = 2^(-z log2 e) on the hardware base-2 exponential
+// (ex2.approx, relative error about 2^-22) and the fast divide: the result is rounded to
+// bf16, whose unit roundoff (2^-9) is far above either error.  For z below about -88,
+// e^-z overflows to infinity and the result is a signed zero (the exact value is under
+// 1e-36 in magnitude).
+__device__ __forceinline__ float silu(float z) {
+    constexpr float kMinusLog2e = -1.4426950408889634f;
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(z * kMinusLog2e));
+    return __fdividef(z, 1.0f + e);
+}
 
 template <typename T> __device__ __forceinline__ float to_f32(T x);
 template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }

@@ -1,12 +1,16 @@
 """bench.py's bookkeeping, on the CPU: the algorithmic work the rooflines divide by, and
-the e2e leg's piece schedule.
+the e2e leg's piece schedule, and the DRAM-traffic records it reports.
 
 The figures are the ones the measurement notes state for the 27B layer (T = 4096,
 Hk = 16, Hv = 48, dk = dv = 128, 10240 conv channels) and the 256-sequence decode step.
 """
+import os
+
 import pytest
 
 import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 S = dict(Hk=16, Hv=48, dk=128, dv=128)
 
@@ -51,3 +55,22 @@ def test_e2e_pieces_cover_the_sequence_in_chunk_multiples():
     top = pieces.index(max(pieces))
     assert pieces[-1] == min(pieces)
     assert pieces[top:] == sorted(pieces[top:], reverse=True)
+
+
+def test_traffic_records_match_their_sources():
+    """Each DRAM-traffic record in profiles/ncu_traffic.json lists the files its kernel's
+    device code comes from and their sha1; the bench reports a record only while they
+    match, so a committed record must match the committed sources."""
+    import hashlib
+    import json
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    recs = json.load(open(path))
+    assert set(recs) >= {"chunk_tc.cu", "conv1d.cu", "decode.cu"}
+    for name, rec in recs.items():
+        h = hashlib.sha1()
+        for src in rec.get("sources", [name]):
+            h.update(open(os.path.join(ROOT, "gated_deltanet_linear_11_gb300", "csrc", src),
+                          "rb").read())
+        assert rec["sha1"] == h.hexdigest(), name
+        assert rec["dram_bytes_per_launch"] > 0
+        assert bench.kernel_traffic(name) == rec["dram_bytes_per_launch"]

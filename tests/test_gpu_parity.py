@@ -60,6 +60,38 @@ def test_conv1d_fwd_in_place_state_and_empty_sequence():
     np.testing.assert_array_equal(np64(st), sr)
 
 
+def test_conv_silu_over_the_bf16_range():
+    """The conv's SiLU against the fp64 definition z / (1 + e^-z) on every finite bf16
+    value with |z| <= 120: a conv whose only tap is the newest input (w = [0, 0, 0, 1],
+    no bias) outputs silu(x) rounded to bf16, which must be within one bf16 unit in the
+    last place of the exactly rounded value, or within 1e-30 where that value is tiny
+    (below z = -87 the exponential overflows and the kernel returns a signed zero)."""
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    vals = (bits << 16).view(np.float32)
+    z = vals[np.isfinite(vals) & (np.abs(vals) <= 120.0)]
+    C = 1024
+    T = -(-z.size // C)
+    x = np.zeros(T * C, dtype=np.float32)
+    x[:z.size] = z
+    xt = torch.from_numpy(x.reshape(T, C)).to(torch.bfloat16)
+    assert np.array_equal(xt.float().numpy().ravel()[:z.size], z)   # exact bf16 values
+    w = torch.zeros(C, 4, dtype=torch.bfloat16)
+    w[:, 3] = 1.0
+    cu = torch.tensor([0, T], dtype=torch.int32)
+    y, _ = gdn.gdn_conv1d_fwd(xt.cuda(), w.cuda(), None, cu.cuda(), cu_seqlens_host=cu)
+    got = y.float().cpu().numpy().ravel()[:z.size].astype(np.float64)
+    zd = z.astype(np.float64)
+    with np.errstate(over="ignore"):
+        exact = zd / (1.0 + np.exp(-zd))
+    ref = torch.from_numpy(exact).to(torch.bfloat16).double().numpy()   # round to nearest
+    r32 = ref.astype(np.float32)
+    ulp = 65536.0 * np.maximum(np.abs(np.nextafter(r32, np.float32(np.inf)) - ref),
+                               np.abs(np.nextafter(r32, np.float32(-np.inf)) - ref))
+    err = np.abs(got - ref)
+    bad = ~((err <= ulp) | (err <= 1e-30))
+    assert not bad.any(), (z[bad][:8], got[bad][:8], ref[bad][:8])
+
+
 def test_conv1d_update_matches_oracle_and_prefill_bits():
     N, P, C = 12, 20, 1024
     d = inputs.conv_inputs(23, [1] * N, C, with_state=True, with_bias=True)
